@@ -1,0 +1,199 @@
+"""Python binding of liblynx.so, the RT-Lynx 2:4 activation-sparse linear layer.
+
+Argument marshalling only: every step of the layer runs in the library's CUDA
+kernels.  PyTorch supplies device memory and the current stream.  There is no
+CPU path; importing this package on a machine where the library cannot be
+loaded raises.
+
+Names and arguments follow ``include/lynx.h``.  Tensors are bf16 CUDA tensors
+(``torch.bfloat16``) laid out row-major; ``s`` is float32.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from ._build import LIB, build, up_to_date
+
+__all__ = [
+    "LynxError", "lib", "LYNX_OK", "LYNX_ERR_TIMEOUT",
+    "lynx_meta_bytes", "lynx_workspace_bytes", "lynx_dense_workspace_bytes",
+    "lynx_sparsify", "lynx_lora_down", "lynx_linear", "lynx_linear_dense",
+    "lynx_sync_status", "lynx_status_string", "lynx_meta_to_canonical", "lynx_debug_set_fault",
+    "lynx_profile_next",
+]
+
+LYNX_OK = 0
+LYNX_ERR_TIMEOUT = -6
+
+_c_i64, _c_sz, _c_p = ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB) or (os.environ.get("LYNX_AUTOBUILD", "1") == "1" and not up_to_date()):
+        build()
+    L = ctypes.CDLL(LIB)
+    sig = {
+        "lynx_meta_bytes": (_c_sz, [_c_i64, _c_i64]),
+        "lynx_workspace_bytes": (_c_sz, [_c_i64, _c_i64, _c_i64, _c_i64]),
+        "lynx_dense_workspace_bytes": (_c_sz, [_c_i64, _c_i64]),
+        "lynx_sparsify": (ctypes.c_int, [_c_p, _c_i64, _c_i64, _c_p, _c_p, _c_p, _c_p]),
+        "lynx_lora_down": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_p]),
+        "lynx_linear": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_i64, _c_p, _c_sz, _c_p]),
+        "lynx_linear_dense": (ctypes.c_int,
+                              [_c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_i64, _c_p, _c_sz, _c_p]),
+        "lynx_sync_status": (ctypes.c_int, [_c_p]),
+        "lynx_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+        "lynx_meta_to_canonical": (ctypes.c_int, [_c_p, _c_p, _c_i64, _c_i64]),
+        "lynx_debug_set_fault": (None, [ctypes.c_int, ctypes.c_uint64]),
+        "lynx_profile_next": (None, [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(L, name)
+        f.restype, f.argtypes = res, args
+    return L
+
+
+lib = _load()
+
+
+class LynxError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {lib.lynx_status_string(status).decode()} (status {status})")
+
+
+def _check(status: int, where: str) -> None:
+    if status != LYNX_OK:
+        raise LynxError(status, where)
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream=None) -> int | None:
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _need(t, name, dtype=None, shape=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def lynx_meta_bytes(M: int, K: int) -> int:
+    return lib.lynx_meta_bytes(M, K)
+
+
+def lynx_workspace_bytes(M: int, N: int, K: int, R: int = 64) -> int:
+    return lib.lynx_workspace_bytes(M, N, K, R)
+
+
+def lynx_dense_workspace_bytes(M: int, R: int = 64) -> int:
+    return lib.lynx_dense_workspace_bytes(M, R)
+
+
+def lynx_sparsify(X, vals=None, meta=None, s=None, stream=None):
+    """Compressed 2:4 values (M x K/2 bf16), metadata (uint8, lynx_meta_bytes) and s (M fp32)."""
+    torch = _torch()
+    _need(X, "X", torch.bfloat16)
+    M, K = X.shape
+    vals = torch.empty((M, K // 2), dtype=torch.bfloat16, device=X.device) if vals is None else vals
+    meta = torch.empty(lynx_meta_bytes(M, K), dtype=torch.uint8, device=X.device) if meta is None else meta
+    s = torch.empty(M, dtype=torch.float32, device=X.device) if s is None else s
+    _check(lib.lynx_sparsify(_ptr(X), M, K, _ptr(vals), _ptr(meta), _ptr(s), _stream(stream)), "lynx_sparsify")
+    return vals, meta, s
+
+
+def lynx_lora_down(X, LB, s=None, T=None, stream=None):
+    """T = bf16(X LB^T / s) (s=None: no division); M x R bf16."""
+    torch = _torch()
+    _need(X, "X", torch.bfloat16)
+    _need(LB, "LB", torch.bfloat16)
+    M, K = X.shape
+    R = LB.shape[0]
+    T = torch.empty((M, R), dtype=torch.bfloat16, device=X.device) if T is None else T
+    _check(lib.lynx_lora_down(_ptr(X), _ptr(LB), _ptr(s), _ptr(T), M, K, R, _stream(stream)), "lynx_lora_down")
+    return T
+
+
+def lynx_linear(X, W, LA, LB, Y=None, workspace=None, stream=None):
+    """Y = bf16(s * (X~ W^T) + (X LB^T) LA^T), the RT-Lynx sparse linear."""
+    torch = _torch()
+    for t, n in ((X, "X"), (W, "W"), (LA, "LA"), (LB, "LB")):
+        _need(t, n, torch.bfloat16)
+    M, K = X.shape
+    N = W.shape[0]
+    R = LB.shape[0]
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device) if Y is None else Y
+    need = lynx_workspace_bytes(M, N, K, R)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=X.device)
+    _check(lib.lynx_linear(_ptr(X), _ptr(W), _ptr(LA), _ptr(LB), _ptr(Y), M, N, K, R, _ptr(workspace),
+                           workspace.numel() * workspace.element_size(), _stream(stream)), "lynx_linear")
+    return Y
+
+
+def lynx_linear_dense(X, W, LA=None, LB=None, Y=None, workspace=None, stream=None):
+    """Y = bf16(X W^T [+ (X LB^T) LA^T]): a selectively skipped layer."""
+    torch = _torch()
+    _need(X, "X", torch.bfloat16)
+    _need(W, "W", torch.bfloat16)
+    M, K = X.shape
+    N = W.shape[0]
+    R = 0 if LB is None else LB.shape[0]
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device) if Y is None else Y
+    if LA is not None and workspace is None:
+        workspace = torch.empty(lynx_dense_workspace_bytes(M, R), dtype=torch.uint8, device=X.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.lynx_linear_dense(_ptr(X), _ptr(W), _ptr(LA), _ptr(LB), _ptr(Y), M, N, K, R, _ptr(workspace), wbytes,
+                                 _stream(stream)), "lynx_linear_dense")
+    return Y
+
+
+def lynx_sync_status(stream=None) -> int:
+    return lib.lynx_sync_status(_stream(stream))
+
+
+def lynx_status_string(status: int) -> str:
+    return lib.lynx_status_string(status).decode()
+
+
+def lynx_meta_to_canonical(meta_host, M: int, K: int):
+    """Host conversion of the tensor-core metadata layout to canonical M x K/8 bytes (numpy uint8)."""
+    import numpy as np
+    src = np.ascontiguousarray(meta_host, dtype=np.uint8)
+    out = np.empty((M, K // 8), dtype=np.uint8)
+    _check(lib.lynx_meta_to_canonical(src.ctypes.data, out.ctypes.data, M, K), "lynx_meta_to_canonical")
+    return out
+
+
+def lynx_profile_next(events) -> None:
+    """Have the next lynx_linear / lynx_linear_dense call on this thread record ``events``
+    (torch.cuda.Event objects, already created) around its kernels."""
+    handles = [e.cuda_event for e in events]
+    if any(h == 0 for h in handles):
+        raise ValueError("record each event once before passing it (torch creates events lazily)")
+    arr = (ctypes.c_void_p * len(handles))(*handles)
+    _profile_keepalive[:] = [arr]
+    lib.lynx_profile_next(arr, len(handles))
+
+
+_profile_keepalive: list = []
+
+
+def lynx_debug_set_fault(inject: int, wait_ns: int = 0) -> None:
+    lib.lynx_debug_set_fault(inject, wait_ns)

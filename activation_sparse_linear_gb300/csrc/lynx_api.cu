@@ -1,0 +1,341 @@
+// C-ABI of the RT-Lynx activation-sparse linear layer: argument checks, tensor
+// maps, workspace carving, kernel launches and the device error word.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/lynx.h"
+#include "kernels.h"
+
+namespace lynx {
+namespace {
+
+constexpr int64_t kMaxM = 65535LL * 128;  // grid.y limit of the GEMM
+constexpr int64_t kMaxN = 1LL << 24;
+constexpr int64_t kMaxK = 1LL << 20;
+constexpr int kRank = 64;
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+
+__device__ int g_error_word;
+
+std::atomic<int> g_inject{0};
+thread_local void* const* t_prof_events = nullptr;
+thread_local int t_prof_count = 0;
+
+// Consumes the stage-timing request of this thread (see lynx_profile_next).
+struct StageEvents {
+  void* const* ev = nullptr;
+  int n = 0;
+  StageEvents(int expected) {
+    if (t_prof_events && t_prof_count == expected) {
+      ev = t_prof_events;
+      n = expected;
+    }
+    t_prof_events = nullptr;
+    t_prof_count = 0;
+  }
+  cudaError_t mark(int i, cudaStream_t st) const {
+    if (!ev || i >= n) return cudaSuccess;
+    return cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), st);
+  }
+};
+std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
+
+int* error_word_ptr() {
+  static int* ptrs[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> g(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<int*>(p);
+  }
+  return ptrs[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [rows x cols] array with row stride `ld` elements.
+bool make_map(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows, uint64_t ld, uint32_t box_cols,
+              uint32_t box_rows, CUtensorMapSwizzle swz) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {ld * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) != 0; }
+
+int check_mk(int64_t M, int64_t K) {
+  if (M < 1 || M > kMaxM || K < 16 || K > kMaxK || K % 16 != 0) return LYNX_ERR_SHAPE;
+  return LYNX_OK;
+}
+
+DevCtl make_ctl() {
+  DevCtl c;
+  c.err = error_word_ptr();
+  c.wait_ns = g_wait_ns.load();
+  c.inject = g_inject.load();
+  return c;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? LYNX_OK : LYNX_ERR_CUDA; }
+
+struct Workspace {
+  void* vals;
+  void* meta;
+  float* s;
+  void* T;
+  size_t bytes;
+};
+
+size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
+
+Workspace carve(void* base, int64_t M, int64_t K, int64_t R) {
+  Workspace w{};
+  const uintptr_t b = reinterpret_cast<uintptr_t>(base);
+  size_t off = 0;
+  w.vals = reinterpret_cast<void*>(b + off);
+  off += align256(static_cast<size_t>(M) * static_cast<size_t>(K));  // M x K/2 bf16
+  w.meta = reinterpret_cast<void*>(b + off);
+  off += align256(static_cast<size_t>(meta_bytes(M, K)));
+  w.s = reinterpret_cast<float*>(b + off);
+  off += align256(static_cast<size_t>(M) * 4);
+  w.T = reinterpret_cast<void*>(b + off);
+  off += align256(static_cast<size_t>(M) * static_cast<size_t>(R) * 2);
+  w.bytes = off;
+  return w;
+}
+
+// T = X LB^T [/ s] on the 64-wide tcgen05 tile.
+int run_lora_down(const void* X, const void* LB, const float* s, void* T, int64_t M, int64_t K, cudaStream_t st) {
+  GemmArgs g;
+  std::memset(&g, 0, sizeof(g));
+  if (!make_map(&g.tmA, X, K, M, K, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) return LYNX_ERR_CUDA;
+  if (!make_map(&g.tmB, LB, K, kRank, K, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)) return LYNX_ERR_CUDA;
+  g.tmT = g.tmA;
+  g.tmLA = g.tmB;
+  g.meta = nullptr;
+  g.rowscale = s;
+  g.scale_mode = s ? SCALE_DIV : SCALE_NONE;
+  g.Y = T;
+  g.ldy = kRank;
+  g.M = static_cast<int>(M);
+  g.N = kRank;
+  g.K = static_cast<int>(K);
+  g.ctl = make_ctl();
+  return cuda_status(launch_gemm(4, g, st));
+}
+
+}  // namespace
+}  // namespace lynx
+
+using namespace lynx;
+
+extern "C" {
+
+size_t lynx_meta_bytes(int64_t M, int64_t K) {
+  if (M < 1 || K < 1) return 0;
+  return static_cast<size_t>(meta_bytes(M, K));
+}
+
+size_t lynx_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t R) {
+  (void)N;
+  if (M < 1 || K < 1 || R < 0) return 0;
+  return carve(nullptr, M, K, R).bytes;
+}
+
+size_t lynx_dense_workspace_bytes(int64_t M, int64_t R) {
+  if (M < 1 || R < 0) return 0;
+  return align256(static_cast<size_t>(M) * static_cast<size_t>(R) * 2);
+}
+
+int lynx_sparsify(const void* X, int64_t M, int64_t K, void* vals, void* meta, float* s, void* stream) {
+  if (!X || !vals || !meta || !s) return LYNX_ERR_NULL;
+  if (int e = check_mk(M, K)) return e;
+  if (misaligned(X) || misaligned(vals) || misaligned(meta) || misaligned(s)) return LYNX_ERR_ALIGN;
+  return cuda_status(launch_sparsify(X, static_cast<int>(M), static_cast<int>(K), vals, meta, s,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+int lynx_lora_down(const void* X, const void* LB, const float* s, void* T, int64_t M, int64_t K, int64_t R,
+                   void* stream) {
+  if (!X || !LB || !T) return LYNX_ERR_NULL;
+  if (int e = check_mk(M, K)) return e;
+  if (R != kRank) return R < 1 ? LYNX_ERR_SHAPE : LYNX_ERR_UNSUPPORTED;
+  if (misaligned(X) || misaligned(LB) || misaligned(T) || (s && (reinterpret_cast<uintptr_t>(s) & 3)))
+    return LYNX_ERR_ALIGN;
+  return run_lora_down(X, LB, s, T, M, K, static_cast<cudaStream_t>(stream));
+}
+
+int lynx_linear(const void* X, const void* W, const void* LA, const void* LB, void* Y, int64_t M, int64_t N,
+                int64_t K, int64_t R, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!X || !W || !LA || !LB || !Y || !workspace) return LYNX_ERR_NULL;
+  if (int e = check_mk(M, K)) return e;
+  if (N < 1 || N > kMaxN) return LYNX_ERR_SHAPE;
+  if (R != kRank) return R < 1 ? LYNX_ERR_SHAPE : LYNX_ERR_UNSUPPORTED;
+  if (misaligned(X) || misaligned(W) || misaligned(LA) || misaligned(LB) || misaligned(Y) || misaligned(workspace))
+    return LYNX_ERR_ALIGN;
+  Workspace ws = carve(workspace, M, K, R);
+  if (workspace_bytes < ws.bytes) return LYNX_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  GemmArgs g;
+  std::memset(&g, 0, sizeof(g));
+  if (!make_map(&g.tmA, ws.vals, K / 2, M, K / 2, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !make_map(&g.tmB, W, K, N, K, 64, 256, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&g.tmT, ws.T, R, M, R, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&g.tmLA, LA, R, N, R, 64, 256, CU_TENSOR_MAP_SWIZZLE_128B))
+    return LYNX_ERR_CUDA;
+  g.meta = static_cast<const uint8_t*>(ws.meta);
+  g.rowscale = ws.s;
+  g.scale_mode = SCALE_MUL;
+  g.Y = Y;
+  g.ldy = N;
+  g.M = static_cast<int>(M);
+  g.N = static_cast<int>(N);
+  g.K = static_cast<int>(K);
+  g.ctl = make_ctl();
+
+  StageEvents prof(4);
+  if (cudaError_t e = prof.mark(0, st)) return cuda_status(e);
+  if (cudaError_t e = launch_sparsify(X, static_cast<int>(M), static_cast<int>(K), ws.vals, ws.meta, ws.s, st))
+    return cuda_status(e);
+  if (cudaError_t e = prof.mark(1, st)) return cuda_status(e);
+  if (int e = run_lora_down(X, LB, ws.s, ws.T, M, K, st)) return e;
+  if (cudaError_t e = prof.mark(2, st)) return cuda_status(e);
+  if (cudaError_t e = launch_gemm(2, g, st)) return cuda_status(e);
+  return cuda_status(prof.mark(3, st));
+}
+
+int lynx_linear_dense(const void* X, const void* W, const void* LA, const void* LB, void* Y, int64_t M,
+                      int64_t N, int64_t K, int64_t R, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!X || !W || !Y) return LYNX_ERR_NULL;
+  const bool lora = LA || LB;
+  if (lora && (!LA || !LB || !workspace)) return LYNX_ERR_NULL;
+  if (int e = check_mk(M, K)) return e;
+  if (N < 1 || N > kMaxN) return LYNX_ERR_SHAPE;
+  if (lora && R != kRank) return R < 1 ? LYNX_ERR_SHAPE : LYNX_ERR_UNSUPPORTED;
+  if (misaligned(X) || misaligned(W) || misaligned(Y) ||
+      (lora && (misaligned(LA) || misaligned(LB) || misaligned(workspace))))
+    return LYNX_ERR_ALIGN;
+  if (lora && workspace_bytes < lynx_dense_workspace_bytes(M, R)) return LYNX_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  GemmArgs g;
+  std::memset(&g, 0, sizeof(g));
+  if (!make_map(&g.tmA, X, K, M, K, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&g.tmB, W, K, N, K, 64, 256, CU_TENSOR_MAP_SWIZZLE_128B))
+    return LYNX_ERR_CUDA;
+  if (lora) {
+    if (!make_map(&g.tmT, workspace, R, M, R, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&g.tmLA, LA, R, N, R, 64, 256, CU_TENSOR_MAP_SWIZZLE_128B))
+      return LYNX_ERR_CUDA;
+  } else {
+    g.tmT = g.tmA;
+    g.tmLA = g.tmB;
+  }
+  g.meta = nullptr;
+  g.rowscale = nullptr;
+  g.scale_mode = SCALE_NONE;
+  g.Y = Y;
+  g.ldy = N;
+  g.M = static_cast<int>(M);
+  g.N = static_cast<int>(N);
+  g.K = static_cast<int>(K);
+  g.ctl = make_ctl();
+  StageEvents prof(lora ? 3 : 2);
+  if (cudaError_t e = prof.mark(0, st)) return cuda_status(e);
+  if (lora) {
+    if (int e = run_lora_down(X, LB, nullptr, workspace, M, K, st)) return e;
+    if (cudaError_t e = prof.mark(1, st)) return cuda_status(e);
+    if (cudaError_t e = launch_gemm(1, g, st)) return cuda_status(e);
+    return cuda_status(prof.mark(2, st));
+  }
+  if (cudaError_t e = launch_gemm(0, g, st)) return cuda_status(e);
+  return cuda_status(prof.mark(1, st));
+}
+
+int lynx_sync_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return LYNX_ERR_CUDA;
+  int* p = error_word_ptr();
+  if (!p) return LYNX_ERR_CUDA;
+  int h = 0;
+  if (cudaMemcpy(&h, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return LYNX_ERR_CUDA;
+  if (h != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return LYNX_ERR_CUDA;
+    return LYNX_ERR_TIMEOUT;
+  }
+  return LYNX_OK;
+}
+
+const char* lynx_status_string(int status) {
+  switch (status) {
+    case LYNX_OK: return "ok";
+    case LYNX_ERR_NULL: return "null pointer argument";
+    case LYNX_ERR_SHAPE: return "shape out of range (M,N >= 1; K >= 16, K % 16 == 0)";
+    case LYNX_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case LYNX_ERR_WORKSPACE: return "workspace too small";
+    case LYNX_ERR_CUDA: return "CUDA call failed";
+    case LYNX_ERR_TIMEOUT: return "device-side wait timed out";
+    case LYNX_ERR_UNSUPPORTED: return "unsupported configuration (LoRA rank must be 64)";
+    default: return "unknown status";
+  }
+}
+
+int lynx_meta_to_canonical(const void* meta, uint8_t* canonical, int64_t M, int64_t K) {
+  if (!meta || !canonical) return LYNX_ERR_NULL;
+  if (M < 1 || K < 8 || K % 8 != 0) return LYNX_ERR_SHAPE;
+  const uint8_t* base = static_cast<const uint8_t*>(meta);
+  const int64_t chunks_k = meta_chunks_k(K);
+  for (int64_t m = 0; m < M; ++m) {
+    uint8_t* out = canonical + m * (K / 8);
+    for (int64_t c = 0; c * kMetaChunkCols < K; ++c) {
+      uint16_t lo, hi;
+      std::memcpy(&lo, base + meta_half_offset(m, c, 0, chunks_k), 2);
+      std::memcpy(&hi, base + meta_half_offset(m, c, 1, chunks_k), 2);
+      const uint32_t word = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+      for (int j = 0; j < 4 && c * kMetaChunkCols + 8 * j < K; ++j)  // byte j of the word = channels 8j..8j+7
+        out[c * 4 + j] = static_cast<uint8_t>(word >> (8 * j));
+    }
+  }
+  return LYNX_OK;
+}
+
+void lynx_profile_next(void* const* events, int count) {
+  t_prof_events = events;
+  t_prof_count = count;
+}
+
+void lynx_debug_set_fault(int inject, uint64_t wait_ns) {
+  g_inject.store(inject);
+  g_wait_ns.store(wait_ns ? wait_ns : kDefaultWaitNs);
+}
+
+}  // extern "C"

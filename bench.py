@@ -1,0 +1,383 @@
+"""Throughput of the RT-Lynx 2:4 activation-sparse linear on the attention QKV
+projection of a single-stream DiT at 1024 px: X 4608 x 3072 bf16 (4096 image +
+512 text tokens), W 9216 x 3072, rank-64 LoRA.
+
+A step is one lynx_linear call: sparsify, LoRA down-projection, and the fused
+tcgen05 2:4-sparse GEMM with the LoRA-up accumulation and the s epilogue.
+The metric is effective TFLOP/s = 2 M N K / step time.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on
+bounded row samples of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = ("qkv", "qkv")
+METRIC = "effective TFLOP/s (2MNK) of fused sparse linear; % of sparse BF16 peak; x vs dense"
+ROTATE = 4          # device copies of the inputs, cycled so that each step reads cold (L2-evicted) data
+FALLBACK_PEAKS = {"hbm_gbs": 6682.8, "bf16_tflops": 1967.9, "bf16_tflops_sustained": 1755.1,
+                  "source": "pool measurement recorded before this run (STREAM copy, cuBLAS bf16 8192^3)"}
+
+
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        d.setdefault("source", "MEASURED_PEAKS.json")
+        return d
+    return dict(FALLBACK_PEAKS)
+
+
+def peak_value(peaks: dict, *names, default=None):
+    for n in names:
+        for k, v in peaks.items():
+            if k == n and isinstance(v, (int, float)):
+                return float(v)
+    return default
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- CPU oracle legs
+def oracle_rows_rate(t: dict, rows_per_call: int, budget_s: float, max_calls: int | None = None):
+    """Time the oracle on consecutive row samples; returns (TFLOP/s, rows, seconds, calls)."""
+    import oracle.lynx_oracle as O
+    M, N, K = t["M"], t["N"], t["K"]
+    done_rows, calls, t0 = 0, 0, time.perf_counter()
+    while True:
+        r0 = (calls * rows_per_call) % M
+        rows = np.arange(r0, min(r0 + rows_per_call, M))
+        O.linear(t["X"], t["W"], t["LA"], t["LB"], rows=rows)
+        done_rows += len(rows)
+        calls += 1
+        el = time.perf_counter() - t0
+        if (max_calls is not None and calls >= max_calls) or (max_calls is None and el >= budget_s):
+            break
+    return 2.0 * done_rows * N * K / el / 1e12, done_rows, el, calls
+
+
+def cpu_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n and n[0]:
+            return int(n[0])
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def run_reference(args) -> int:
+    """The oracle as it stands, on the host cores: each step is a bounded row sample."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import synth
+    t = synth.layer_tensors(*WORKLOAD)
+    rows = 64
+    oracle_rows_rate(t, rows, 0, max_calls=max(1, args.warmup))  # warm-up
+    times = []
+    for i in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_rows_rate(t, rows, 0, max_calls=1)
+        times.append(time.perf_counter() - t0)
+    step_s = sum(times) / len(times)
+    value = 2.0 * rows * t["N"] * t["K"] / step_s / 1e12
+    cores = cpu_threads()
+    sample = f"{rows} of {t['M']} rows per step (QKV 4608x3072 -> 9216, rank 64), float64 numpy oracle"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(t, "reference"),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_dict(t, impl="lynx"):
+    return {"workload": "attention QKV projection, single-stream DiT 1024px: X 4608x3072 bf16 "
+                        "(4096 image + 512 text tokens, N(0,1), 3% outlier channels x10), W 9216x3072 "
+                        "N(0,1/3072), LoRA rank 64 N(0,0.02), seeded",
+            "M": t["M"], "N": t["N"], "K": t["K"], "R": t["R"],
+            "l2": f"inputs rotated over {ROTATE} device copies (> L2) so every step reads L2-cold data"
+            if impl != "reference" else "n/a (host)"}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def main() -> int:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="lynx", choices=["lynx", "reference"])
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    import activation_sparse_linear_gb300 as asl
+    import synth
+
+    t = synth.layer_tensors(*WORKLOAD)
+    M, N, K, R = t["M"], t["N"], t["K"], t["R"]
+    dev = torch.device("cuda", local)
+
+    def to_dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    base = {k: to_dev(t[k]) for k in ("X", "W", "LA", "LB")}
+    sets = []
+    for i in range(ROTATE):
+        sets.append({
+            "X": base["X"].clone(), "W": base["W"].clone(), "LA": base["LA"].clone(), "LB": base["LB"].clone(),
+            "Y": torch.empty((M, N), dtype=torch.bfloat16, device=dev),
+            "ws": torch.empty(asl.lynx_workspace_bytes(M, N, K, R), dtype=torch.uint8, device=dev),
+        })
+    del base
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    L = asl.lib
+
+    def call(s):
+        return L.lynx_linear(s["X"].data_ptr(), s["W"].data_ptr(), s["LA"].data_ptr(), s["LB"].data_ptr(),
+                             s["Y"].data_ptr(), M, N, K, R, s["ws"].data_ptr(), s["ws"].numel(), sp)
+
+    # warm-up
+    for i in range(args.warmup):
+        assert call(sets[i % ROTATE]) == 0
+    st = asl.lynx_sync_status()
+    assert st == 0, asl.lynx_status_string(st)
+
+    # per-stage events, created up front (torch creates events lazily on first record)
+    nev = 4
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
+    for row in evs:
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
+    import ctypes
+    ev_arrays = [(ctypes.c_void_p * nev)(*[e.cuda_event for e in row]) for row in evs]
+
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0]) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_index) as clk:
+        t_start.record(stream)
+        for i in range(args.steps):
+            L.lynx_profile_next(ev_arrays[i], nev)
+            if call(sets[i % ROTATE]) != 0:
+                raise RuntimeError("lynx_linear failed")
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    st = asl.lynx_sync_status()
+    assert st == 0, asl.lynx_status_string(st)
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
+    ms_per_step = elapsed_ms / args.steps
+    flops = 2.0 * M * N * K
+    value = flops * args.steps * world / (elapsed_ms * 1e-3) / 1e12
+
+    stage_ms = np.array([[row[j].elapsed_time(row[j + 1]) for j in range(nev - 1)] for row in evs])
+    stage_avg = stage_ms.mean(axis=0)  # sparsify, lora_down, sparse GEMM
+
+    peaks = load_peaks()
+    dense_tf = peak_value(peaks, "bf16_tflops", "bf16_tflops_burst", default=1967.9)
+    hbm = peak_value(peaks, "hbm_gbs", "hbm_GBps", default=6682.8)
+    sparse_peak = 2.0 * dense_tf
+    gemm_flops = 2.0 * M * N * K + 2.0 * M * N * R  # sparse branch (dense-equivalent) + LoRA-up
+    gemm_tf = gemm_flops / (stage_avg[2] * 1e-3) / 1e12
+    sparsify_bytes = M * K * 2 + M * K + M * K / 8 + M * 4
+    sparsify_gbs = sparsify_bytes / (stage_avg[0] * 1e-3) / 1e9
+    lora_bytes = M * K * 2 + R * K * 2 + M * R * 2 + M * 4
+    lora_gbs = lora_bytes / (stage_avg[1] * 1e-3) / 1e9
+
+    # dense cuBLAS at the same shape, same rotation, same stream
+    for i in range(args.warmup):
+        torch.matmul(sets[i % ROTATE]["X"], sets[i % ROTATE]["W"].t(), out=sets[i % ROTATE]["Y"])
+    nd = min(args.steps, 500)
+    torch.cuda.synchronize()
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    d0.record(stream)
+    for i in range(nd):
+        s = sets[i % ROTATE]
+        torch.matmul(s["X"], s["W"].t(), out=s["Y"])
+    d1.record(stream)
+    torch.cuda.synchronize()
+    dense_ms = d0.elapsed_time(d1) / nd
+
+    # end to end through the C-ABI with host buffers: H2D of X, the layer, D2H of Y
+    Xh = torch.empty((M, K), dtype=torch.bfloat16, pin_memory=True)
+    Xh.copy_(sets[0]["X"].cpu())
+    Yh = torch.empty((M, N), dtype=torch.bfloat16, pin_memory=True)
+    ne = min(args.steps, 100)
+    for i in range(3):
+        s = sets[i % ROTATE]
+        s["X"].copy_(Xh, non_blocking=True)
+        call(s)
+        Yh.copy_(s["Y"], non_blocking=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(ne):
+        s = sets[i % ROTATE]
+        s["X"].copy_(Xh, non_blocking=True)
+        assert call(s) == 0
+        Yh.copy_(s["Y"], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / ne
+    e2e_value = flops * world / (e2e_ms * 1e-3) / 1e12
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return 0
+
+    # CPU baseline: the oracle on a bounded row sample, ~10 s
+    cpu_tf, cpu_rows, cpu_s, _ = oracle_rows_rate(t, 64, 10.0)
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_dict(t),
+        "roofline": {"bound": "tensor", "achieved": gemm_tf, "peak": sparse_peak, "unit": "TFLOP/s",
+                     "frac": gemm_tf / sparse_peak, "traffic": None,
+                     "kernel": "sparse GEMM + LoRA-up + s epilogue (tcgen05.mma.sp)",
+                     "peak_source": f"2 x dense bf16 burst {dense_tf} TFLOP/s (nominal 2:4 ratio), {peaks['source']}"},
+        "cpu_baseline": {"value": cpu_tf, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
+                         "sample": f"{cpu_rows} rows of the QKV workload in {cpu_s:.1f} s (float64 numpy oracle)"},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": M * K * 2,
+                "d2h_bytes_per_step": M * N * 2, "ms_per_step": e2e_ms,
+                "note": "pinned host X -> device, lynx_linear, Y -> pinned host; weights resident"},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+        "detail": {
+            "stage_ms": {"sparsify": stage_avg[0], "lora_down": stage_avg[1], "sparse_gemm": stage_avg[2]},
+            "sparse_gemm_pct_of_sparse_peak": 100.0 * gemm_tf / sparse_peak,
+            "step_pct_of_sparse_peak": 100.0 * (value / world) / sparse_peak,
+            "sparsify_GBs": sparsify_gbs, "sparsify_frac_hbm": sparsify_gbs / hbm,
+            "lora_down_GBs": lora_gbs, "lora_down_frac_hbm": lora_gbs / hbm,
+            "dense_cublas_ms": dense_ms, "dense_cublas_tflops": flops / (dense_ms * 1e-3) / 1e12,
+            "x_vs_dense_cublas": dense_ms / ms_per_step,
+            "hbm_peak_GBs": hbm, "dense_bf16_peak_tflops": dense_tf,
+        },
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

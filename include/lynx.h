@@ -1,0 +1,148 @@
+/*
+ * lynx.h -- C ABI of the RT-Lynx 2:4 activation-sparse linear layer (sm_103a).
+ *
+ * The layer (RT-Lynx page, aitrends.kr article 60737, Method / Code examples):
+ *
+ *     Y = S(X) W^T + X (LA LB)^T,     S(X) = s * X~,
+ *     X~ = the two largest-|x| entries of every 4 consecutive input channels of
+ *          each token row (ties to the lower channel index),
+ *     s  = ||X||_2 / ||X~||_2 per row (s = 1 when X~ is all zero),
+ *
+ * with a rank-R (R = 64) LoRA branch on the dense X.
+ *
+ * Conventions shared by every entry point:
+ *   - Matrices are row-major device arrays of bf16 (stored as 16-bit words)
+ *     unless stated: X is M x K, W is N x K (nn.Linear layout), LA is N x R,
+ *     LB is R x K, Y is M x N.  Every pointer must be 16-byte aligned.
+ *   - K must be a positive multiple of 16; M and N are any value >= 1;
+ *     R must be 64 wherever a LoRA branch is computed.
+ *   - All memory is owned by the caller.  The library allocates nothing;
+ *     scratch space is passed in as `workspace`.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
+ *     call only enqueues work and returns; results are ready when the stream
+ *     is.
+ *   - Return value: LYNX_OK or a negative lynx_status.  Argument errors are
+ *     detected on the host and returned before anything is enqueued.
+ *     Device-side failures (a bounded wait that ran out) are recorded in a
+ *     device error word and returned by lynx_sync_status.
+ *   - No entry point aborts the process or traps on the device.
+ */
+#ifndef LYNX_H_
+#define LYNX_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define LYNX_API __attribute__((visibility("default")))
+#else
+#define LYNX_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LYNX_OK = 0,
+  LYNX_ERR_NULL = -1,        /* a required pointer is NULL */
+  LYNX_ERR_SHAPE = -2,       /* M, N, K or R out of range, or K % 16 != 0 */
+  LYNX_ERR_ALIGN = -3,       /* a pointer is not 16-byte aligned */
+  LYNX_ERR_WORKSPACE = -4,   /* workspace smaller than lynx_*workspace_bytes() */
+  LYNX_ERR_CUDA = -5,        /* a CUDA runtime/driver call failed */
+  LYNX_ERR_TIMEOUT = -6,     /* a device-side bounded wait ran out */
+  LYNX_ERR_UNSUPPORTED = -7  /* valid but not implemented (R != 64) */
+} lynx_status;
+
+/* Bytes of 2:4 metadata for an M x K activation:
+ *     ceil(M/128) * (ceil(K/64)*64/32) * 2048.
+ * Layout (the one the sparse GEMM copies into tensor memory): one 2 KiB chunk
+ * per (128-row block, 32-channel chunk), row blocks outermost.  A chunk holds
+ * 128 lanes of 16 bytes; only the first little-endian 32-bit word of a lane
+ * is metadata (the other 12 bytes are never written).  A row's 32-bit word
+ * carries group g (channels 4g..4g+3 of the chunk) in bits 4g..4g+3 as
+ * i0 | (i1 << 2), i0 < i1 the kept positions.  Inside each 16-row block the
+ * words of rows r and r+8 are stored by 16-bit halves: lane 16b+i (i < 8)
+ * holds the low halves of rows 16b+i (bits 0-15) and 16b+8+i (bits 16-31),
+ * lane 16b+8+i their high halves -- the order in which tcgen05.mma.sp reads
+ * metadata from tensor memory.  Padding rows and channels (up to multiples
+ * of 128 and 64) hold the pattern of an all-zero group (0x4). */
+LYNX_API size_t lynx_meta_bytes(int64_t M, int64_t K);
+
+/* Workspace bytes needed by lynx_linear: compressed values, metadata, s and
+ * the M x R LoRA intermediate, each 256-byte aligned. */
+LYNX_API size_t lynx_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t R);
+
+/* Workspace bytes needed by lynx_linear_dense when a LoRA branch is given
+ * (the M x R intermediate X LB^T); 0 suffices without LoRA. */
+LYNX_API size_t lynx_dense_workspace_bytes(int64_t M, int64_t R);
+
+/* Online 2:4 sparsification: S(X) in the form the sparse tensor core consumes.
+ * (RT-Lynx page, Method: Top-K based 2:4 activation selection, done online,
+ * handed to the kernel in the sparse-tensor-core format; Code examples,
+ * first formula for s.)
+ *   X    [in]  M x K bf16.
+ *   vals [out] M x K/2 bf16: the two kept entries of each group, lower index first.
+ *   meta [out] lynx_meta_bytes(M, K) bytes, layout above.
+ *   s    [out] M fp32: ||X_m|| / ||X~_m|| (1 for a row whose kept entries are zero).
+ * The values are copies of the inputs; s is applied later, by the GEMM epilogue. */
+LYNX_API int lynx_sparsify(const void* X, int64_t M, int64_t K, void* vals, void* meta, float* s, void* stream);
+
+/* LoRA down-projection of the dense activation:
+ *   T[m, r] = bf16( sum_k X[m,k] LB[r,k] / s[m] )      (s == NULL: no division)
+ *   X [in] M x K, LB [in] R x K, s [in] M fp32 or NULL, T [out] M x R bf16; R = 64.
+ * (RT-Lynx page, Method: Yr = X (LA LB)^T; the division by s lets the fused
+ * epilogue scale the whole accumulator by s.) */
+LYNX_API int lynx_lora_down(const void* X, const void* LB, const float* s, void* T, int64_t M, int64_t K, int64_t R,
+                   void* stream);
+
+/* The full RT-Lynx sparse linear: Y = bf16( s * (X~ W^T) + (X LB^T) LA^T ).
+ *   X [in] M x K, W [in] N x K, LA [in] N x R, LB [in] R x K, Y [out] M x N bf16.
+ *   workspace: >= lynx_workspace_bytes(M, N, K, R) bytes of device memory,
+ *   16-byte aligned, not shared with a concurrent call.
+ * Enqueues three kernels: sparsify, LoRA down-projection, and the tcgen05
+ * 2:4-sparse GEMM whose extra K-steps accumulate T' LA^T into the same
+ * tensor-memory accumulator, with s applied in the epilogue.
+ * (RT-Lynx page, Method and CUDA kernel optimisation.) */
+LYNX_API int lynx_linear(const void* X, const void* W, const void* LA, const void* LB, void* Y, int64_t M, int64_t N,
+                int64_t K, int64_t R, void* workspace, size_t workspace_bytes, void* stream);
+
+/* A selectively skipped (dense) layer: Y = bf16( X W^T [+ (X LB^T) LA^T] ).
+ * LA and LB are both NULL (no LoRA) or both given (then R = 64 and the
+ * workspace must hold lynx_dense_workspace_bytes(M, R) bytes).
+ * (RT-Lynx page, Method: Selective Layer Skipping.) */
+LYNX_API int lynx_linear_dense(const void* X, const void* W, const void* LA, const void* LB, void* Y, int64_t M,
+                      int64_t N, int64_t K, int64_t R, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Waits for `stream`, then reads and clears the device error word of the
+ * current device.  Returns LYNX_OK, LYNX_ERR_TIMEOUT or LYNX_ERR_CUDA. */
+LYNX_API int lynx_sync_status(void* stream);
+
+/* Static, human-readable text of a status code. */
+LYNX_API const char* lynx_status_string(int status);
+
+/* Host-side helper: converts metadata in the layout above (a host copy of
+ * lynx_meta_bytes(M, K) bytes) to the canonical row-major M x K/8 bytes,
+ * byte j = nibble(group 2j) | nibble(group 2j+1) << 4.  K % 8 == 0. */
+LYNX_API int lynx_meta_to_canonical(const void* meta, uint8_t* canonical, int64_t M, int64_t K);
+
+/* Stage-timing hook.  The next lynx_linear or lynx_linear_dense call made
+ * from this host thread records events[0] on its stream before its first
+ * kernel and events[i] right after its i-th kernel; count must be the number
+ * of kernels + 1 (4 for lynx_linear: sparsify, LoRA down-projection, sparse
+ * GEMM; 3 for lynx_linear_dense with LoRA, 2 without).  The events are
+ * cudaEvent_t handles owned by the caller.  The setting is used by that one
+ * call and then cleared; a count that does not match is ignored. */
+LYNX_API void lynx_profile_next(void* const* events, int count);
+
+/* Test hook.  inject = 1 makes the next GEMM launches never deliver their
+ * first pipeline stage, so their bounded waits run out after wait_ns
+ * nanoseconds and lynx_sync_status reports LYNX_ERR_TIMEOUT.  inject = 0
+ * restores normal operation; wait_ns = 0 restores the default bound (2 s). */
+LYNX_API void lynx_debug_set_fault(int inject, uint64_t wait_ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LYNX_H_ */

@@ -36,7 +36,7 @@ import numpy as np
 
 __all__ = [
     "widen", "select_2of4", "keep_mask", "norm_scale", "sparsify", "canonical_meta",
-    "linear", "linear_dense", "NIBBLE_OF_PAIR",
+    "linear", "linear_dense", "lora_down", "NIBBLE_OF_PAIR",
 ]
 
 #: 4-bit metadata of a kept index pair (i0 < i1): i0 in bits 0-1, i1 in bits 2-3.
@@ -139,6 +139,19 @@ def linear(X, W, LA, LB, rows=None) -> np.ndarray:
     ys = s[:, None] * (xt @ w.T)
     yr = (x @ widen(LB).T) @ widen(LA).T
     return ys + yr
+
+
+def lora_down(X, LB, s=None) -> np.ndarray:
+    """First factor of the LoRA branch Yr = X (LA LB)^T = (X LB^T) LA^T, divided by s when given.
+
+    RT-Lynx page, Method.  Dividing by the row scale s of the sparse branch
+    lets Ys and Yr share one accumulator that is scaled by s at the end:
+    s * (X~ W^T + (X LB^T / s) LA^T) = Ys + Yr.
+    """
+    t = widen(X) @ widen(LB).T
+    if s is not None:
+        t = t / np.asarray(s, dtype=np.float64)[:, None]
+    return t
 
 
 def linear_dense(X, W, LA=None, LB=None, rows=None) -> np.ndarray:

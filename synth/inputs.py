@@ -77,8 +77,10 @@ def act_bf16(key: tuple, M: int, K: int, frac: float, scale: float,
 
 
 def _gelu(z: np.ndarray) -> np.ndarray:
+    """Exact-erf GELU in float32 (the result is rounded to bf16 afterwards)."""
     from scipy.special import erf
-    return (0.5 * z * (1.0 + erf(z / math.sqrt(2.0)))).astype(np.float32)
+    z = z.astype(np.float32, copy=False)
+    return np.float32(0.5) * z * (np.float32(1.0) + erf(z * np.float32(1.0 / math.sqrt(2.0))))
 
 
 def gelu_bf16(key: tuple, M: int, K: int, pre_var: float, frac: float, scale: float,
@@ -92,7 +94,7 @@ def gelu_bf16(key: tuple, M: int, K: int, pre_var: float, frac: float, scale: fl
     step = 1 << 20
     flat_in, flat_out = z.reshape(-1), out.reshape(-1)
     for i in range(0, flat_in.size, step):  # chunked to bound temporaries
-        flat_out[i:i + step] = _gelu(flat_in[i:i + step].astype(np.float64))
+        flat_out[i:i + step] = _gelu(flat_in[i:i + step])
     return bf16_bits(out)
 
 

@@ -1,0 +1,117 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol that
+include/lynx.h declares, and rejects bad arguments on the host before it
+touches the device.  The metadata layout helper is checked against the layout
+the header documents, re-derived here in Python."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "lynx.h")
+
+
+@pytest.fixture(scope="module")
+def asl():
+    import activation_sparse_linear_gb300 as asl
+    return asl
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"LYNX_API\s+[\w\s\*]+?\b(lynx_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    for name in ("lynx_sparsify", "lynx_linear", "lynx_linear_dense", "lynx_sync_status", "lynx_meta_bytes",
+                 "lynx_workspace_bytes"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(asl):
+    for name in declared_symbols():
+        assert hasattr(asl.lib, name), name
+        assert ctypes.cast(getattr(asl.lib, name), ctypes.c_void_p).value
+
+
+def test_no_cpu_fallback_in_package():
+    pkg = os.path.join(ROOT, "activation_sparse_linear_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in src.replace("the oracle", ""), f
+
+
+def test_sizes(asl):
+    # one 2 KiB chunk per (128-row block, 32-channel chunk); channels padded to 64
+    assert asl.lynx_meta_bytes(4608, 3072) == 36 * 96 * 2048
+    assert asl.lynx_meta_bytes(1, 16) == 1 * 2 * 2048
+    assert asl.lynx_meta_bytes(129, 130) == 2 * 6 * 2048
+    ws = asl.lynx_workspace_bytes(4608, 9216, 3072, 64)
+    assert ws >= 4608 * 3072 + 36 * 96 * 2048 + 4608 * 4 + 4608 * 64 * 2
+    assert asl.lynx_dense_workspace_bytes(100, 64) >= 100 * 64 * 2
+
+
+A = 1 << 20  # a fake, 16-byte aligned address: never dereferenced by the host checks below
+
+
+@pytest.mark.parametrize("args,status", [
+    ((0, A, A, A, A, 16, 16, 16, 64, A, 1 << 30), -1),            # null X
+    ((A, A, A, A, A, 16, 16, 24, 64, A, 1 << 30), -2),            # K % 16
+    ((A, A, A, A, A, 0, 16, 16, 64, A, 1 << 30), -2),             # M = 0
+    ((A, A, A, A, A, 16, 0, 16, 64, A, 1 << 30), -2),             # N = 0
+    ((A, A, A, A, A, 16, 16, 16, 32, A, 1 << 30), -7),            # R != 64
+    ((A + 8, A, A, A, A, 16, 16, 16, 64, A, 1 << 30), -3),        # misaligned X
+    ((A, A, A, A, A + 2, 16, 16, 16, 64, A, 1 << 30), -3),        # misaligned Y
+    ((A, A, A, A, A, 16, 16, 16, 64, A, 100), -4),                # workspace too small
+])
+def test_linear_rejects_bad_arguments_on_host(asl, args, status):
+    X, W, LA, LB, Y, M, N, K, R, ws, wsb = args
+    assert asl.lib.lynx_linear(X or None, W, LA, LB, Y, M, N, K, R, ws, wsb, None) == status
+
+
+def test_other_entry_points_reject_bad_arguments(asl):
+    L = asl.lib
+    assert L.lynx_sparsify(None, 4, 16, A, A, A, None) == -1
+    assert L.lynx_sparsify(A, 4, 20, A, A, A, None) == -2
+    assert L.lynx_sparsify(A, 4, 16, A + 4, A, A, None) == -3
+    assert L.lynx_lora_down(A, A, None, A, 4, 16, 16, None) == -7
+    assert L.lynx_linear_dense(A, A, A, None, A, 4, 16, 16, 64, A, 1 << 20, None) == -1   # one LoRA factor
+    assert L.lynx_linear_dense(A, A, A, A, A, 4, 16, 16, 64, A, 10, None) == -4
+    assert L.lynx_linear_dense(A, A, None, None, A, 4, 16, 17, 64, None, 0, None) == -2
+    for code in range(-7, 1):
+        assert L.lynx_status_string(code)
+
+
+@pytest.mark.parametrize("M,K", [(1, 16), (5, 136), (130, 256), (17, 96)])
+def test_meta_to_canonical_matches_documented_layout(asl, M, K):
+    from helpers import pack_meta_reference
+    rng = np.random.default_rng(M * 1000 + K)
+    nibs = np.array([0x4, 0x8, 0xC, 0x9, 0xD, 0xE], dtype=np.uint8)
+    g = nibs[rng.integers(0, 6, size=(M, K // 4))]
+    canon = (g[:, 0::2] | (g[:, 1::2] << 4)).astype(np.uint8)
+    w0 = pack_meta_reference(canon, M, K)
+    lanes = rng.integers(0, 2**32, size=w0.shape + (4,), dtype=np.uint64).astype(np.uint32)  # words 1-3: junk
+    lanes[..., 0] = w0
+    packed = lanes.reshape(-1).view(np.uint8)
+    assert packed.size == asl.lynx_meta_bytes(M, K)
+    assert np.array_equal(asl.lynx_meta_to_canonical(packed, M, K), canon)
+
+
+def test_meta_layout_pairs_rows_r_and_r_plus_8():
+    """Spot check of the 16-bit pairing on one hand-made row (rows 0 and 8 of a block)."""
+    from helpers import pack_meta_reference
+    M, K = 16, 32
+    canon = np.full((M, K // 8), 0x44, dtype=np.uint8)
+    canon[0] = [0x98, 0xDC, 0x49, 0xEC]  # row 0 word 0xECDC4989 -> nibbles 8,9,C,D,9,4,C,E... little-endian bytes
+    canon[8] = [0x8E, 0x9D, 0xC4, 0x48]
+    w = pack_meta_reference(canon, M, K)[0, 0]
+    row0 = 0x98 | 0xDC << 8 | 0x49 << 16 | 0xEC << 24
+    row8 = 0x8E | 0x9D << 8 | 0xC4 << 16 | 0x48 << 24
+    assert w[0] == (row0 & 0xFFFF) | ((row8 & 0xFFFF) << 16)
+    assert w[8] == (row0 >> 16) | ((row8 >> 16) << 16)
+    assert w[1] == 0x44444444 and w[9] == 0x44444444

@@ -1,0 +1,155 @@
+"""Parity of the CUDA path (through the C-ABI) with the CPU oracle, element by
+element, on sizes that span several tiles and a ragged tail, plus the edge and
+degenerate cases of the method."""
+import numpy as np
+import pytest
+
+import oracle.lynx_oracle as O
+import synth
+from helpers import REL_FRO, S_RTOL, assert_y_close, meta_word0, pack_meta_reference, to_bits, to_dev, widen
+
+pytestmark = pytest.mark.gpu
+
+
+def _x(kind, M, K, seed=1):
+    if kind == "act":
+        return synth.act_bf16((M, K, seed), M, K, 0.05, 8.0)
+    if kind == "gelu":
+        return synth.gelu_bf16((M, K, seed), M, K, 3.97, 0.03, 10.0)
+    return synth.structured_x(kind, M, K, seed)
+
+
+SPARSIFY_CASES = [
+    (256, 512, "act"), (1, 16, "act"), (3, 48, "act"), (129, 528, "act"), (300, 3072, "act"),
+    (77, 1040, "mixed"), (64, 256, "equal"), (64, 256, "two4"), (40, 128, "zero"), (64, 256, "ties"),
+    (130, 12288, "gelu"),
+]
+
+
+@pytest.mark.parametrize("M,K,kind", SPARSIFY_CASES)
+def test_sparsify_bit_exact(lynx, M, K, kind):
+    import torch
+    X = _x(kind, M, K)
+    vals, meta, s = lynx.lynx_sparsify(to_dev(X))
+    assert lynx.lynx_sync_status() == 0
+    ref = O.sparsify(X)
+    assert np.array_equal(to_bits(vals), ref["vals"])
+    meta_h = meta.cpu().numpy()
+    assert np.array_equal(lynx.lynx_meta_to_canonical(meta_h, M, K), ref["meta"])
+    assert np.array_equal(meta_word0(meta_h, M, K), pack_meta_reference(ref["meta"], M, K))  # padding included
+    np.testing.assert_allclose(s.cpu().numpy(), ref["s"], rtol=S_RTOL, atol=0)
+    torch.cuda.synchronize()
+
+
+def test_sparsify_special_values(lynx):
+    s = lynx.lynx_sparsify(to_dev(_x("equal", 32, 256)))[2].cpu().numpy()
+    np.testing.assert_allclose(s, np.sqrt(2.0), rtol=1e-6)
+    s = lynx.lynx_sparsify(to_dev(_x("two4", 32, 256)))[2].cpu().numpy()
+    assert np.all(s == 1.0)
+    s = lynx.lynx_sparsify(to_dev(_x("zero", 32, 256)))[2].cpu().numpy()
+    assert np.all(s == 1.0)
+
+
+@pytest.mark.parametrize("M,K,scaled", [(256, 512, True), (300, 528, True), (5, 3072, False), (129, 12288, True)])
+def test_lora_down(lynx, M, K, scaled):
+    X = _x("act", M, K, 3)
+    LB = synth.gaussian_bf16((M, K, 4), (64, K), 0.02)
+    s = O.sparsify(X)["s"] if scaled else None
+    import torch
+    s_dev = torch.from_numpy(s.astype(np.float32)).cuda() if scaled else None
+    T = lynx.lynx_lora_down(to_dev(X), to_dev(LB), s_dev)
+    assert lynx.lynx_sync_status() == 0
+    assert_y_close(to_bits(T), O.lora_down(X, LB, s), "T")
+
+
+LINEAR_CASES = [(256, 512, 512), (300, 520, 528), (1, 8, 16), (129, 136, 144), (200, 1000, 1024),
+                (128, 256, 64), (384, 768, 3072)]
+
+
+def _layer(M, N, K, seed=7, xkind="act"):
+    X = _x(xkind, M, K, seed)
+    W = synth.gaussian_bf16((seed, 1), (N, K), 1.0 / np.sqrt(K))
+    LA = synth.gaussian_bf16((seed, 2), (N, 64), 0.02)
+    LB = synth.gaussian_bf16((seed, 3), (64, K), 0.02)
+    return X, W, LA, LB
+
+
+@pytest.mark.parametrize("M,N,K", LINEAR_CASES)
+def test_linear_full_comparison(lynx, M, N, K):
+    X, W, LA, LB = _layer(M, N, K)
+    Y = lynx.lynx_linear(to_dev(X), to_dev(W), to_dev(LA), to_dev(LB))
+    assert lynx.lynx_sync_status() == 0
+    assert_y_close(to_bits(Y), O.linear(X, W, LA, LB))
+
+
+@pytest.mark.parametrize("kind", ["mixed", "equal", "two4", "ties", "gelu"])
+def test_linear_structured_inputs(lynx, kind):
+    X, W, LA, LB = _layer(160, 384, 256, 11, kind)
+    Y = lynx.lynx_linear(to_dev(X), to_dev(W), to_dev(LA), to_dev(LB))
+    assert lynx.lynx_sync_status() == 0
+    # 8 outlier channels x10 before the GELU make |y|max ~ 10 rms: bf16 output rounding floor applies
+    assert_y_close(to_bits(Y), O.linear(X, W, LA, LB), bf16_floor=(kind == "gelu"))
+
+
+def test_linear_zero_rows_give_lora_only(lynx):
+    X, W, LA, LB = _layer(64, 256, 128, 12)
+    X[5] = 0
+    X[17] = 0
+    Y = to_bits(lynx.lynx_linear(to_dev(X), to_dev(W), to_dev(LA), to_dev(LB)))
+    assert np.all(Y[5] == 0) and np.all(Y[17] == 0)  # X = 0 gives Ys = 0 and Yr = 0
+    assert_y_close(Y, O.linear(X, W, LA, LB))
+
+
+def test_linear_zero_lora_and_24_input_is_cublas_gemm(lynx):
+    """Already-2:4 X with LA = 0 reduces to Y = X W^T: compare with cuBLAS and the oracle."""
+    import torch
+    M, N, K = 256, 512, 768
+    X = _x("two4", M, K, 13)
+    W = synth.gaussian_bf16((13, 1), (N, K), 1.0 / np.sqrt(K))
+    LA = np.zeros((N, 64), dtype=np.uint16)
+    LB = synth.gaussian_bf16((13, 3), (64, K), 0.02)
+    Xd, Wd = to_dev(X), to_dev(W)
+    Y = lynx.lynx_linear(Xd, Wd, to_dev(LA), to_dev(LB))
+    assert lynx.lynx_sync_status() == 0
+    ref = O.linear_dense(X, W)
+    assert_y_close(to_bits(Y), ref)
+    cub = to_bits(torch.matmul(Xd, Wd.t()))
+    assert_y_close(cub, ref, "cuBLAS")
+    # both are bf16 roundings of nearly the same fp32 sum
+    assert np.mean(to_bits(Y) == cub) > 0.9
+
+
+@pytest.mark.parametrize("M,N,K,lora", [(256, 512, 512, False), (300, 520, 528, True), (129, 136, 144, False),
+                                        (384, 768, 3072, True)])
+def test_linear_dense(lynx, M, N, K, lora):
+    X, W, LA, LB = _layer(M, N, K, 17)
+    if lora:
+        Y = lynx.lynx_linear_dense(to_dev(X), to_dev(W), to_dev(LA), to_dev(LB))
+        ref = O.linear_dense(X, W, LA, LB)
+    else:
+        Y = lynx.lynx_linear_dense(to_dev(X), to_dev(W))
+        ref = O.linear_dense(X, W)
+    assert lynx.lynx_sync_status() == 0
+    assert_y_close(to_bits(Y), ref)
+
+
+def test_linear_is_deterministic(lynx):
+    X, W, LA, LB = _layer(256, 512, 1024, 21)
+    args = [to_dev(a) for a in (X, W, LA, LB)]
+    y1 = to_bits(lynx.lynx_linear(*args))
+    y2 = to_bits(lynx.lynx_linear(*args))
+    assert np.array_equal(y1, y2)
+
+
+def test_output_guard_band_untouched(lynx):
+    """Y inside a larger buffer: the kernels write exactly M x N elements."""
+    import torch
+    M, N, K = 130, 264, 256
+    X, W, LA, LB = _layer(M, N, K, 23)
+    buf = torch.full((M * N + 4096,), -7.0, dtype=torch.bfloat16, device="cuda")
+    Y = buf[2048:2048 + M * N].view(M, N)
+    lynx.lynx_linear(to_dev(X), to_dev(W), to_dev(LA), to_dev(LB), Y=Y)
+    assert lynx.lynx_sync_status() == 0
+    b = buf.float().cpu().numpy()
+    assert np.all(b[:2048] == -7.0) and np.all(b[2048 + M * N:] == -7.0)
+    assert_y_close(to_bits(Y), O.linear(X, W, LA, LB))

@@ -225,6 +225,20 @@ def test_dense_layer_with_lora_against_loops():
     assert np.allclose(O.linear_dense(X, W, LA, LB), want, rtol=1e-13, atol=1e-13)
 
 
+def test_lora_down_hand_case_and_recombination():
+    case = GOLD["linear"][0]
+    X, LB, LA, W = (bits(case[k]) for k in ("X", "LB", "LA", "W"))
+    s = O.sparsify(X)["s"]
+    t = O.lora_down(X, LB, s)
+    # hand case: X LB^T = 1 - 3 + 2 + 0.5 + 4 = 4.5, s = 5.5/sqrt(29)
+    assert abs(t[0, 0] - 4.5 / (5.5 / math.sqrt(29.0))) < 1e-14
+    assert O.lora_down(X, LB)[0, 0] == 4.5
+    # s * (X~ W^T + T' LA^T) recombines to the layer output
+    x = O.widen(X)
+    acc = np.where(O.sparsify(X)["mask"], x, 0.0) @ O.widen(W).T + t @ O.widen(LA).T
+    assert np.allclose(s[:, None] * acc, O.linear(X, W, LA, LB), rtol=1e-14, atol=0)
+
+
 # ----------------------------------------------------------------------------- input generator
 def test_bf16_rounding_matches_torch():
     import torch
