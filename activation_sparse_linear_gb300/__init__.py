@@ -20,7 +20,7 @@ __all__ = [
     "lynx_meta_bytes", "lynx_workspace_bytes", "lynx_dense_workspace_bytes",
     "lynx_sparsify", "lynx_lora_down", "lynx_linear", "lynx_linear_dense",
     "lynx_sync_status", "lynx_status_string", "lynx_meta_to_canonical", "lynx_debug_set_fault",
-    "lynx_profile_next",
+    "lynx_profile_next", "lynx_linear_kernel_count", "lynx_mma_rate",
 ]
 
 LYNX_OK = 0
@@ -47,6 +47,9 @@ def _load() -> ctypes.CDLL:
         "lynx_meta_to_canonical": (ctypes.c_int, [_c_p, _c_p, _c_i64, _c_i64]),
         "lynx_debug_set_fault": (None, [ctypes.c_int, ctypes.c_uint64]),
         "lynx_profile_next": (None, [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]),
+        "lynx_linear_kernel_count": (ctypes.c_int, [_c_i64, _c_i64, _c_i64, _c_i64]),
+        "lynx_mma_rate": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_double),
+                                         ctypes.POINTER(ctypes.c_double), _c_p]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -179,6 +182,19 @@ def lynx_meta_to_canonical(meta_host, M: int, K: int):
     out = np.empty((M, K // 8), dtype=np.uint8)
     _check(lib.lynx_meta_to_canonical(src.ctypes.data, out.ctypes.data, M, K), "lynx_meta_to_canonical")
     return out
+
+
+def lynx_linear_kernel_count(M: int, N: int, K: int, R: int = 64) -> int:
+    return lib.lynx_linear_kernel_count(M, N, K, R)
+
+
+def lynx_mma_rate(mode: int, iters: int = 20000, stream=None) -> tuple[float, float]:
+    """(dense-equivalent TFLOP/s, MACs per SM clock) of back-to-back smem-resident MMAs.
+
+    mode 0 dense, 1 2:4 sparse, 2 2:4 sparse with a metadata tcgen05.cp per MMA."""
+    tf, mpc = ctypes.c_double(), ctypes.c_double()
+    _check(lib.lynx_mma_rate(int(mode), iters, ctypes.byref(tf), ctypes.byref(mpc), _stream(stream)), "lynx_mma_rate")
+    return tf.value, mpc.value
 
 
 def lynx_profile_next(events) -> None:

@@ -9,36 +9,39 @@
 
 namespace lynx {
 
-// Metadata tiling shared by the sparsify kernel, the sparse GEMM and the host
-// conversion to the canonical layout.  One tcgen05.mma.sp (M = 128 rows, 32
-// input channels) reads one 32-bit TMEM column: 8 groups x 4 bits per row.
-// Inside every 16-row block the hardware pairs rows r and r+8 by 16-bit
+// Metadata tiling shared by the sparsify kernel, the sparse GEMMs and the host
+// conversion to the canonical layout.  One tcgen05.mma.sp (M = 128 rows per
+// CTA, 32 input channels) reads one 32-bit TMEM column: 8 groups x 4 bits per
+// row.  Inside every 16-row block the hardware pairs rows r and r+8 by 16-bit
 // halves: lane 16b+i (i < 8) holds bits 0-15 of row 16b+i in its low half and
 // bits 0-15 of row 16b+8+i in its high half; lane 16b+8+i holds bits 16-31 of
 // the same two rows.  A row's 32 bits carry group g (channels 4g..4g+3 of the
-// chunk) in bits 4g..4g+3 as i0 | i1 << 2.
+// chunk) in bits 4g..4g+3 as i0 | i1 << 2.  The MMA's metadata address must
+// be an even column; bit 0 of the instruction descriptor (sparsity selector)
+// selects that column or the next one.
 //
-// In global memory every (128-row block, 32-channel chunk) owns a 2 KiB chunk
-// of 128 lanes x 16 bytes, row blocks outermost; word 0 of lane L is the TMEM
-// word of lane L, words 1-3 are never written or read as metadata.  The 16-byte
-// lane pitch lets tcgen05.cp.128x128b land each chunk on its own 32-column
-// aligned TMEM slot.  Channels are padded to a multiple of 64 (one GEMM stage)
-// and rows to a multiple of 128 with the pattern of an all-zero group (0x4).
+// In global memory every (128-row block, 128-channel block) owns a 2 KiB chunk
+// of 128 lanes x 16 bytes, row blocks outermost: word w of lane L is the TMEM
+// word of lane L for channels 32w..32w+31 of the block, so one
+// tcgen05.cp.128x128b lands four MMAs' metadata in four TMEM columns.
+// Channels are padded to a multiple of 128 and rows to a multiple of 256 (a
+// CTA pair) with the pattern of an all-zero group (0x4).
 constexpr int kMetaRows = 128;
+constexpr int kMetaRowPad = 256;
 constexpr int kMetaChunkCols = 32;
+constexpr int kMetaBlockCols = 128;
 constexpr int kMetaChunkBytes = kMetaRows * 16;
-constexpr int kMetaKPad = 64;
 __host__ __device__ inline int64_t round_up(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
-__host__ __device__ inline int64_t meta_chunks_k(int64_t K) { return round_up(K, kMetaKPad) / kMetaChunkCols; }
+__host__ __device__ inline int64_t meta_blocks_k(int64_t K) { return round_up(K, kMetaBlockCols) / kMetaBlockCols; }
 __host__ __device__ inline int64_t meta_bytes(int64_t M, int64_t K) {
-  return round_up(M, kMetaRows) / kMetaRows * meta_chunks_k(K) * kMetaChunkBytes;
+  return round_up(M, kMetaRowPad) / kMetaRows * meta_blocks_k(K) * kMetaChunkBytes;
 }
-// Byte offset of the 16-bit half holding bits [16q, 16q+16) of row r's word for chunk c.
-__host__ __device__ inline int64_t meta_half_offset(int64_t r, int64_t c, int q, int64_t chunks_k) {
+// Byte offset of the 16-bit half holding bits [16q, 16q+16) of row r's word for 32-channel chunk c.
+__host__ __device__ inline int64_t meta_half_offset(int64_t r, int64_t c, int q, int64_t blocks_k) {
   const int64_t blk = r / kMetaRows, rr = r % kMetaRows;
   const int64_t lane = (rr / 16) * 16 + q * 8 + (rr % 8);
   const int64_t h = (rr % 16) / 8;
-  return (blk * chunks_k + c) * kMetaChunkBytes + lane * 16 + h * 2;
+  return (blk * blocks_k + c / 4) * kMetaChunkBytes + lane * 16 + (c % 4) * 4 + h * 2;
 }
 
 cudaError_t launch_sparsify(const void* X, int M, int K, void* vals, void* meta, float* s, cudaStream_t st);
@@ -56,11 +59,36 @@ struct GemmArgs {
   void* Y;
   int64_t ldy;
   int M, N, K;
+  int splits;         // >1: split-K; each split writes an fp32 partial tile to `partial`
+  float* partial;     // splits x M x N fp32 (split-K only; no scale applied)
   DevCtl ctl;
 };
 
 // kind: 0 = dense, 256-wide tiles; 1 = dense + LoRA-up tail; 2 = sparse + LoRA-up tail;
 // 3 = sparse, no LoRA; 4 = dense, 64-wide tiles (LoRA down-projection).
 cudaError_t launch_gemm(int kind, const GemmArgs& a, cudaStream_t st);
+
+struct PairArgs {
+  CUtensorMap tmA;     // sparse: compressed values (box 32 x 128, 64-byte swizzle); dense: X (box 64 x 128)
+  CUtensorMap tmB;     // W, box 64 x 128 (one CTA's half of a 256-wide column tile), 128-byte swizzle
+  CUtensorMap tmMeta;  // metadata as uint32 [2 * chunks][256]; box 256 x 2 = one 2 KiB chunk
+  CUtensorMap tmT;     // T' (M x 64), box 32 x 128, 64-byte swizzle
+  CUtensorMap tmLA;    // LA (N x 64), box 32 x 128, 64-byte swizzle
+  const float* rowscale;
+  int scale_mode;      // SCALE_NONE or SCALE_MUL
+  void* Y;
+  int64_t ldy;
+  int M, N, K;
+  DevCtl ctl;
+};
+
+// The CTA-pair (cta_group::2) GEMM on 256 x 256 output tiles.
+cudaError_t launch_gemm_pair(bool sparse, bool lora, const PairArgs& a, cudaStream_t st);
+
+// T[m, r] = bf16( sum_s partial[s][m][r] / s[m] ) for the split-K LoRA down-projection.
+cudaError_t launch_lora_finalize(const float* partial, int splits, const float* s, void* T, int M, int R,
+                                 cudaStream_t st);
+
+int sm_count();
 
 }  // namespace lynx

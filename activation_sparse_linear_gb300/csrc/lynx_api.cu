@@ -73,18 +73,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D bf16 tensor map over a row-major [rows x cols] array with row stride `ld` elements.
+// 2-D tensor map over a row-major [rows x cols] array with row stride `ld` elements (bf16 by default).
 bool make_map(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows, uint64_t ld, uint32_t box_cols,
-              uint32_t box_rows, CUtensorMapSwizzle swz) {
+              uint32_t box_rows, CUtensorMapSwizzle swz,
+              CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   auto fn = encode_fn();
   if (!fn) return false;
+  const uint64_t esize = dtype == CU_TENSOR_MAP_DATA_TYPE_UINT32 ? 4 : 2;
   cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {ld * 2};
+  cuuint64_t strides[1] = {ld * esize};
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t es[2] = {1, 1};
-  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = fn(tm, dtype, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -105,11 +106,14 @@ DevCtl make_ctl() {
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? LYNX_OK : LYNX_ERR_CUDA; }
 
+constexpr int kMaxSplits = 8;  // split-K depth of the LoRA down-projection inside lynx_linear
+
 struct Workspace {
   void* vals;
   void* meta;
   float* s;
   void* T;
+  float* partial;
   size_t bytes;
 };
 
@@ -127,12 +131,25 @@ Workspace carve(void* base, int64_t M, int64_t K, int64_t R) {
   off += align256(static_cast<size_t>(M) * 4);
   w.T = reinterpret_cast<void*>(b + off);
   off += align256(static_cast<size_t>(M) * static_cast<size_t>(R) * 2);
+  w.partial = reinterpret_cast<float*>(b + off);
+  off += align256(static_cast<size_t>(kMaxSplits) * M * R * 4);
   w.bytes = off;
   return w;
 }
 
-// T = X LB^T [/ s] on the 64-wide tcgen05 tile.
-int run_lora_down(const void* X, const void* LB, const float* s, void* T, int64_t M, int64_t K, cudaStream_t st) {
+// T = X LB^T [/ s] on the 64-wide tcgen05 tile.  With a `partial` buffer of
+// kMaxSplits x M x R fp32 the K loop is split so that about one tile per SM
+// runs, and a small kernel sums the partials.
+int lora_splits(int64_t M, int64_t K) {
+  const int64_t num_m = (M + 127) / 128, nk = (K + 63) / 64;
+  int64_t sp = sm_count() / num_m;
+  if (sp > kMaxSplits) sp = kMaxSplits;
+  if (sp > nk) sp = nk;
+  return sp < 1 ? 1 : static_cast<int>(sp);
+}
+
+int run_lora_down(const void* X, const void* LB, const float* s, void* T, int64_t M, int64_t K, cudaStream_t st,
+                  float* partial = nullptr) {
   GemmArgs g;
   std::memset(&g, 0, sizeof(g));
   if (!make_map(&g.tmA, X, K, M, K, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) return LYNX_ERR_CUDA;
@@ -148,6 +165,17 @@ int run_lora_down(const void* X, const void* LB, const float* s, void* T, int64_
   g.N = kRank;
   g.K = static_cast<int>(K);
   g.ctl = make_ctl();
+  g.splits = 1;
+  g.partial = nullptr;
+  if (partial) {
+    const int sp = lora_splits(M, K);
+    if (sp > 1) {
+      g.splits = static_cast<int>(sp);
+      g.partial = partial;
+      if (cudaError_t e = launch_gemm(4, g, st)) return cuda_status(e);
+      return cuda_status(launch_lora_finalize(partial, g.splits, s, T, g.M, kRank, st));
+    }
+  }
   return cuda_status(launch_gemm(4, g, st));
 }
 
@@ -204,14 +232,16 @@ int lynx_linear(const void* X, const void* W, const void* LA, const void* LB, vo
   if (workspace_bytes < ws.bytes) return LYNX_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
-  GemmArgs g;
+  PairArgs g;
   std::memset(&g, 0, sizeof(g));
+  const uint64_t meta_rows = 2 * static_cast<uint64_t>(meta_bytes(M, K) / kMetaChunkBytes);  // 1 KiB rows
   if (!make_map(&g.tmA, ws.vals, K / 2, M, K / 2, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !make_map(&g.tmB, W, K, N, K, 64, 256, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&g.tmT, ws.T, R, M, R, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&g.tmLA, LA, R, N, R, 64, 256, CU_TENSOR_MAP_SWIZZLE_128B))
+      !make_map(&g.tmB, W, K, N, K, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&g.tmMeta, ws.meta, 256, meta_rows, 256, 256, 2, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_DATA_TYPE_UINT32) ||
+      !make_map(&g.tmT, ws.T, R, M, R, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !make_map(&g.tmLA, LA, R, N, R, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B))
     return LYNX_ERR_CUDA;
-  g.meta = static_cast<const uint8_t*>(ws.meta);
   g.rowscale = ws.s;
   g.scale_mode = SCALE_MUL;
   g.Y = Y;
@@ -226,9 +256,9 @@ int lynx_linear(const void* X, const void* W, const void* LA, const void* LB, vo
   if (cudaError_t e = launch_sparsify(X, static_cast<int>(M), static_cast<int>(K), ws.vals, ws.meta, ws.s, st))
     return cuda_status(e);
   if (cudaError_t e = prof.mark(1, st)) return cuda_status(e);
-  if (int e = run_lora_down(X, LB, ws.s, ws.T, M, K, st)) return e;
+  if (int e = run_lora_down(X, LB, ws.s, ws.T, M, K, st, ws.partial)) return e;
   if (cudaError_t e = prof.mark(2, st)) return cuda_status(e);
-  if (cudaError_t e = launch_gemm(2, g, st)) return cuda_status(e);
+  if (cudaError_t e = launch_gemm_pair(true, true, g, st)) return cuda_status(e);
   return cuda_status(prof.mark(3, st));
 }
 
@@ -246,20 +276,16 @@ int lynx_linear_dense(const void* X, const void* W, const void* LA, const void* 
   if (lora && workspace_bytes < lynx_dense_workspace_bytes(M, R)) return LYNX_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
-  GemmArgs g;
+  PairArgs g;
   std::memset(&g, 0, sizeof(g));
   if (!make_map(&g.tmA, X, K, M, K, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&g.tmB, W, K, N, K, 64, 256, CU_TENSOR_MAP_SWIZZLE_128B))
+      !make_map(&g.tmB, W, K, N, K, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
     return LYNX_ERR_CUDA;
   if (lora) {
-    if (!make_map(&g.tmT, workspace, R, M, R, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&g.tmLA, LA, R, N, R, 64, 256, CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!make_map(&g.tmT, workspace, R, M, R, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !make_map(&g.tmLA, LA, R, N, R, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B))
       return LYNX_ERR_CUDA;
-  } else {
-    g.tmT = g.tmA;
-    g.tmLA = g.tmB;
   }
-  g.meta = nullptr;
   g.rowscale = nullptr;
   g.scale_mode = SCALE_NONE;
   g.Y = Y;
@@ -273,10 +299,10 @@ int lynx_linear_dense(const void* X, const void* W, const void* LA, const void* 
   if (lora) {
     if (int e = run_lora_down(X, LB, nullptr, workspace, M, K, st)) return e;
     if (cudaError_t e = prof.mark(1, st)) return cuda_status(e);
-    if (cudaError_t e = launch_gemm(1, g, st)) return cuda_status(e);
+    if (cudaError_t e = launch_gemm_pair(false, true, g, st)) return cuda_status(e);
     return cuda_status(prof.mark(2, st));
   }
-  if (cudaError_t e = launch_gemm(0, g, st)) return cuda_status(e);
+  if (cudaError_t e = launch_gemm_pair(false, false, g, st)) return cuda_status(e);
   return cuda_status(prof.mark(1, st));
 }
 
@@ -313,19 +339,26 @@ int lynx_meta_to_canonical(const void* meta, uint8_t* canonical, int64_t M, int6
   if (!meta || !canonical) return LYNX_ERR_NULL;
   if (M < 1 || K < 8 || K % 8 != 0) return LYNX_ERR_SHAPE;
   const uint8_t* base = static_cast<const uint8_t*>(meta);
-  const int64_t chunks_k = meta_chunks_k(K);
+  const int64_t blocks_k = meta_blocks_k(K);
   for (int64_t m = 0; m < M; ++m) {
     uint8_t* out = canonical + m * (K / 8);
     for (int64_t c = 0; c * kMetaChunkCols < K; ++c) {
       uint16_t lo, hi;
-      std::memcpy(&lo, base + meta_half_offset(m, c, 0, chunks_k), 2);
-      std::memcpy(&hi, base + meta_half_offset(m, c, 1, chunks_k), 2);
+      std::memcpy(&lo, base + meta_half_offset(m, c, 0, blocks_k), 2);
+      std::memcpy(&hi, base + meta_half_offset(m, c, 1, blocks_k), 2);
       const uint32_t word = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
       for (int j = 0; j < 4 && c * kMetaChunkCols + 8 * j < K; ++j)  // byte j of the word = channels 8j..8j+7
         out[c * 4 + j] = static_cast<uint8_t>(word >> (8 * j));
     }
   }
   return LYNX_OK;
+}
+
+int lynx_linear_kernel_count(int64_t M, int64_t N, int64_t K, int64_t R) {
+  (void)N;
+  (void)R;
+  if (M < 1 || K < 1) return 0;
+  return lora_splits(M, K) > 1 ? 4 : 3;
 }
 
 void lynx_profile_next(void* const* events, int count) {

@@ -62,26 +62,38 @@ class ClockSampler:
         self.proc = None
 
     def __enter__(self):
+        import threading
+        self.lines = []
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                  "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            time.sleep(0.3)
         except OSError:
             self.proc = None
+            return self
+        self.reader = threading.Thread(target=self._read, daemon=True)
+        self.reader.start()
+        t0 = time.time()
+        while not self.lines and time.time() - t0 < 10.0:  # nvidia-smi is up before the timed region starts
+            time.sleep(0.02)
+        self.skip = len(self.lines)
         return self
 
+    def _read(self):
+        for line in self.proc.stdout:
+            if line.strip():
+                self.lines.append(line)
+
     def __exit__(self, *exc):
-        self.lines = []
         if self.proc is not None:
             time.sleep(0.15)
             self.proc.terminate()
             try:
-                out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [l for l in out.splitlines() if l.strip()]
+            self.reader.join(timeout=5)
+            self.lines = self.lines[max(0, self.skip - 1):]
         return False
 
     def summary(self) -> dict:
@@ -297,6 +309,11 @@ def main() -> int:
     lora_bytes = M * K * 2 + R * K * 2 + M * R * 2 + M * 4
     lora_gbs = lora_bytes / (stage_avg[1] * 1e-3) / 1e9
 
+    # tensor-core rate of smem-resident back-to-back MMAs (dense vs 2:4 sparse)
+    mma_dense_tf, mma_dense_mpc = asl.lynx_mma_rate(0, 20000)
+    mma_sparse_tf, mma_sparse_mpc = asl.lynx_mma_rate(1, 20000)
+    mma_sparse_cp_tf, _ = asl.lynx_mma_rate(2, 20000)
+
     # dense cuBLAS at the same shape, same rotation, same stream
     for i in range(args.warmup):
         torch.matmul(sets[i % ROTATE]["X"], sets[i % ROTATE]["W"].t(), out=sets[i % ROTATE]["Y"])
@@ -315,7 +332,7 @@ def main() -> int:
     Xh = torch.empty((M, K), dtype=torch.bfloat16, pin_memory=True)
     Xh.copy_(sets[0]["X"].cpu())
     Yh = torch.empty((M, N), dtype=torch.bfloat16, pin_memory=True)
-    ne = min(args.steps, 100)
+    ne = min(args.steps, 100)  # end-to-end steps (host copies dominate; fewer suffice)
     for i in range(3):
         s = sets[i % ROTATE]
         s["X"].copy_(Xh, non_blocking=True)
@@ -359,7 +376,7 @@ def main() -> int:
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": M * K * 2,
                 "d2h_bytes_per_step": M * N * 2, "ms_per_step": e2e_ms,
                 "note": "pinned host X -> device, lynx_linear, Y -> pinned host; weights resident"},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": L.lynx_linear_kernel_count(M, N, K, R) * args.steps,
         "clocks": clocks,
         "detail": {
             "stage_ms": {"sparsify": stage_avg[0], "lora_down": stage_avg[1], "sparse_gemm": stage_avg[2]},
@@ -370,6 +387,11 @@ def main() -> int:
             "dense_cublas_ms": dense_ms, "dense_cublas_tflops": flops / (dense_ms * 1e-3) / 1e12,
             "x_vs_dense_cublas": dense_ms / ms_per_step,
             "hbm_peak_GBs": hbm, "dense_bf16_peak_tflops": dense_tf,
+            "mma_microbench": {"dense_tflops": mma_dense_tf, "sparse_tflops_effective": mma_sparse_tf,
+                               "dense_macs_per_clk": mma_dense_mpc, "sparse_macs_per_clk_effective": mma_sparse_mpc,
+                               "sparse_over_dense": mma_sparse_tf / mma_dense_tf,
+                               "sparse_with_meta_copy_tflops_effective": mma_sparse_cp_tf,
+                               "sparse_gemm_frac_of_microbench": gemm_tf / mma_sparse_tf},
         },
     }
     print(json.dumps(line), flush=True)

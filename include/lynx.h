@@ -69,8 +69,9 @@ typedef enum {
  * of 128 and 64) hold the pattern of an all-zero group (0x4). */
 LYNX_API size_t lynx_meta_bytes(int64_t M, int64_t K);
 
-/* Workspace bytes needed by lynx_linear: compressed values, metadata, s and
- * the M x R LoRA intermediate, each 256-byte aligned. */
+/* Workspace bytes needed by lynx_linear: compressed values, metadata, s,
+ * the M x R LoRA intermediate and up to 8 fp32 split-K partials of it, each
+ * 256-byte aligned. */
 LYNX_API size_t lynx_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t R);
 
 /* Workspace bytes needed by lynx_linear_dense when a LoRA branch is given
@@ -100,7 +101,8 @@ LYNX_API int lynx_lora_down(const void* X, const void* LB, const float* s, void*
  *   X [in] M x K, W [in] N x K, LA [in] N x R, LB [in] R x K, Y [out] M x N bf16.
  *   workspace: >= lynx_workspace_bytes(M, N, K, R) bytes of device memory,
  *   16-byte aligned, not shared with a concurrent call.
- * Enqueues three kernels: sparsify, LoRA down-projection, and the tcgen05
+ * Enqueues sparsify, the LoRA down-projection (split over K, plus a small
+ * reduction kernel, when few row blocks would leave SMs idle) and the tcgen05
  * 2:4-sparse GEMM whose extra K-steps accumulate T' LA^T into the same
  * tensor-memory accumulator, with s applied in the epilogue.
  * (RT-Lynx page, Method and CUDA kernel optimisation.) */
@@ -126,14 +128,27 @@ LYNX_API const char* lynx_status_string(int status);
  * byte j = nibble(group 2j) | nibble(group 2j+1) << 4.  K % 8 == 0. */
 LYNX_API int lynx_meta_to_canonical(const void* meta, uint8_t* canonical, int64_t M, int64_t K);
 
+/* Number of kernels lynx_linear enqueues for these sizes on the current
+ * device (3, or 4 when the LoRA down-projection is split over K). */
+LYNX_API int lynx_linear_kernel_count(int64_t M, int64_t N, int64_t K, int64_t R);
+
 /* Stage-timing hook.  The next lynx_linear or lynx_linear_dense call made
  * from this host thread records events[0] on its stream before its first
- * kernel and events[i] right after its i-th kernel; count must be the number
- * of kernels + 1 (4 for lynx_linear: sparsify, LoRA down-projection, sparse
+ * stage and events[i] right after its i-th stage; count must be the number
+ * of stages + 1 (4 for lynx_linear: sparsify, LoRA down-projection, sparse
  * GEMM; 3 for lynx_linear_dense with LoRA, 2 without).  The events are
  * cudaEvent_t handles owned by the caller.  The setting is used by that one
  * call and then cleared; a count that does not match is ignored. */
 LYNX_API void lynx_profile_next(void* const* events, int count);
+
+/* Tensor-core rate microbenchmark: every SM issues `iters` back-to-back
+ * instructions of shape 128 x 256 with operands resident in shared memory:
+ * mode 0 tcgen05.mma (dense), mode 1 tcgen05.mma.sp (2:4 sparse A, metadata
+ * resident in tensor memory), mode 2 tcgen05.mma.sp each preceded by the
+ * tcgen05.cp of its 2 KiB metadata chunk (the sparse GEMM's pattern).  Writes
+ * the dense-equivalent rate (2*M*N*K per instruction, K = 16 dense or 32
+ * logical sparse) in TFLOP/s and in MACs per SM clock.  Synchronises `stream`. */
+LYNX_API int lynx_mma_rate(int mode, int iters, double* tflops, double* macs_per_clock, void* stream);
 
 /* Test hook.  inject = 1 makes the next GEMM launches never deliver their
  * first pipeline stage, so their bounded waits run out after wait_ns

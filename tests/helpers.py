@@ -66,30 +66,23 @@ def assert_y_close(y_bits: np.ndarray, ref: np.ndarray, what: str = "Y", bf16_fl
 
 
 def pack_meta_reference(canon: np.ndarray, M: int, K: int) -> np.ndarray:
-    """Word 0 of every lane of the tensor-core metadata layout described in
-    include/lynx.h, built from canonical M x K/8 bytes.  Shape
-    (row blocks, 32-channel chunks, 128 lanes) uint32."""
-    Mp, Kp = -(-M // 128) * 128, -(-K // 64) * 64
-    C = Kp // 32
+    """The whole tensor-core metadata buffer described in include/lynx.h, built
+    from canonical M x K/8 bytes: uint8 array of lynx_meta_bytes(M, K) bytes."""
+    Mp, Kp = -(-M // 256) * 256, -(-K // 128) * 128
+    C = Kp // 32                                   # 32-channel chunks per row
     nib = np.full((Mp, Kp // 4), 4, dtype=np.uint32)
     nib[:M, :K // 4] = np.stack([canon & 0xF, canon >> 4], axis=-1).reshape(M, K // 4)
-    words = np.zeros((Mp, C), dtype=np.uint32)
+    words = np.zeros((Mp, C), dtype=np.uint32)      # row word of every chunk
     for g in range(8):
         words |= nib[:, g::8] << np.uint32(4 * g)
-    out = np.zeros((Mp // 128, C, 128), dtype=np.uint32)
-    r = np.arange(Mp)
-    blk, rr = r // 128, r % 128
-    i, h, b16 = rr % 8, (rr % 16) // 8, (rr // 16) * 16
     lo, hi = words & np.uint32(0xFFFF), words >> np.uint32(16)
-    for rowi in range(Mp):
-        sh = np.uint32(16 * h[rowi])
-        out[blk[rowi], :, b16[rowi] + i[rowi]] |= lo[rowi] << sh
-        out[blk[rowi], :, b16[rowi] + 8 + i[rowi]] |= hi[rowi] << sh
-    return out
-
-
-def meta_word0(meta_bytes_host: np.ndarray, M: int, K: int) -> np.ndarray:
-    """Word 0 of every lane of a metadata buffer, shaped like pack_meta_reference's result."""
-    Mp, Kp = -(-M // 128) * 128, -(-K // 64) * 64
-    w = np.ascontiguousarray(meta_bytes_host, dtype=np.uint8).view(np.uint32)
-    return w.reshape(Mp // 128, Kp // 32, 128, 4)[..., 0]
+    # TMEM order inside each 16-row block: lane 16b+i <- low halves of rows 16b+i, 16b+8+i;
+    # lane 16b+8+i <- their high halves
+    r = lo.reshape(Mp // 16, 2, 8, C)               # [16-row block, half (rows i / 8+i), i, chunk]
+    h = hi.reshape(Mp // 16, 2, 8, C)
+    lane_lo = r[:, 0] | (r[:, 1] << np.uint32(16))  # lanes 16b+i
+    lane_hi = h[:, 0] | (h[:, 1] << np.uint32(16))  # lanes 16b+8+i
+    lanes = np.stack([lane_lo, lane_hi], axis=1).reshape(Mp, C)   # lane-major within each 128-row block
+    # [row block, lane, channel block, word] -> [row block, channel block, lane, word]
+    out = lanes.reshape(Mp // 128, 128, Kp // 128, 4).transpose(0, 2, 1, 3)
+    return np.ascontiguousarray(out).reshape(-1).view(np.uint8)

@@ -47,12 +47,13 @@ def test_no_cpu_fallback_in_package():
 
 
 def test_sizes(asl):
-    # one 2 KiB chunk per (128-row block, 32-channel chunk); channels padded to 64
-    assert asl.lynx_meta_bytes(4608, 3072) == 36 * 96 * 2048
-    assert asl.lynx_meta_bytes(1, 16) == 1 * 2 * 2048
-    assert asl.lynx_meta_bytes(129, 130) == 2 * 6 * 2048
+    # one 2 KiB chunk per (128-row block, 128-channel block); rows padded to 256, channels to 128
+    assert asl.lynx_meta_bytes(4608, 3072) == 36 * 24 * 2048
+    assert asl.lynx_meta_bytes(1, 16) == 2 * 1 * 2048
+    assert asl.lynx_meta_bytes(129, 130) == 2 * 2 * 2048
+    assert asl.lynx_meta_bytes(257, 3072) == 4 * 24 * 2048
     ws = asl.lynx_workspace_bytes(4608, 9216, 3072, 64)
-    assert ws >= 4608 * 3072 + 36 * 96 * 2048 + 4608 * 4 + 4608 * 64 * 2
+    assert ws >= 4608 * 3072 + 36 * 24 * 2048 + 4608 * 4 + 4608 * 64 * 2
     assert asl.lynx_dense_workspace_bytes(100, 64) >= 100 * 64 * 2
 
 
@@ -87,31 +88,30 @@ def test_other_entry_points_reject_bad_arguments(asl):
         assert L.lynx_status_string(code)
 
 
-@pytest.mark.parametrize("M,K", [(1, 16), (5, 136), (130, 256), (17, 96)])
+@pytest.mark.parametrize("M,K", [(1, 16), (5, 136), (130, 256), (17, 96), (300, 512)])
 def test_meta_to_canonical_matches_documented_layout(asl, M, K):
     from helpers import pack_meta_reference
     rng = np.random.default_rng(M * 1000 + K)
     nibs = np.array([0x4, 0x8, 0xC, 0x9, 0xD, 0xE], dtype=np.uint8)
     g = nibs[rng.integers(0, 6, size=(M, K // 4))]
     canon = (g[:, 0::2] | (g[:, 1::2] << 4)).astype(np.uint8)
-    w0 = pack_meta_reference(canon, M, K)
-    lanes = rng.integers(0, 2**32, size=w0.shape + (4,), dtype=np.uint64).astype(np.uint32)  # words 1-3: junk
-    lanes[..., 0] = w0
-    packed = lanes.reshape(-1).view(np.uint8)
+    packed = pack_meta_reference(canon, M, K)
     assert packed.size == asl.lynx_meta_bytes(M, K)
     assert np.array_equal(asl.lynx_meta_to_canonical(packed, M, K), canon)
 
 
 def test_meta_layout_pairs_rows_r_and_r_plus_8():
-    """Spot check of the 16-bit pairing on one hand-made row (rows 0 and 8 of a block)."""
+    """Spot check of the documented 16-bit pairing on two hand-made rows (0 and 8 of a block)."""
     from helpers import pack_meta_reference
-    M, K = 16, 32
+    M, K = 16, 128
     canon = np.full((M, K // 8), 0x44, dtype=np.uint8)
-    canon[0] = [0x98, 0xDC, 0x49, 0xEC]  # row 0 word 0xECDC4989 -> nibbles 8,9,C,D,9,4,C,E... little-endian bytes
-    canon[8] = [0x8E, 0x9D, 0xC4, 0x48]
-    w = pack_meta_reference(canon, M, K)[0, 0]
+    canon[0, :4] = [0x98, 0xDC, 0x49, 0xEC]   # row 0, channels 0..31
+    canon[8, 4:8] = [0x8E, 0x9D, 0xC4, 0x48]  # row 8, channels 32..63
+    words = pack_meta_reference(canon, M, K).view(np.uint32).reshape(2, 1, 128, 4)[0, 0]
     row0 = 0x98 | 0xDC << 8 | 0x49 << 16 | 0xEC << 24
     row8 = 0x8E | 0x9D << 8 | 0xC4 << 16 | 0x48 << 24
-    assert w[0] == (row0 & 0xFFFF) | ((row8 & 0xFFFF) << 16)
-    assert w[8] == (row0 >> 16) | ((row8 >> 16) << 16)
-    assert w[1] == 0x44444444 and w[9] == 0x44444444
+    assert words[0, 0] == (row0 & 0xFFFF) | (0x4444 << 16)          # lane 0, chunk 0: low halves of rows 0, 8
+    assert words[8, 0] == (row0 >> 16) | (0x4444 << 16)             # lane 8, chunk 0: high halves
+    assert words[0, 1] == 0x4444 | ((row8 & 0xFFFF) << 16)          # lane 0, chunk 1
+    assert words[8, 1] == 0x4444 | ((row8 >> 16) << 16)             # lane 8, chunk 1
+    assert words[1, 0] == 0x44444444 and words[9, 3] == 0x44444444

@@ -6,7 +6,7 @@ import pytest
 
 import oracle.lynx_oracle as O
 import synth
-from helpers import REL_FRO, S_RTOL, assert_y_close, meta_word0, pack_meta_reference, to_bits, to_dev, widen
+from helpers import REL_FRO, S_RTOL, assert_y_close, pack_meta_reference, to_bits, to_dev, widen
 
 pytestmark = pytest.mark.gpu
 
@@ -36,9 +36,25 @@ def test_sparsify_bit_exact(lynx, M, K, kind):
     assert np.array_equal(to_bits(vals), ref["vals"])
     meta_h = meta.cpu().numpy()
     assert np.array_equal(lynx.lynx_meta_to_canonical(meta_h, M, K), ref["meta"])
-    assert np.array_equal(meta_word0(meta_h, M, K), pack_meta_reference(ref["meta"], M, K))  # padding included
+    assert np.array_equal(meta_h, pack_meta_reference(ref["meta"], M, K))  # every byte, padding included
     np.testing.assert_allclose(s.cpu().numpy(), ref["s"], rtol=S_RTOL, atol=0)
     torch.cuda.synchronize()
+
+
+def test_sparsify_exhaustive_tuples(lynx):
+    """Every 4-tuple over {-2,-1,-0,+0,1,2,3} (ties and signed zeros everywhere), bit-exact."""
+    import itertools
+    tuples = np.array(list(itertools.product([-2.0, -1.0, -0.0, 0.0, 1.0, 2.0, 3.0], repeat=4)), dtype=np.float32)
+    G = 16  # groups per row (K = 64)
+    rows = -(-len(tuples) // G)
+    pad = np.zeros((rows * G - len(tuples), 4), dtype=np.float32)
+    X = synth.bf16_bits(np.concatenate([tuples, pad]).reshape(rows, 4 * G))
+    vals, meta, s = lynx.lynx_sparsify(to_dev(X))
+    assert lynx.lynx_sync_status() == 0
+    ref = O.sparsify(X)
+    assert np.array_equal(to_bits(vals), ref["vals"])
+    assert np.array_equal(lynx.lynx_meta_to_canonical(meta.cpu().numpy(), rows, 4 * G), ref["meta"])
+    np.testing.assert_allclose(s.cpu().numpy(), ref["s"], rtol=S_RTOL, atol=0)
 
 
 def test_sparsify_special_values(lynx):
@@ -153,3 +169,9 @@ def test_output_guard_band_untouched(lynx):
     b = buf.float().cpu().numpy()
     assert np.all(b[:2048] == -7.0) and np.all(b[2048 + M * N:] == -7.0)
     assert_y_close(to_bits(Y), O.linear(X, W, LA, LB))
+
+
+def test_mma_rate_microbenchmark_runs(lynx):
+    for mode in (0, 1, 2):
+        tf, mpc = lynx.lynx_mma_rate(mode, 2000)
+        assert tf > 100 and mpc > 0
