@@ -191,7 +191,8 @@ def lynx_linear_kernel_count(M: int, N: int, K: int, R: int = 64) -> int:
 def lynx_mma_rate(mode: int, iters: int = 20000, stream=None) -> tuple[float, float]:
     """(dense-equivalent TFLOP/s, MACs per SM clock) of back-to-back smem-resident MMAs.
 
-    mode 0 dense, 1 2:4 sparse, 2 2:4 sparse with a metadata tcgen05.cp per MMA."""
+    mode 0 dense, 1 2:4 sparse, 2 2:4 sparse with a metadata tcgen05.cp per MMA,
+    3 sparse with a commit per two MMAs, 4 sparse with two commits per four MMAs."""
     tf, mpc = ctypes.c_double(), ctypes.c_double()
     _check(lib.lynx_mma_rate(int(mode), iters, ctypes.byref(tf), ctypes.byref(mpc), _stream(stream)), "lynx_mma_rate")
     return tf.value, mpc.value

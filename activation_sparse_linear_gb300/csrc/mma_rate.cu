@@ -17,7 +17,9 @@ __device__ int g_rate_error;
 
 // mode 0: dense; 1: sparse, metadata resident in TMEM; 2: sparse, each MMA
 // preceded by a tcgen05.cp.128x128b of its 2 KiB metadata chunk into one of
-// eight 32-column slots (the sparse GEMM's per-MMA pattern).
+// eight 32-column slots; 3: sparse with a tcgen05.commit after every two
+// MMAs (one pipeline stage of 64 channels); 4: sparse with two commits after
+// every four MMAs.
 __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int mode, int iters, DevCtl ctl,
                                                           unsigned long long* cycles) {
   extern __shared__ uint8_t smem_raw[];
@@ -26,6 +28,7 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int mode, int iters, D
   uint8_t* B = smem + 128 * 128;   // 256 rows x 128 B
   uint8_t* E = B + kN * 128;       // 2 KiB metadata chunk: 128 lanes x 16 B
   __shared__ __align__(8) uint64_t bar;
+  __shared__ __align__(8) uint64_t stage_bar[8];
   __shared__ uint32_t slot;
   const int t = threadIdx.x, warp = t >> 5;
   // small finite operands: 1.0 in every bf16 slot of A and B
@@ -33,6 +36,7 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int mode, int iters, D
   for (int i = t; i < 128 * 4; i += blockDim.x) reinterpret_cast<uint32_t*>(E)[i] = 0x44444444u;
   if (t == 0) {
     mbar_init(&bar, 1);
+    for (int i = 0; i < 8; ++i) mbar_init(&stage_bar[i], 1);
     fence_mbar_init();
   }
   fence_proxy_async();
@@ -60,9 +64,15 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int mode, int iters, D
         tc_cp_128x128b(slot_col, sdesc(smem_u32(E), 128, 128, SWZ_NONE));
         tc_mma_sp(tm, sdesc(smem_u32(A) + (k & 1) * 32, 16, 1024, SWZ_128B),
                   sdesc(smem_u32(B) + (k & 1) * 64, 16, 1024, SWZ_128B), slot_col, IDS, i != 0);
-      } else if (mode == 1)
+      } else if (mode >= 1) {
         tc_mma_sp(tm, sdesc(smem_u32(A) + (k & 1) * 32, 16, 1024, SWZ_128B),
                   sdesc(smem_u32(B) + (k & 1) * 64, 16, 1024, SWZ_128B), tm + 256, IDS, i != 0);
+        if (mode == 3 && (i & 1)) tc_commit(&stage_bar[(i >> 1) & 7]);
+        if (mode == 4 && (i & 3) == 3) {
+          tc_commit(&stage_bar[(i >> 1) & 7]);
+          tc_commit(&stage_bar[((i >> 1) + 1) & 7]);
+        }
+      }
       else
         tc_mma(tm, sdesc(smem_u32(A) + k * 32, 16, 1024, SWZ_128B), sdesc(smem_u32(B) + k * 32, 16, 1024, SWZ_128B),
                ID, i != 0);
@@ -87,7 +97,7 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int mode, int iters, D
 using namespace lynx;
 
 extern "C" int lynx_mma_rate(int mode, int iters, double* tflops, double* macs_per_clock, void* stream) {
-  if (mode < 0 || mode > 2) return LYNX_ERR_UNSUPPORTED;
+  if (mode < 0 || mode > 4) return LYNX_ERR_UNSUPPORTED;
   const int sparse = mode != 0;
   if (!tflops || !macs_per_clock) return LYNX_ERR_NULL;
   if (iters < 1 || iters > (1 << 24)) return LYNX_ERR_SHAPE;

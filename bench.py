@@ -313,6 +313,8 @@ def main() -> int:
     mma_dense_tf, mma_dense_mpc = asl.lynx_mma_rate(0, 20000)
     mma_sparse_tf, mma_sparse_mpc = asl.lynx_mma_rate(1, 20000)
     mma_sparse_cp_tf, _ = asl.lynx_mma_rate(2, 20000)
+    mma_sparse_c2_tf, _ = asl.lynx_mma_rate(3, 20000)
+    mma_sparse_c4_tf, _ = asl.lynx_mma_rate(4, 20000)
 
     # dense cuBLAS at the same shape, same rotation, same stream
     for i in range(args.warmup):
@@ -327,6 +329,20 @@ def main() -> int:
     d1.record(stream)
     torch.cuda.synchronize()
     dense_ms = d0.elapsed_time(d1) / nd
+
+    # this library's dense tcgen05 GEMM (selectively skipped layer, no LoRA) at the same shape
+    for i in range(args.warmup):
+        s = sets[i % ROTATE]
+        L.lynx_linear_dense(s["X"].data_ptr(), s["W"].data_ptr(), None, None, s["Y"].data_ptr(), M, N, K, R, None, 0, sp)
+    torch.cuda.synchronize()
+    l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    l0.record(stream)
+    for i in range(nd):
+        s = sets[i % ROTATE]
+        L.lynx_linear_dense(s["X"].data_ptr(), s["W"].data_ptr(), None, None, s["Y"].data_ptr(), M, N, K, R, None, 0, sp)
+    l1.record(stream)
+    torch.cuda.synchronize()
+    lynx_dense_ms = l0.elapsed_time(l1) / nd
 
     # end to end through the C-ABI with host buffers: H2D of X, the layer, D2H of Y
     Xh = torch.empty((M, K), dtype=torch.bfloat16, pin_memory=True)
@@ -386,11 +402,14 @@ def main() -> int:
             "lora_down_GBs": lora_gbs, "lora_down_frac_hbm": lora_gbs / hbm,
             "dense_cublas_ms": dense_ms, "dense_cublas_tflops": flops / (dense_ms * 1e-3) / 1e12,
             "x_vs_dense_cublas": dense_ms / ms_per_step,
+            "lynx_dense_gemm_ms": lynx_dense_ms, "lynx_dense_gemm_tflops": flops / (lynx_dense_ms * 1e-3) / 1e12,
             "hbm_peak_GBs": hbm, "dense_bf16_peak_tflops": dense_tf,
             "mma_microbench": {"dense_tflops": mma_dense_tf, "sparse_tflops_effective": mma_sparse_tf,
                                "dense_macs_per_clk": mma_dense_mpc, "sparse_macs_per_clk_effective": mma_sparse_mpc,
                                "sparse_over_dense": mma_sparse_tf / mma_dense_tf,
                                "sparse_with_meta_copy_tflops_effective": mma_sparse_cp_tf,
+                               "sparse_commit_every_2_tflops_effective": mma_sparse_c2_tf,
+                               "sparse_2commits_every_4_tflops_effective": mma_sparse_c4_tf,
                                "sparse_gemm_frac_of_microbench": gemm_tf / mma_sparse_tf},
         },
     }
