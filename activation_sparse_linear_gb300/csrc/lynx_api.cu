@@ -331,6 +331,7 @@ const char* lynx_status_string(int status) {
     case LYNX_ERR_CUDA: return "CUDA call failed";
     case LYNX_ERR_TIMEOUT: return "device-side wait timed out";
     case LYNX_ERR_UNSUPPORTED: return "unsupported configuration (LoRA rank must be 64)";
+    case LYNX_ERR_TOO_LARGE: return "problem needs more scratch than lynx_linear_noalloc's fixed array";
     default: return "unknown status";
   }
 }
@@ -372,3 +373,39 @@ void lynx_debug_set_fault(int inject, uint64_t wait_ns) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- lynx_linear_noalloc
+// Scratch for callers that cannot allocate: a file-scope device array, so the
+// CUDA module loader reserves it with the library's device image.  Host code
+// must not hand the symbol itself to a kernel (on the host it only names a
+// host-side shadow); its device address comes from cudaGetSymbolAddress, looked
+// up once per device with that device current.
+namespace lynx {
+namespace {
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[LYNX_NOALLOC_SCRATCH_BYTES];
+
+void* noalloc_scratch() {
+  static void* ptrs[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> g(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return nullptr;
+    ptrs[dev] = p;
+  }
+  return ptrs[dev];
+}
+
+}  // namespace
+}  // namespace lynx
+
+extern "C" int lynx_linear_noalloc(const void* X, const void* W, const void* LA, const void* LB, void* Y, int64_t M,
+                                   int64_t N, int64_t K, int64_t R, void* stream) {
+  if (lynx_workspace_bytes(M, N, K, R) > LYNX_NOALLOC_SCRATCH_BYTES) return LYNX_ERR_TOO_LARGE;
+  void* ws = lynx::noalloc_scratch();
+  if (!ws) return LYNX_ERR_CUDA;
+  return lynx_linear(X, W, LA, LB, Y, M, N, K, R, ws, LYNX_NOALLOC_SCRATCH_BYTES, stream);
+}

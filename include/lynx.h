@@ -51,7 +51,8 @@ typedef enum {
   LYNX_ERR_WORKSPACE = -4,   /* workspace smaller than lynx_*workspace_bytes() */
   LYNX_ERR_CUDA = -5,        /* a CUDA runtime/driver call failed */
   LYNX_ERR_TIMEOUT = -6,     /* a device-side bounded wait ran out */
-  LYNX_ERR_UNSUPPORTED = -7  /* valid but not implemented (R != 64) */
+  LYNX_ERR_UNSUPPORTED = -7, /* valid but not implemented (R != 64) */
+  LYNX_ERR_TOO_LARGE = -8    /* needs more scratch than lynx_linear_noalloc owns */
 } lynx_status;
 
 /* Bytes of 2:4 metadata for an M x K activation:
@@ -109,6 +110,36 @@ LYNX_API int lynx_lora_down(const void* X, const void* LB, const float* s, void*
 LYNX_API int lynx_linear(const void* X, const void* W, const void* LA, const void* LB, void* Y, int64_t M, int64_t N,
                 int64_t K, int64_t R, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Size of the fixed scratch array behind lynx_linear_noalloc, per GPU. */
+#define LYNX_NOALLOC_SCRATCH_BYTES (64u << 20)
+
+/* lynx_linear for callers that must not allocate device memory.  (No
+ * counterpart in the RT-Lynx paper: this is a deployment convenience.)
+ *
+ * Some callers cannot call cudaMalloc or any allocator on the path that runs
+ * the layer: a request loop in a serving process that must never stall on
+ * an allocation (cudaMalloc can synchronise the device), or a plug-in inside
+ * another runtime that owns every byte of device memory and gives its
+ * plug-ins none.  This entry point takes the same arguments as lynx_linear
+ * minus the workspace: its scratch is one array of LYNX_NOALLOC_SCRATCH_BYTES
+ * in the library's own device image, which every GPU that loads the library
+ * holds until the process exits.  It allocates nothing itself and calls no
+ * allocating routine.
+ *
+ * Limits and rules:
+ *   - a problem whose lynx_workspace_bytes(M, N, K, R) exceeds
+ *     LYNX_NOALLOC_SCRATCH_BYTES is rejected with LYNX_ERR_TOO_LARGE before
+ *     anything is enqueued;
+ *   - the first call on a device, with that device current, looks up the
+ *     array's device address (cudaGetSymbolAddress); make that first call
+ *     before any stream capture;
+ *   - every call on a device shares the one array and leaves its contents
+ *     behind (nothing in it has to start at zero), so calls whose kernels
+ *     overlap on the GPU -- on different streams, or from different threads --
+ *     race and corrupt each other's results: order them on one stream. */
+LYNX_API int lynx_linear_noalloc(const void* X, const void* W, const void* LA, const void* LB, void* Y, int64_t M,
+                                 int64_t N, int64_t K, int64_t R, void* stream);
+
 /* A selectively skipped (dense) layer: Y = bf16( X W^T [+ (X LB^T) LA^T] ).
  * LA and LB are both NULL (no LoRA) or both given (then R = 64 and the
  * workspace must hold lynx_dense_workspace_bytes(M, R) bytes).
@@ -145,7 +176,9 @@ LYNX_API void lynx_profile_next(void* const* events, int count);
  * instructions of shape 128 x 256 with operands resident in shared memory:
  * mode 0 tcgen05.mma (dense), mode 1 tcgen05.mma.sp (2:4 sparse A, metadata
  * resident in tensor memory), mode 2 tcgen05.mma.sp each preceded by the
- * tcgen05.cp of its 2 KiB metadata chunk (the sparse GEMM's pattern).  Writes
+ * tcgen05.cp of its 2 KiB metadata chunk, mode 3 tcgen05.mma.sp with a
+ * tcgen05.commit after every two MMAs, mode 4 with two commits after every
+ * four MMAs.  Writes
  * the dense-equivalent rate (2*M*N*K per instruction, K = 16 dense or 32
  * logical sparse) in TFLOP/s and in MACs per SM clock.  Synchronises `stream`. */
 LYNX_API int lynx_mma_rate(int mode, int iters, double* tflops, double* macs_per_clock, void* stream);

@@ -1,0 +1,62 @@
+"""lynx_linear_noalloc: the entry point for callers that may not allocate device
+memory (a serving loop that must never stall in cudaMalloc, a plug-in whose host
+runtime owns all device memory).  It runs the same layer on a fixed scratch
+array inside the library, so its output must match lynx_linear's, call after
+call, and a problem too large for that array must be refused up front.
+
+This file is named to be collected last, so that a run stopping at the first
+failure has already run every other test."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import synth
+from helpers import assert_y_close, to_bits, to_dev, widen
+
+pytestmark = pytest.mark.gpu
+
+LYNX_ERR_TOO_LARGE = -8
+
+
+def _fn(lynx):
+    fn = lynx.lib.lynx_linear_noalloc
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int64] * 4 + [ctypes.c_void_p]
+    return fn
+
+
+def _layer(M, N, K, seed):
+    X = synth.act_bf16((M, K, seed), M, K, 0.03, 10.0)
+    W = synth.gaussian_bf16((seed, 1), (N, K), 1.0 / np.sqrt(K))
+    LA = synth.gaussian_bf16((seed, 2), (N, 64), 0.02)
+    LB = synth.gaussian_bf16((seed, 3), (64, K), 0.02)
+    return [to_dev(a) for a in (X, W, LA, LB)]
+
+
+def test_noalloc_matches_lynx_linear_on_consecutive_calls(lynx):
+    import torch
+    fn = _fn(lynx)
+    stream = torch.cuda.current_stream().cuda_stream
+    outs = []
+    for seed, (M, N, K) in ((31, (300, 520, 528)), (32, (1024, 1536, 3072))):
+        X, W, LA, LB = _layer(M, N, K, seed)
+        ref = lynx.lynx_linear(X, W, LA, LB)  # the existing entry point, with its own workspace
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        st = fn(X.data_ptr(), W.data_ptr(), LA.data_ptr(), LB.data_ptr(), Y.data_ptr(), M, N, K, 64, stream)
+        assert st == 0, lynx.lynx_status_string(st)
+        assert lynx.lynx_sync_status() == 0
+        assert_y_close(to_bits(Y), widen(to_bits(ref)), "noalloc vs lynx_linear")
+        outs.append((Y, ref))
+    # the second call reused the scratch array; the first call's result is untouched
+    Y0, ref0 = outs[0]
+    assert_y_close(to_bits(Y0), widen(to_bits(ref0)), "first call after the second")
+
+
+def test_noalloc_refuses_problems_beyond_its_scratch(lynx):
+    fn = _fn(lynx)
+    fake = 1 << 20  # aligned, never dereferenced: the size check comes first
+    M, N, K = 16384, 3072, 12288
+    assert lynx.lynx_workspace_bytes(M, N, K, 64) > (64 << 20)
+    assert fn(fake, fake, fake, fake, fake, M, N, K, 64, None) == LYNX_ERR_TOO_LARGE
+    assert "scratch" in lynx.lynx_status_string(LYNX_ERR_TOO_LARGE)
