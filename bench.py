@@ -43,6 +43,22 @@ def load_peaks() -> dict:
     return dict(FALLBACK_PEAKS)
 
 
+def profiled_traffic(profile: str, source: str):
+    """DRAM bytes per launch recorded by an ncu capture, if the kernel source is still the one captured."""
+    import hashlib
+    import re
+    try:
+        text = open(os.path.join(ROOT, "profiles", profile)).read()
+        src = open(os.path.join(ROOT, "activation_sparse_linear_gb300", "csrc", source), "rb").read()
+    except OSError:
+        return None
+    sha = re.search(r"kernel_source_sha256_prefix:\s*([0-9a-f]+)", text)
+    traffic = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
+    if not sha or not traffic or not hashlib.sha256(src).hexdigest().startswith(sha.group(1)):
+        return None
+    return int(traffic.group(1))
+
+
 def peak_value(peaks: dict, *names, default=None):
     for n in names:
         for k, v in peaks.items():
@@ -131,12 +147,12 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(x: float, world: int) -> float:
+def max_over_ranks(x: float, world: int, device: str = "cuda") -> float:
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -233,7 +249,7 @@ def main() -> int:
     import activation_sparse_linear_gb300 as asl
     import synth
 
-    t = synth.layer_tensors(*WORKLOAD)
+    t = synth.layer_tensors(*WORKLOAD, batch=rank)  # each replica its own batch of tokens, shared weights
     M, N, K, R = t["M"], t["N"], t["K"], t["R"]
     dev = torch.device("cuda", local)
 
@@ -384,7 +400,8 @@ def main() -> int:
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": config_dict(t),
         "roofline": {"bound": "tensor", "achieved": gemm_tf, "peak": sparse_peak, "unit": "TFLOP/s",
-                     "frac": gemm_tf / sparse_peak, "traffic": None,
+                     "frac": gemm_tf / sparse_peak,
+                     "traffic": profiled_traffic("sparse_gemm_pair_qkv.md", "gemm_pair.cu"),
                      "kernel": "sparse GEMM + LoRA-up + s epilogue (tcgen05.mma.sp)",
                      "peak_source": f"2 x dense bf16 burst {dense_tf} TFLOP/s (nominal 2:4 ratio), {peaks['source']}"},
         "cpu_baseline": {"value": cpu_tf, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",

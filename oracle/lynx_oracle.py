@@ -14,7 +14,7 @@ What is computed follows the RT-Lynx page (aitrends.kr article 60737):
 * Technical details: LoRA rank R = 64; QKV and Up/Down linears are sparsified;
   some single-stream layers are left dense (Selective Layer Skipping).
 
-Readings taken where the page is silent (each is listed in the design doc):
+Readings taken where the page is silent:
 
 * groups are 4 consecutive input channels (the K axis) of one token (row);
 * "top-K" means the two largest |x| of each group; ties go to the lower index;

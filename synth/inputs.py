@@ -153,8 +153,8 @@ WORKLOADS = {
 }
 
 
-def _x(wl: Workload, layer: Layer, M: int, block: int) -> np.ndarray:
-    base = (wl.seed, M, block, layer.lid)
+def _x(wl: Workload, layer: Layer, M: int, block: int, batch: int = 0) -> np.ndarray:
+    base = (wl.seed, M, block, layer.lid) + ((batch,) if batch else ())
     chan = (wl.seed, block, layer.lid, 99)
     parts = []
     rows = [M // wl.halves + (1 if h < M % wl.halves else 0) for h in range(wl.halves)]
@@ -169,8 +169,11 @@ def _x(wl: Workload, layer: Layer, M: int, block: int) -> np.ndarray:
 
 
 def layer_tensors(workload: str, layer: str, M: int | None = None, block: int = 0,
-                  with_x: bool = True) -> dict:
-    """Seeded tensors of one linear: X (M x K), W (N x K), LA (N x R), LB (R x K), bf16 bits."""
+                  with_x: bool = True, batch: int = 0) -> dict:
+    """Seeded tensors of one linear: X (M x K), W (N x K), LA (N x R), LB (R x K), bf16 bits.
+
+    ``batch`` > 0 draws another independent batch of activations for the same weights
+    (one per data-parallel replica)."""
     wl = WORKLOADS[workload]
     ly = wl.layer(layer)
     M = wl.M if M is None else M
@@ -182,7 +185,7 @@ def layer_tensors(workload: str, layer: str, M: int | None = None, block: int = 
         "M": M, "N": ly.N, "K": ly.K, "R": wl.rank, "sparse": ly.sparse,
     }
     if with_x:
-        out["X"] = _x(wl, ly, M, block)
+        out["X"] = _x(wl, ly, M, block, batch)
     return out
 
 
