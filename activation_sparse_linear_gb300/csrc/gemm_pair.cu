@@ -3,25 +3,23 @@
 //
 // Two CTAs of a cluster share one 256 x 256 output tile.  CTA r of the pair
 // owns rows 128r..128r+127 of the tile (its TMEM holds their 128 x 256 fp32
-// accumulator) and stages, per 64-channel step, its own 128 rows of A and its
-// half (128 columns) of the W tile; one tcgen05.mma.cta_group::2 issued by
-// the leader CTA (rank 0) multiplies the whole 256 x 256 x K step, reading A
-// and W from both CTAs' shared memory.  Each CTA therefore stages half of the
-// weight bytes a single-CTA 128 x 256 tile would need, which lets 8 stages be
-// in flight within shared memory.
+// accumulator) and stages, per step, its own 128 rows of A and its half (128
+// columns) of the W tile; one tcgen05.mma.cta_group::2 issued by the leader
+// CTA (rank 0) multiplies the whole 256 x 256 x K step, reading A and W from
+// both CTAs' shared memory, so each CTA stages half of the weight bytes a
+// single-CTA 128 x 256 tile would need.
 //
-// Sparse A (compressed values, 64-byte rows, 64-byte swizzle) goes through
-// tcgen05.mma.sp.cta_group::2; every second stage also carries each CTA's
-// 2 KiB metadata chunk for the next 128 channels, which the leader copies
+// Sparse A (compressed values, 128-byte swizzle) goes through
+// tcgen05.mma.sp.cta_group::2 in steps of 128 channels: every stage carries
+// each CTA's 2 KiB metadata chunk of those channels, which the leader copies
 // into both TMEMs with one tcgen05.cp.cta_group::2 (each CTA's own shared
-// memory into its own TMEM).  MMA j of a chunk reads the even column pair
+// memory into its own TMEM); MMA j of the stage reads the even column pair
 // (j & 2) with the sparsity selector j & 1.
 //
 // The LoRA-up branch ("RT-Lynx" page, CUDA kernel optimisation: Yr is produced
-// on chip and accumulated into Ys) is two extra 32-channel stages: A = T'
-// (128 rows x 32, 64-byte rows), B = this CTA's half of LA; dense MMAs into the
-// same accumulator.  Because the epilogue multiplies the tile by s, T' holds
-// (X LB^T)/s.
+// on chip and accumulated into Ys) is one extra stage: A = T' (128 x 64),
+// B = this CTA's half of LA; four dense MMAs into the same accumulator.
+// Because the epilogue multiplies the tile by s, T' holds (X LB^T)/s.
 //
 // Roles per CTA: warp 0 lane 0 TMA producer (both CTAs), warp 1 lane 0 MMA
 // issuer (leader only), warps 2-9 epilogue (two warps per TMEM lane quarter,
@@ -38,27 +36,31 @@ namespace {
 constexpr int ROWS = 128;          // rows per CTA
 constexpr int TN = 256;            // output columns per pair tile (MMA N)
 constexpr int HALF_N = TN / 2;     // W rows staged per CTA
-constexpr int BK = 64;             // logical channels per stage
 constexpr int META_RING = 8;       // TMEM metadata groups
 constexpr int META_GROUP_COLS = 4;
 constexpr int META_COL = TN;       // first metadata column (after the accumulator)
 constexpr int TMEM_COLS = 512;
 constexpr int EPI_WARPS = 8;
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
+constexpr int SUB = HALF_N * 128;  // one 64-channel W sub-tile of this CTA (128 rows x 128 B)
 
 enum Site : int { SITE_PRODUCER = 11, SITE_MMA = 12, SITE_EPILOGUE = 13, SITE_DRAIN = 14 };
 
+// Per stage and CTA: sparse = 128 channels (A: 64 kept values per row, 128-byte rows; W: two 64-channel
+// sub-tiles; one metadata chunk) feeding four tcgen05.mma.sp; dense = 64 channels feeding four tcgen05.mma.
+// Four MMAs per barrier round keep the single issuing thread ahead of the tensor pipe.
 template <bool SPARSE>
 struct PairCfg {
-  static constexpr int A_SLOT = SPARSE ? ROWS * 64 : ROWS * 128;  // LoRA T' halves also fit 8 KiB
-  static constexpr int B_SLOT = HALF_N * 128;
+  static constexpr int BK = SPARSE ? 128 : 64;
+  static constexpr int A_SLOT = ROWS * 128;
+  static constexpr int B_SLOT = SPARSE ? 2 * SUB : SUB;
   static constexpr int M_SLOT = SPARSE ? kMetaChunkBytes : 0;
   static constexpr int STAGE = A_SLOT + B_SLOT + M_SLOT;
-  static constexpr int NST = SPARSE ? 8 : 6;
+  static constexpr int NST = SPARSE ? 4 : 6;
   static constexpr int SMEM = NST * STAGE + 256 + 1024;
   static_assert(STAGE % 1024 == 0, "stage slots keep 1 KiB alignment");
   static_assert(SMEM <= 232448, "shared memory budget");
-  static_assert(NST <= 2 * META_RING, "a metadata group must outlive the stages in flight");
+  static_assert(NST <= META_RING, "a metadata group must outlive the stages in flight");
 };
 
 template <bool SPARSE, bool LORA>
@@ -84,8 +86,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const int num_mp = (a.M + 2 * ROWS - 1) / (2 * ROWS);
   const int num_n = (a.N + TN - 1) / TN;
   const int ntiles = num_mp * num_n;
-  const int nk = (a.K + BK - 1) / BK;
-  const int nstages = nk + (LORA ? 2 : 0);
+  const int nk = (a.K + C::BK - 1) / C::BK;
+  const int nstages = nk + (LORA ? 1 : 0);
   const int64_t blocks_k = meta_blocks_k(a.K);
 
   if (threadIdx.x == 0) {
@@ -123,16 +125,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ TMA producer (both CTAs)
-      int g = 0;
+      constexpr uint32_t STAGE_BYTES = C::A_SLOT + C::B_SLOT + C::M_SLOT;
+      constexpr uint32_t LORA_BYTES = C::A_SLOT + SUB;
+      const uint32_t full_leader0 = mapa_shared(&full[0], 0);  // the leader's full barriers, 8 B apart
+      int g = 0, st = 0;
+      uint32_t ph = 0;
       bool stop = false;
       for (int tile = cluster; tile < ntiles && !stop; tile += nclusters) {
         const int mp = tile % num_mp, nb = tile / num_mp;
         const int m0 = mp * 2 * ROWS + static_cast<int>(rank) * ROWS;
         const int n0 = nb * TN + static_cast<int>(rank) * HALF_N;
-        const int rowblk = mp * 2 + static_cast<int>(rank);
+        const int meta_row = static_cast<int>(2 * ((mp * 2 + static_cast<int>(rank)) * blocks_k));
         for (int it = 0; it < nstages; ++it) {
-          const int st = g % C::NST;
-          const uint32_t ph = (g / C::NST) & 1;
           if (!mbar_wait(&empty[st], ph ^ 1, a.ctl, SITE_PRODUCER) || *abort_flag) {
             *abort_flag = 1;
             stop = true;
@@ -140,27 +144,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           }
           uint8_t* sA = smem + st * C::STAGE;
           uint8_t* sB = sA + C::A_SLOT;
-          uint8_t* sM = sB + C::B_SLOT;
-          const uint32_t fb = mapa_shared(&full[st], 0);  // the leader's full barrier
-          if (a.ctl.inject == 1 && g == 0) {  // test hook: this stage never arrives
-            ++g;
-            continue;
-          }
-          if (it < nk) {
-            const bool meta_stage = SPARSE && (it % 2 == 0);
-            const uint32_t bytes = (SPARSE ? ROWS * 64 : ROWS * 128) + C::B_SLOT + (meta_stage ? C::M_SLOT : 0);
-            if (leader) mbar_arrive_expect_tx(&full[st], 2 * bytes);
-            tma_load_2d_pair(sA, &a.tmA, fb, SPARSE ? it * (BK / 2) : it * BK, m0);
-            tma_load_2d_pair(sB, &a.tmB, fb, it * BK, n0);
-            if (meta_stage)
-              tma_load_2d_pair(sM, &a.tmMeta, fb, 0, static_cast<int>(2 * (rowblk * blocks_k + it / 2)));
-          } else {
-            const int l = it - nk;  // LoRA half: rank channels 32l..32l+31
-            if (leader) mbar_arrive_expect_tx(&full[st], 2 * (ROWS * 64 + HALF_N * 64));
-            tma_load_2d_pair(sA, &a.tmT, fb, 32 * l, m0);
-            tma_load_2d_pair(sB, &a.tmLA, fb, 32 * l, n0);
+          const uint32_t fb = full_leader0 + 8 * st;
+          if (!(a.ctl.inject == 1 && g == 0)) {  // test hook: the first stage never arrives
+            if (it < nk) {
+              if (leader) mbar_arrive_expect_tx(&full[st], 2 * STAGE_BYTES);
+              if constexpr (SPARSE) {
+                tma_load_2d_pair(sA, &a.tmA, fb, it * 64, m0);
+                tma_load_2d_pair(sB, &a.tmB, fb, it * 128, n0);
+                tma_load_2d_pair(sB + SUB, &a.tmB, fb, it * 128 + 64, n0);
+                tma_load_2d_pair(sB + C::B_SLOT, &a.tmMeta, fb, 0, meta_row + 2 * it);
+              } else {
+                tma_load_2d_pair(sA, &a.tmA, fb, it * 64, m0);
+                tma_load_2d_pair(sB, &a.tmB, fb, it * 64, n0);
+              }
+            } else {
+              if (leader) mbar_arrive_expect_tx(&full[st], 2 * LORA_BYTES);
+              tma_load_2d_pair(sA, &a.tmT, fb, 0, m0);
+              tma_load_2d_pair(sB, &a.tmLA, fb, 0, n0);
+            }
           }
           ++g;
+          if (++st == C::NST) {
+            st = 0;
+            ph ^= 1;
+          }
         }
       }
       *issued_sh = g;
@@ -168,9 +175,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0 && leader) {
       // ------------------------------------------------------------ MMA issuer (leader)
+      // Descriptors and TMEM addresses are built once; each stage only adds offsets, so the issuing
+      // thread's work per MMA stays well under the MMA's own duration.
       constexpr uint32_t IDESC = idesc_bf16(2 * ROWS, TN, false);
       constexpr uint32_t IDESC_SP = idesc_bf16(2 * ROWS, TN, true);
-      int g = 0, tcount = 0;
+      constexpr uint64_t STEP = C::STAGE >> 4;  // descriptor start-address units per stage
+      const uint32_t s0 = smem_u32(smem);
+      const uint64_t a0 = sdesc(s0, 16, 1024, SWZ_128B);
+      const uint64_t b0 = sdesc(s0 + C::A_SLOT, 16, 1024, SWZ_128B);
+      const uint64_t e0 = sdesc(s0 + C::A_SLOT + C::B_SLOT, 128, 128, SWZ_NONE);
+      const uint32_t meta0 = tmem + META_COL;
+      int g = 0, st = 0, tcount = 0;
+      uint32_t ph = 0;
       bool stop = false;
       for (int tile = cluster; tile < ntiles && !stop; tile += nclusters, ++tcount) {
         if (!mbar_wait(acc_empty, (tcount & 1) ^ 1, a.ctl, SITE_MMA)) {
@@ -179,37 +195,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
         tc_fence_after();
         for (int it = 0; it < nstages; ++it) {
-          const int st = g % C::NST;
-          const uint32_t ph = (g / C::NST) & 1;
           if (!mbar_wait(&full[st], ph, a.ctl, SITE_MMA)) {
             *abort_flag = 1;
             stop = true;
             break;
           }
           tc_fence_after();
-          const uint32_t sA = smem_u32(smem + st * C::STAGE);
-          const uint32_t sB = sA + C::A_SLOT;
+          const uint64_t ad = a0 + st * STEP, bd = b0 + st * STEP;
+          const uint32_t acc0 = it != 0;
           if (it < nk) {
             if constexpr (SPARSE) {
-              const uint32_t group = tmem + META_COL + ((it / 2) % META_RING) * META_GROUP_COLS;
-              if (it % 2 == 0) tc_cp_pair_128x128b(group, sdesc(sB + C::B_SLOT, 128, 128, SWZ_NONE));
-#pragma unroll
-              for (int j = 0; j < 2; ++j)
-                tc_mma_sp_pair(tmem, sdesc(sA + j * 32, 16, 512, SWZ_64B), sdesc(sB + j * 64, 16, 1024, SWZ_128B),
-                               group + 2 * (it % 2), IDESC_SP | j, (it | j) != 0);
+              const uint32_t grp = meta0 + (it & (META_RING - 1)) * META_GROUP_COLS;
+              tc_cp_pair_128x128b(grp, e0 + st * STEP);
+              // MMA j: A bytes 32j of the 128-byte rows; W sub-tile j/2 at byte 64 (j%2);
+              // metadata column pair j/2 with selector j%2
+              tc_mma_sp_pair(tmem, ad, bd, grp, IDESC_SP, acc0);
+              tc_mma_sp_pair(tmem, ad + 2, bd + 4, grp, IDESC_SP | 1u, 1);
+              tc_mma_sp_pair(tmem, ad + 4, bd + (SUB >> 4), grp + 2, IDESC_SP, 1);
+              tc_mma_sp_pair(tmem, ad + 6, bd + (SUB >> 4) + 4, grp + 2, IDESC_SP | 1u, 1);
             } else {
-#pragma unroll
-              for (int j = 0; j < 4; ++j)
-                tc_mma_pair(tmem, sdesc(sA + j * 32, 16, 1024, SWZ_128B), sdesc(sB + j * 32, 16, 1024, SWZ_128B),
-                            IDESC, (it | j) != 0);
+              tc_mma_pair(tmem, ad, bd, IDESC, acc0);
+              tc_mma_pair(tmem, ad + 2, bd + 2, IDESC, 1);
+              tc_mma_pair(tmem, ad + 4, bd + 4, IDESC, 1);
+              tc_mma_pair(tmem, ad + 6, bd + 6, IDESC, 1);
             }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-              tc_mma_pair(tmem, sdesc(sA + j * 32, 16, 512, SWZ_64B), sdesc(sB + j * 32, 16, 512, SWZ_64B), IDESC, 1);
+          } else {  // LoRA-up: T' (128 x 64) against this CTA's half of LA, four K = 16 steps
+            tc_mma_pair(tmem, ad, bd, IDESC, 1);
+            tc_mma_pair(tmem, ad + 2, bd + 2, IDESC, 1);
+            tc_mma_pair(tmem, ad + 4, bd + 4, IDESC, 1);
+            tc_mma_pair(tmem, ad + 6, bd + 6, IDESC, 1);
           }
           tc_commit_pair(&empty[st], 0x3);
           ++g;
+          if (++st == C::NST) {
+            st = 0;
+            ph ^= 1;
+          }
         }
         if (!stop) tc_commit_pair(acc_full, 0x3);
       }

@@ -69,11 +69,11 @@ struct GemmArgs {
 cudaError_t launch_gemm(int kind, const GemmArgs& a, cudaStream_t st);
 
 struct PairArgs {
-  CUtensorMap tmA;     // sparse: compressed values (box 32 x 128, 64-byte swizzle); dense: X (box 64 x 128)
+  CUtensorMap tmA;     // sparse: compressed values; dense: X (both box 64 x 128, 128-byte swizzle)
   CUtensorMap tmB;     // W, box 64 x 128 (one CTA's half of a 256-wide column tile), 128-byte swizzle
   CUtensorMap tmMeta;  // metadata as uint32 [2 * chunks][256]; box 256 x 2 = one 2 KiB chunk
-  CUtensorMap tmT;     // T' (M x 64), box 32 x 128, 64-byte swizzle
-  CUtensorMap tmLA;    // LA (N x 64), box 32 x 128, 64-byte swizzle
+  CUtensorMap tmT;     // T' (M x 64), box 64 x 128, 128-byte swizzle
+  CUtensorMap tmLA;    // LA (N x 64), box 64 x 128, 128-byte swizzle
   const float* rowscale;
   int scale_mode;      // SCALE_NONE or SCALE_MUL
   void* Y;

@@ -235,12 +235,12 @@ int lynx_linear(const void* X, const void* W, const void* LA, const void* LB, vo
   PairArgs g;
   std::memset(&g, 0, sizeof(g));
   const uint64_t meta_rows = 2 * static_cast<uint64_t>(meta_bytes(M, K) / kMetaChunkBytes);  // 1 KiB rows
-  if (!make_map(&g.tmA, ws.vals, K / 2, M, K / 2, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
+  if (!make_map(&g.tmA, ws.vals, K / 2, M, K / 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&g.tmB, W, K, N, K, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&g.tmMeta, ws.meta, 256, meta_rows, 256, 256, 2, CU_TENSOR_MAP_SWIZZLE_NONE,
                 CU_TENSOR_MAP_DATA_TYPE_UINT32) ||
-      !make_map(&g.tmT, ws.T, R, M, R, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !make_map(&g.tmLA, LA, R, N, R, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B))
+      !make_map(&g.tmT, ws.T, R, M, R, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&g.tmLA, LA, R, N, R, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
     return LYNX_ERR_CUDA;
   g.rowscale = ws.s;
   g.scale_mode = SCALE_MUL;
@@ -282,8 +282,8 @@ int lynx_linear_dense(const void* X, const void* W, const void* LA, const void* 
       !make_map(&g.tmB, W, K, N, K, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
     return LYNX_ERR_CUDA;
   if (lora) {
-    if (!make_map(&g.tmT, workspace, R, M, R, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
-        !make_map(&g.tmLA, LA, R, N, R, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B))
+    if (!make_map(&g.tmT, workspace, R, M, R, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&g.tmLA, LA, R, N, R, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
       return LYNX_ERR_CUDA;
   }
   g.rowscale = nullptr;

@@ -331,6 +331,7 @@ def main() -> int:
     mma_sparse_cp_tf, _ = asl.lynx_mma_rate(2, 20000)
     mma_sparse_c2_tf, _ = asl.lynx_mma_rate(3, 20000)
     mma_sparse_c4_tf, _ = asl.lynx_mma_rate(4, 20000)
+    mma_more = {f"mode{m}": asl.lynx_mma_rate(m, 20000)[0] for m in (5, 6, 7, 8)}
 
     # dense cuBLAS at the same shape, same rotation, same stream
     for i in range(args.warmup):
@@ -427,6 +428,10 @@ def main() -> int:
                                "sparse_with_meta_copy_tflops_effective": mma_sparse_cp_tf,
                                "sparse_commit_every_2_tflops_effective": mma_sparse_c2_tf,
                                "sparse_2commits_every_4_tflops_effective": mma_sparse_c4_tf,
+                               "sparse_a64swizzle_tflops_effective": mma_more["mode5"],
+                               "pair_sparse_a128swizzle_tflops_effective": mma_more["mode6"],
+                               "pair_sparse_a64swizzle_tflops_effective": mma_more["mode7"],
+                               "pair_dense_tflops": mma_more["mode8"],
                                "sparse_gemm_frac_of_microbench": gemm_tf / mma_sparse_tf},
         },
     }

@@ -178,7 +178,17 @@ LYNX_API void lynx_profile_next(void* const* events, int count);
  * resident in tensor memory), mode 2 tcgen05.mma.sp each preceded by the
  * tcgen05.cp of its 2 KiB metadata chunk, mode 3 tcgen05.mma.sp with a
  * tcgen05.commit after every two MMAs, mode 4 with two commits after every
- * four MMAs.  Writes
+ * four MMAs, mode 5 tcgen05.mma.sp with A in 64-byte rows (64-byte swizzle);
+ * modes 6-8 run on CTA pairs (tcgen05 cta_group::2, M = 256 over two SMs):
+ * 6 sparse with 128-byte-swizzled A, 7 sparse with 64-byte-swizzled A,
+ * 8 dense, 9 as 7 with pseudo-random operands, 10 as 7 with varied
+ * metadata, 11 both, 12 as 7 with a barrier wait, fence and multicast
+ * commit per two MMAs, 13 the wait only, 14 the fence only, 15 the
+ * multicast commit only, 16 a commit to the issuing CTA only, 17-19 the
+ * sequence of mode 12 once every 4, 8 or 16 MMAs, 20 as 7 with the
+ * selector alternating, 21 as 7 with the metadata column alternating, 22 as
+ * 7 with the metadata address walking the GEMM's 32-column ring, 23 the
+ * sequence of mode 12 with descriptors built once outside the loop.  Writes
  * the dense-equivalent rate (2*M*N*K per instruction, K = 16 dense or 32
  * logical sparse) in TFLOP/s and in MACs per SM clock.  Synchronises `stream`. */
 LYNX_API int lynx_mma_rate(int mode, int iters, double* tflops, double* macs_per_clock, void* stream);
