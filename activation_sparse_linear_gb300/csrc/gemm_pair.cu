@@ -1,30 +1,37 @@
 // CTA-pair (cta_group::2) tcgen05 GEMM for the RT-Lynx linear layer:
-//   Y[256 x 256 tile] = rowscale o (A_op . W^T) [+ T' . LA^T]
+//   Y = rowscale o (A_op . W^T) [+ T' . LA^T]
 //
-// Two CTAs of a cluster share one 256 x 256 output tile.  CTA r of the pair
-// owns rows 128r..128r+127 of the tile (its TMEM holds their 128 x 256 fp32
-// accumulator) and stages, per step, its own 128 rows of A and its half (128
-// columns) of the W tile; one tcgen05.mma.cta_group::2 issued by the leader
-// CTA (rank 0) multiplies the whole 256 x 256 x K step, reading A and W from
-// both CTAs' shared memory, so each CTA stages half of the weight bytes a
-// single-CTA 128 x 256 tile would need.
+// Two CTAs of a cluster share one output tile of 256 * MB rows x TN columns.
+// CTA r of the pair owns MB blocks of 128 rows (its TMEM holds MB fp32
+// accumulators of 128 x TN) and stages, per step, its own rows of A and its
+// half (TN/2 rows) of the W tile; each tcgen05.mma.cta_group::2 issued by the
+// leader CTA (rank 0) multiplies 256 rows (row block h of both CTAs) by all TN
+// columns, reading A and W from both CTAs' shared memory.
+//
+// The shape is set by the bytes each SM must pull into shared memory per
+// multiply-add, which bounds this kernel: per 128-channel step a CTA stages
+// MB x 16 KiB of compressed A, TN/2 x 256 B of W and MB x 2 KiB of metadata.
+// The sparse path takes MB = 2, TN = 192 (60 KiB per 6.3 M logical MACs,
+// against 50 KiB per 4.2 M for MB = 1, TN = 256); the two accumulators and
+// the metadata ring fill 416 of the 512 TMEM columns.
 //
 // Sparse A (compressed values, 128-byte swizzle) goes through
 // tcgen05.mma.sp.cta_group::2 in steps of 128 channels: every stage carries
-// each CTA's 2 KiB metadata chunk of those channels, which the leader copies
-// into both TMEMs with one tcgen05.cp.cta_group::2 (each CTA's own shared
-// memory into its own TMEM); MMA j of the stage reads the even column pair
-// (j & 2) with the sparsity selector j & 1.
+// each CTA's 2 KiB metadata chunk per row block, which the leader copies into
+// both TMEMs with tcgen05.cp.cta_group::2 (each CTA's own shared memory into
+// its own TMEM); MMA j of a chunk reads the even column pair (j & 2) with the
+// sparsity selector j & 1.
 //
 // The LoRA-up branch ("RT-Lynx" page, CUDA kernel optimisation: Yr is produced
-// on chip and accumulated into Ys) is one extra stage: A = T' (128 x 64),
-// B = this CTA's half of LA; four dense MMAs into the same accumulator.
-// Because the epilogue multiplies the tile by s, T' holds (X LB^T)/s.
+// on chip and accumulated into Ys) is one extra stage: A = T' (128 x 64 per row
+// block), B = this CTA's half of LA; four dense MMAs per row block into the
+// same accumulators.  Because the epilogue multiplies the tile by s, T' holds
+// (X LB^T)/s.
 //
 // Roles per CTA: warp 0 lane 0 TMA producer (both CTAs), warp 1 lane 0 MMA
-// issuer (leader only), warps 2-9 epilogue (two warps per TMEM lane quarter,
-// 128 columns each: TMEM -> registers -> scale -> bf16 -> global).  Every
-// mbarrier wait is bounded.
+// issuer (leader only), warps 2-9 epilogue (two warps per TMEM lane quarter:
+// TMEM -> registers -> scale -> bf16 -> global).  Every mbarrier wait is
+// bounded.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -33,43 +40,70 @@
 namespace lynx {
 namespace {
 
-constexpr int ROWS = 128;          // rows per CTA
-constexpr int TN = 256;            // output columns per pair tile (MMA N)
-constexpr int HALF_N = TN / 2;     // W rows staged per CTA
-constexpr int META_RING = 8;       // TMEM metadata groups
+constexpr int BLOCK = 128;         // rows per TMEM accumulator (one row per lane)
+constexpr int META_RING = 4;       // TMEM metadata stages
 constexpr int META_GROUP_COLS = 4;
-constexpr int META_COL = TN;       // first metadata column (after the accumulator)
 constexpr int TMEM_COLS = 512;
 constexpr int EPI_WARPS = 8;
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
-constexpr int SUB = HALF_N * 128;  // one 64-channel W sub-tile of this CTA (128 rows x 128 B)
+constexpr int SMEM_LIMIT = 232448;
+constexpr int Y_BOX = 32;                          // output staging box: 32 rows x 32 columns bf16 (64-byte rows)
+constexpr int Y_BUF = Y_BOX * Y_BOX * 2;
+constexpr int Y_STAGING = EPI_WARPS * 2 * Y_BUF;   // two boxes per epilogue warp
 
 enum Site : int { SITE_PRODUCER = 11, SITE_MMA = 12, SITE_EPILOGUE = 13, SITE_DRAIN = 14 };
 
-// Per stage and CTA: sparse = 128 channels (A: 64 kept values per row, 128-byte rows; W: two 64-channel
-// sub-tiles; one metadata chunk) feeding four tcgen05.mma.sp; dense = 64 channels feeding four tcgen05.mma.
-// Four MMAs per barrier round keep the single issuing thread ahead of the tensor pipe.
-template <bool SPARSE>
+// Per stage and CTA: sparse = 128 channels (A: 64 kept values per row, 128-byte rows, per row block; W: two
+// 64-channel sub-tiles; one metadata chunk per row block) feeding four tcgen05.mma.sp per row block;
+// dense = 64 channels feeding four tcgen05.mma per row block.  Several MMAs per barrier round keep the
+// single issuing thread ahead of the tensor pipe.
+template <bool SPARSE, int MB, int TN>
 struct PairCfg {
+  static constexpr int ROWS = MB * BLOCK;    // rows per CTA
+  static constexpr int HALF_N = TN / 2;      // W rows staged per CTA
   static constexpr int BK = SPARSE ? 128 : 64;
-  static constexpr int A_SLOT = ROWS * 128;
+  static constexpr int A_BLOCK = BLOCK * 128;
+  static constexpr int A_SLOT = MB * A_BLOCK;
+  static constexpr int SUB = HALF_N * 128;   // one 64-channel W sub-tile of this CTA
   static constexpr int B_SLOT = SPARSE ? 2 * SUB : SUB;
-  static constexpr int M_SLOT = SPARSE ? kMetaChunkBytes : 0;
+  static constexpr int M_SLOT = SPARSE ? MB * kMetaChunkBytes : 0;
   static constexpr int STAGE = A_SLOT + B_SLOT + M_SLOT;
-  static constexpr int NST = SPARSE ? 4 : 6;
-  static constexpr int SMEM = NST * STAGE + 256 + 1024;
+  static constexpr int NST = (SMEM_LIMIT - 1280 - Y_STAGING) / STAGE;
+  static constexpr int SMEM = NST * STAGE + Y_STAGING + 256 + 1024;
+  static constexpr int META_COL = MB * TN;   // first metadata column (after the accumulators)
   static_assert(STAGE % 1024 == 0, "stage slots keep 1 KiB alignment");
-  static_assert(SMEM <= 232448, "shared memory budget");
-  static_assert(NST <= META_RING, "a metadata group must outlive the stages in flight");
+  static_assert(NST >= 2 && SMEM <= SMEM_LIMIT, "shared memory budget");
+  static_assert(TN % 32 == 0 && TN <= 256 && HALF_N % 8 == 0, "MMA N");
+  static_assert(META_COL + (SPARSE ? META_RING * MB * META_GROUP_COLS : 0) <= TMEM_COLS, "TMEM budget");
+  static_assert(!SPARSE || NST <= META_RING, "a metadata group must outlive the stages in flight");
 };
 
-template <bool SPARSE, bool LORA>
+// Stores 32 bf16 columns (16 packed pairs) of one output row starting at column col0, clipped to N.
+__device__ __forceinline__ void store_chunk(__nv_bfloat16* yrow, int col0, int N, bool vec_ok, const uint32_t* p) {
+  if (vec_ok && col0 + 32 <= N) {
+    uint4* dst = reinterpret_cast<uint4*>(yrow + col0);
+#pragma unroll
+    for (int v = 0; v < 4; ++v) dst[v] = make_uint4(p[4 * v], p[4 * v + 1], p[4 * v + 2], p[4 * v + 3]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (col0 + j < N) {
+        const uint32_t w = p[j / 2];
+        reinterpret_cast<uint16_t*>(yrow)[col0 + j] =
+            (j & 1) ? static_cast<uint16_t>(w >> 16) : static_cast<uint16_t>(w & 0xFFFFu);
+      }
+    }
+  }
+}
+
+template <bool SPARSE, bool LORA, int MB, int TN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ PairArgs a) {
-  using C = PairCfg<SPARSE>;
+  using C = PairCfg<SPARSE, MB, TN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::NST * C::STAGE);
+  uint8_t* ystage = smem + C::NST * C::STAGE;  // 1 KiB aligned
+  uint64_t* full = reinterpret_cast<uint64_t*>(ystage + Y_STAGING);
   uint64_t* empty = full + C::NST;
   uint64_t* acc_full = empty + C::NST;
   uint64_t* acc_empty = acc_full + 1;
@@ -83,12 +117,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const uint32_t rank = cluster_ctarank();
   const bool leader = rank == 0;
   const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
-  const int num_mp = (a.M + 2 * ROWS - 1) / (2 * ROWS);
+  const int num_mp = (a.M + 2 * C::ROWS - 1) / (2 * C::ROWS);
   const int num_n = (a.N + TN - 1) / TN;
   const int ntiles = num_mp * num_n;
   const int nk = (a.K + C::BK - 1) / C::BK;
   const int nstages = nk + (LORA ? 1 : 0);
   const int64_t blocks_k = meta_blocks_k(a.K);
+  const int meta_rowblocks = static_cast<int>(round_up(a.M, kMetaRowPad) / kMetaRows);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NST; ++i) {
@@ -111,6 +146,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       prefetch_tmap(&a.tmT);
       prefetch_tmap(&a.tmLA);
     }
+    if (a.y_tma) prefetch_tmap(&a.tmY);
   }
   if (warp == 1) {
     tmem_alloc_pair(tslot, TMEM_COLS);
@@ -125,17 +161,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ TMA producer (both CTAs)
-      constexpr uint32_t STAGE_BYTES = C::A_SLOT + C::B_SLOT + C::M_SLOT;
-      constexpr uint32_t LORA_BYTES = C::A_SLOT + SUB;
+      constexpr uint32_t STAGE_BYTES = C::STAGE;
+      constexpr uint32_t LORA_BYTES = C::A_SLOT + C::SUB;
       const uint32_t full_leader0 = mapa_shared(&full[0], 0);  // the leader's full barriers, 8 B apart
       int g = 0, st = 0;
       uint32_t ph = 0;
       bool stop = false;
       for (int tile = cluster; tile < ntiles && !stop; tile += nclusters) {
         const int mp = tile % num_mp, nb = tile / num_mp;
-        const int m0 = mp * 2 * ROWS + static_cast<int>(rank) * ROWS;
-        const int n0 = nb * TN + static_cast<int>(rank) * HALF_N;
-        const int meta_row = static_cast<int>(2 * ((mp * 2 + static_cast<int>(rank)) * blocks_k));
+        const int m0 = mp * 2 * C::ROWS + static_cast<int>(rank) * C::ROWS;
+        const int n0 = nb * TN + static_cast<int>(rank) * C::HALF_N;
+        int meta_row[MB];  // first 1 KiB row of each row block's metadata chunks
+#pragma unroll
+        for (int h = 0; h < MB; ++h) {
+          int rb = m0 / BLOCK + h;
+          if (rb >= meta_rowblocks) rb = meta_rowblocks - 1;  // rows past the padded M: never stored
+          meta_row[h] = static_cast<int>(2 * (rb * blocks_k));
+        }
         for (int it = 0; it < nstages; ++it) {
           if (!mbar_wait(&empty[st], ph ^ 1, a.ctl, SITE_PRODUCER) || *abort_flag) {
             *abort_flag = 1;
@@ -148,18 +190,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           if (!(a.ctl.inject == 1 && g == 0)) {  // test hook: the first stage never arrives
             if (it < nk) {
               if (leader) mbar_arrive_expect_tx(&full[st], 2 * STAGE_BYTES);
+#pragma unroll
+              for (int h = 0; h < MB; ++h) tma_load_2d_pair(sA + h * C::A_BLOCK, &a.tmA, fb, it * 64, m0 + h * BLOCK);
               if constexpr (SPARSE) {
-                tma_load_2d_pair(sA, &a.tmA, fb, it * 64, m0);
                 tma_load_2d_pair(sB, &a.tmB, fb, it * 128, n0);
-                tma_load_2d_pair(sB + SUB, &a.tmB, fb, it * 128 + 64, n0);
-                tma_load_2d_pair(sB + C::B_SLOT, &a.tmMeta, fb, 0, meta_row + 2 * it);
+                tma_load_2d_pair(sB + C::SUB, &a.tmB, fb, it * 128 + 64, n0);
+#pragma unroll
+                for (int h = 0; h < MB; ++h)
+                  tma_load_2d_pair(sB + C::B_SLOT + h * kMetaChunkBytes, &a.tmMeta, fb, 0, meta_row[h] + 2 * it);
               } else {
-                tma_load_2d_pair(sA, &a.tmA, fb, it * 64, m0);
                 tma_load_2d_pair(sB, &a.tmB, fb, it * 64, n0);
               }
             } else {
               if (leader) mbar_arrive_expect_tx(&full[st], 2 * LORA_BYTES);
-              tma_load_2d_pair(sA, &a.tmT, fb, 0, m0);
+#pragma unroll
+              for (int h = 0; h < MB; ++h) tma_load_2d_pair(sA + h * C::A_BLOCK, &a.tmT, fb, 0, m0 + h * BLOCK);
               tma_load_2d_pair(sB, &a.tmLA, fb, 0, n0);
             }
           }
@@ -177,14 +222,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       // ------------------------------------------------------------ MMA issuer (leader)
       // Descriptors and TMEM addresses are built once; each stage only adds offsets, so the issuing
       // thread's work per MMA stays well under the MMA's own duration.
-      constexpr uint32_t IDESC = idesc_bf16(2 * ROWS, TN, false);
-      constexpr uint32_t IDESC_SP = idesc_bf16(2 * ROWS, TN, true);
-      constexpr uint64_t STEP = C::STAGE >> 4;  // descriptor start-address units per stage
+      constexpr uint32_t IDESC = idesc_bf16(2 * BLOCK, TN, false);
+      constexpr uint32_t IDESC_SP = idesc_bf16(2 * BLOCK, TN, true);
+      constexpr uint64_t STEP = C::STAGE >> 4;    // descriptor start-address units per stage
+      constexpr uint64_t ABLK = C::A_BLOCK >> 4;  // ... per row block of A
+      constexpr uint64_t WSUB = C::SUB >> 4;      // ... per W sub-tile
+      constexpr uint64_t MCHUNK = kMetaChunkBytes >> 4;
       const uint32_t s0 = smem_u32(smem);
       const uint64_t a0 = sdesc(s0, 16, 1024, SWZ_128B);
       const uint64_t b0 = sdesc(s0 + C::A_SLOT, 16, 1024, SWZ_128B);
       const uint64_t e0 = sdesc(s0 + C::A_SLOT + C::B_SLOT, 128, 128, SWZ_NONE);
-      const uint32_t meta0 = tmem + META_COL;
+      const uint32_t meta0 = tmem + C::META_COL;
       int g = 0, st = 0, tcount = 0;
       uint32_t ph = 0;
       bool stop = false;
@@ -205,25 +253,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           const uint32_t acc0 = it != 0;
           if (it < nk) {
             if constexpr (SPARSE) {
-              const uint32_t grp = meta0 + (it & (META_RING - 1)) * META_GROUP_COLS;
-              tc_cp_pair_128x128b(grp, e0 + st * STEP);
-              // MMA j: A bytes 32j of the 128-byte rows; W sub-tile j/2 at byte 64 (j%2);
-              // metadata column pair j/2 with selector j%2
-              tc_mma_sp_pair(tmem, ad, bd, grp, IDESC_SP, acc0);
-              tc_mma_sp_pair(tmem, ad + 2, bd + 4, grp, IDESC_SP | 1u, 1);
-              tc_mma_sp_pair(tmem, ad + 4, bd + (SUB >> 4), grp + 2, IDESC_SP, 1);
-              tc_mma_sp_pair(tmem, ad + 6, bd + (SUB >> 4) + 4, grp + 2, IDESC_SP | 1u, 1);
+              const uint32_t grp0 = meta0 + (it & (META_RING - 1)) * (MB * META_GROUP_COLS);
+#pragma unroll
+              for (int h = 0; h < MB; ++h)
+                tc_cp_pair_128x128b(grp0 + h * META_GROUP_COLS, e0 + st * STEP + h * MCHUNK);
+#pragma unroll
+              for (int h = 0; h < MB; ++h) {
+                // MMA j: A bytes 32j of the 128-byte rows of row block h; W sub-tile j/2 at byte 64 (j%2);
+                // metadata column pair j/2 of row block h's group with selector j%2
+                const uint32_t d = tmem + h * TN, grp = grp0 + h * META_GROUP_COLS;
+                const uint64_t ah = ad + h * ABLK;
+                tc_mma_sp_pair(d, ah, bd, grp, IDESC_SP, acc0);
+                tc_mma_sp_pair(d, ah + 2, bd + 4, grp, IDESC_SP | 1u, 1);
+                tc_mma_sp_pair(d, ah + 4, bd + WSUB, grp + 2, IDESC_SP, 1);
+                tc_mma_sp_pair(d, ah + 6, bd + WSUB + 4, grp + 2, IDESC_SP | 1u, 1);
+              }
             } else {
-              tc_mma_pair(tmem, ad, bd, IDESC, acc0);
-              tc_mma_pair(tmem, ad + 2, bd + 2, IDESC, 1);
-              tc_mma_pair(tmem, ad + 4, bd + 4, IDESC, 1);
-              tc_mma_pair(tmem, ad + 6, bd + 6, IDESC, 1);
+#pragma unroll
+              for (int h = 0; h < MB; ++h) {
+                const uint32_t d = tmem + h * TN;
+                const uint64_t ah = ad + h * ABLK;
+                tc_mma_pair(d, ah, bd, IDESC, acc0);
+                tc_mma_pair(d, ah + 2, bd + 2, IDESC, 1);
+                tc_mma_pair(d, ah + 4, bd + 4, IDESC, 1);
+                tc_mma_pair(d, ah + 6, bd + 6, IDESC, 1);
+              }
             }
-          } else {  // LoRA-up: T' (128 x 64) against this CTA's half of LA, four K = 16 steps
-            tc_mma_pair(tmem, ad, bd, IDESC, 1);
-            tc_mma_pair(tmem, ad + 2, bd + 2, IDESC, 1);
-            tc_mma_pair(tmem, ad + 4, bd + 4, IDESC, 1);
-            tc_mma_pair(tmem, ad + 6, bd + 6, IDESC, 1);
+          } else {  // LoRA-up: T' (128 x 64 per row block) against this CTA's half of LA, four K = 16 steps
+#pragma unroll
+            for (int h = 0; h < MB; ++h) {
+              const uint32_t d = tmem + h * TN;
+              const uint64_t ah = ad + h * ABLK;
+              tc_mma_pair(d, ah, bd, IDESC, 1);
+              tc_mma_pair(d, ah + 2, bd + 2, IDESC, 1);
+              tc_mma_pair(d, ah + 4, bd + 4, IDESC, 1);
+              tc_mma_pair(d, ah + 6, bd + 6, IDESC, 1);
+            }
           }
           tc_commit_pair(&empty[st], 0x3);
           ++g;
@@ -240,61 +305,78 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     }
   } else {
     // -------------------------------------------------------------- epilogue (both CTAs)
-    const int q = warp & 3;                  // TMEM lane quarter this warp may access
-    const int half = (warp - 2) / 4;          // which 128 of the 256 columns
-    constexpr int COLS = TN / 2;
+    // Two warps per TMEM lane quarter q: with two row blocks each drains one block's 32 rows over all TN
+    // columns; with one row block each drains half of the columns.  Chunks of 32 columns are read two at a
+    // time; the accumulators are released as soon as the last read has landed.  With y_tma each chunk is
+    // written as a bf16 32 x 32 box into this warp's staging buffer (64-byte swizzle, so that the 32 lanes
+    // writing one row each hit distinct banks) and stored by TMA; otherwise lanes store their rows directly.
+    const int q = warp & 3;
+    const int w2 = (warp - 2) / 4;
+    const int h = MB == 2 ? w2 : 0;
+    constexpr int COLS = MB == 2 ? TN : TN / 2;
+    constexpr int NC = COLS / 32;
+    static_assert(NC % 2 == 0, "chunks are drained in pairs");
+    const int col_off = MB == 2 ? 0 : w2 * COLS;
     const bool vec_ok = (a.ldy % 8) == 0;
     const bool scaled = a.scale_mode == SCALE_MUL;
+    const bool y_tma = a.y_tma != 0;
+    uint8_t* ybuf = ystage + (warp - 2) * 2 * Y_BUF;
     const uint32_t acc_empty_leader = mapa_shared(acc_empty, 0);
+    const uint32_t taddr_warp = tmem + (static_cast<uint32_t>(q * 32) << 16) + h * TN + col_off;
     int tcount = 0;
     for (int tile = cluster; tile < ntiles; tile += nclusters, ++tcount) {
+      const int mp = tile % num_mp, nb = tile / num_mp;
+      const int row0 = mp * 2 * C::ROWS + static_cast<int>(rank) * C::ROWS + h * BLOCK + q * 32;
+      const int row = row0 + lane;
+      const int n0 = nb * TN + col_off;
+      const float sc = (scaled && row < a.M) ? a.rowscale[row] : 1.f;  // issued before the wait
       bool ok = mbar_wait(acc_full, tcount & 1, a.ctl, SITE_EPILOGUE);
       ok = __all_sync(0xFFFFFFFFu, ok) && !*abort_flag;
       if (!ok) break;
       tc_fence_after();
-      const int mp = tile % num_mp, nb = tile / num_mp;
-      const int row = mp * 2 * ROWS + static_cast<int>(rank) * ROWS + q * 32 + lane;
-      const int n0 = nb * TN + half * COLS;
-      const float sc = (scaled && row < a.M) ? a.rowscale[row] : 1.f;
-      uint32_t packed[COLS / 2];
+      __nv_bfloat16* yrow = static_cast<__nv_bfloat16*>(a.Y) + static_cast<int64_t>(row) * a.ldy;
+      const bool live = row < a.M;
 #pragma unroll
-      for (int c = 0; c < COLS / 32; ++c) {
-        uint32_t r[32];
-        tc_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + half * COLS + c * 32, r);
+      for (int c2 = 0; c2 < NC; c2 += 2) {
+        uint32_t r0[32], r1[32];
+        tc_ld_32x32b_x32(taddr_warp + c2 * 32, r0);
+        tc_ld_32x32b_x32(taddr_warp + (c2 + 1) * 32, r1);
         tc_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[2 * j]) * sc, __uint_as_float(r[2 * j + 1]) * sc);
-          packed[c * 16 + j] = *reinterpret_cast<uint32_t*>(&h);
+        if (c2 + 2 == NC) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(acc_empty_leader);  // the pair's accumulators may be overwritten
         }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(acc_empty_leader);  // the pair's accumulator may be overwritten
-      if (row < a.M) {
-        __nv_bfloat16* yrow = static_cast<__nv_bfloat16*>(a.Y) + static_cast<int64_t>(row) * a.ldy;
+        if (y_tma) {
+          if (lane == 0) bulk_wait_read_all();  // both staging boxes free again
+          __syncwarp();
+        }
 #pragma unroll
-        for (int c = 0; c < COLS / 32; ++c) {
-          const int col0 = n0 + c * 32;
-          if (vec_ok && col0 + 32 <= a.N) {
-            uint4* dst = reinterpret_cast<uint4*>(yrow + col0);
+        for (int u = 0; u < 2; ++u) {
+          uint32_t* rr = u ? r1 : r0;
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
-              dst[v] = make_uint4(packed[c * 16 + 4 * v], packed[c * 16 + 4 * v + 1], packed[c * 16 + 4 * v + 2],
-                                  packed[c * 16 + 4 * v + 3]);
-          } else {
+          for (int j = 0; j < 16; ++j) {
+            __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(rr[2 * j]) * sc, __uint_as_float(rr[2 * j + 1]) * sc);
+            rr[j] = *reinterpret_cast<uint32_t*>(&v);
+          }
+          const int col0 = n0 + (c2 + u) * 32;
+          if (y_tma) {
+            uint8_t* box = ybuf + u * Y_BUF;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              if (col0 + j < a.N) {
-                const uint32_t w = packed[c * 16 + j / 2];
-                reinterpret_cast<uint16_t*>(yrow)[col0 + j] =
-                    (j & 1) ? static_cast<uint16_t>(w >> 16) : static_cast<uint16_t>(w & 0xFFFFu);
-              }
-            }
+            for (int v = 0; v < 4; ++v)  // 16-byte piece v of this lane's 64-byte row, 64-byte swizzle
+              *reinterpret_cast<uint4*>(box + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4)) =
+                  make_uint4(rr[4 * v], rr[4 * v + 1], rr[4 * v + 2], rr[4 * v + 3]);
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0 && col0 < a.N && row0 < a.M) tma_store_2d(&a.tmY, box, col0, row0);
+          } else if (live) {
+            store_chunk(yrow, col0, a.N, vec_ok, rr);
           }
         }
+        if (y_tma && lane == 0) bulk_commit();
       }
     }
+    if (y_tma && lane == 0) bulk_wait_all();
   }
   __syncwarp();
   __syncthreads();
@@ -316,10 +398,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   }
 }
 
-template <bool SPARSE, bool LORA>
+template <bool SPARSE, bool LORA, int MB, int TN>
 cudaError_t launch(const PairArgs& a, cudaStream_t st) {
-  using C = PairCfg<SPARSE>;
-  auto* k = gemm_pair_kernel<SPARSE, LORA>;
+  using C = PairCfg<SPARSE, MB, TN>;
+  auto* k = gemm_pair_kernel<SPARSE, LORA, MB, TN>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -330,7 +412,7 @@ cudaError_t launch(const PairArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  const int ntiles = ((a.M + 2 * ROWS - 1) / (2 * ROWS)) * ((a.N + TN - 1) / TN);
+  const int ntiles = ((a.M + 2 * C::ROWS - 1) / (2 * C::ROWS)) * ((a.N + TN - 1) / TN);
   int clusters = sm_count() / 2;
   if (clusters > ntiles) clusters = ntiles;
   if (clusters < 1) clusters = 1;
@@ -341,8 +423,9 @@ cudaError_t launch(const PairArgs& a, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_gemm_pair(bool sparse, bool lora, const PairArgs& a, cudaStream_t st) {
-  if (sparse) return lora ? launch<true, true>(a, st) : launch<true, false>(a, st);
-  return lora ? launch<false, true>(a, st) : launch<false, false>(a, st);
+  constexpr int MBs = kPairSparseRowBlocks, TNs = kPairSparseTileN, TNd = kPairDenseTileN;
+  if (sparse) return lora ? launch<true, true, MBs, TNs>(a, st) : launch<true, false, MBs, TNs>(a, st);
+  return lora ? launch<false, true, 1, TNd>(a, st) : launch<false, false, 1, TNd>(a, st);
 }
 
 }  // namespace lynx

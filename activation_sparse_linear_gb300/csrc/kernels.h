@@ -68,12 +68,20 @@ struct GemmArgs {
 // 3 = sparse, no LoRA; 4 = dense, 64-wide tiles (LoRA down-projection).
 cudaError_t launch_gemm(int kind, const GemmArgs& a, cudaStream_t st);
 
+// Pair-tile shapes: the sparse path gives each CTA two 128-row blocks (a 512 x 192 output tile per pair),
+// the dense path one (256 x 256).  W and LA are staged TileN/2 rows per CTA.
+constexpr int kPairSparseRowBlocks = 2;
+constexpr int kPairSparseTileN = 192;
+constexpr int kPairDenseTileN = 256;
+
 struct PairArgs {
   CUtensorMap tmA;     // sparse: compressed values; dense: X (both box 64 x 128, 128-byte swizzle)
-  CUtensorMap tmB;     // W, box 64 x 128 (one CTA's half of a 256-wide column tile), 128-byte swizzle
+  CUtensorMap tmB;     // W, box 64 x TileN/2 (one CTA's half of a column tile), 128-byte swizzle
   CUtensorMap tmMeta;  // metadata as uint32 [2 * chunks][256]; box 256 x 2 = one 2 KiB chunk
   CUtensorMap tmT;     // T' (M x 64), box 64 x 128, 128-byte swizzle
-  CUtensorMap tmLA;    // LA (N x 64), box 64 x 128, 128-byte swizzle
+  CUtensorMap tmLA;    // LA (N x 64), box 64 x TileN/2, 128-byte swizzle
+  CUtensorMap tmY;     // Y (M x N bf16), box 32 x 32, 64-byte swizzle; used when y_tma != 0 (N % 8 == 0)
+  int y_tma;
   const float* rowscale;
   int scale_mode;      // SCALE_NONE or SCALE_MUL
   void* Y;
@@ -82,7 +90,7 @@ struct PairArgs {
   DevCtl ctl;
 };
 
-// The CTA-pair (cta_group::2) GEMM on 256 x 256 output tiles.
+// The CTA-pair (cta_group::2) GEMM.
 cudaError_t launch_gemm_pair(bool sparse, bool lora, const PairArgs& a, cudaStream_t st);
 
 // T[m, r] = bf16( sum_s partial[s][m][r] / s[m] ) for the split-K LoRA down-projection.

@@ -89,6 +89,16 @@ bool make_map(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows, u
   return r == CUDA_SUCCESS;
 }
 
+// Output tensor map for the pair GEMM's TMA-store epilogue: rows of N bf16 need a 16-byte multiple stride,
+// so other N keep the direct per-lane stores.
+bool set_y_map(PairArgs* g, void* Y, int64_t M, int64_t N) {
+  g->y_tma = 0;
+  if (N % 8 != 0) return true;
+  if (!make_map(&g->tmY, Y, N, M, N, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)) return false;
+  g->y_tma = 1;
+  return true;
+}
+
 bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) != 0; }
 
 int check_mk(int64_t M, int64_t K) {
@@ -236,12 +246,13 @@ int lynx_linear(const void* X, const void* W, const void* LA, const void* LB, vo
   std::memset(&g, 0, sizeof(g));
   const uint64_t meta_rows = 2 * static_cast<uint64_t>(meta_bytes(M, K) / kMetaChunkBytes);  // 1 KiB rows
   if (!make_map(&g.tmA, ws.vals, K / 2, M, K / 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&g.tmB, W, K, N, K, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&g.tmB, W, K, N, K, 64, kPairSparseTileN / 2, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&g.tmMeta, ws.meta, 256, meta_rows, 256, 256, 2, CU_TENSOR_MAP_SWIZZLE_NONE,
                 CU_TENSOR_MAP_DATA_TYPE_UINT32) ||
       !make_map(&g.tmT, ws.T, R, M, R, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&g.tmLA, LA, R, N, R, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+      !make_map(&g.tmLA, LA, R, N, R, 64, kPairSparseTileN / 2, CU_TENSOR_MAP_SWIZZLE_128B))
     return LYNX_ERR_CUDA;
+  if (!set_y_map(&g, Y, M, N)) return LYNX_ERR_CUDA;
   g.rowscale = ws.s;
   g.scale_mode = SCALE_MUL;
   g.Y = Y;
@@ -279,13 +290,14 @@ int lynx_linear_dense(const void* X, const void* W, const void* LA, const void* 
   PairArgs g;
   std::memset(&g, 0, sizeof(g));
   if (!make_map(&g.tmA, X, K, M, K, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&g.tmB, W, K, N, K, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+      !make_map(&g.tmB, W, K, N, K, 64, kPairDenseTileN / 2, CU_TENSOR_MAP_SWIZZLE_128B))
     return LYNX_ERR_CUDA;
   if (lora) {
     if (!make_map(&g.tmT, workspace, R, M, R, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&g.tmLA, LA, R, N, R, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+        !make_map(&g.tmLA, LA, R, N, R, 64, kPairDenseTileN / 2, CU_TENSOR_MAP_SWIZZLE_128B))
       return LYNX_ERR_CUDA;
   }
+  if (!set_y_map(&g, Y, M, N)) return LYNX_ERR_CUDA;
   g.rowscale = nullptr;
   g.scale_mode = SCALE_NONE;
   g.Y = Y;

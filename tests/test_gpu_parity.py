@@ -78,8 +78,9 @@ def test_lora_down(lynx, M, K, scaled):
     assert_y_close(to_bits(T), O.lora_down(X, LB, s), "T")
 
 
+# N % 8 != 0 (1003, 130) takes the per-lane store epilogue; the others the TMA-store epilogue
 LINEAR_CASES = [(256, 512, 512), (300, 520, 528), (1, 8, 16), (129, 136, 144), (200, 1000, 1024),
-                (128, 256, 64), (384, 768, 3072)]
+                (128, 256, 64), (384, 768, 3072), (200, 1003, 256), (600, 1160, 384)]
 
 
 def _layer(M, N, K, seed=7, xkind="act"):
@@ -136,7 +137,7 @@ def test_linear_zero_lora_and_24_input_is_cublas_gemm(lynx):
 
 
 @pytest.mark.parametrize("M,N,K,lora", [(256, 512, 512, False), (300, 520, 528, True), (129, 136, 144, False),
-                                        (384, 768, 3072, True)])
+                                        (384, 768, 3072, True), (129, 130, 144, True)])
 def test_linear_dense(lynx, M, N, K, lora):
     X, W, LA, LB = _layer(M, N, K, 17)
     if lora:
