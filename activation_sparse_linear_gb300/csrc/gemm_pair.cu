@@ -45,7 +45,8 @@ constexpr int META_RING = 4;       // TMEM metadata stages
 constexpr int META_GROUP_COLS = 4;
 constexpr int TMEM_COLS = 512;
 constexpr int EPI_WARPS = 8;
-constexpr int THREADS = 64 + 32 * EPI_WARPS;
+constexpr int MMA_WARP2 = 2 + EPI_WARPS;         // second MMA issuer (two row blocks per CTA)
+constexpr int THREADS = 96 + 32 * EPI_WARPS;
 constexpr int SMEM_LIMIT = 232448;
 constexpr int Y_BOX = 32;                          // output staging box: 32 rows x 32 columns bf16 (64-byte rows)
 constexpr int Y_BUF = Y_BOX * Y_BOX * 2;
@@ -100,6 +101,10 @@ template <bool SPARSE, bool LORA, int MB, int TN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ PairArgs a) {
   using C = PairCfg<SPARSE, MB, TN>;
+  // With two row blocks, two threads issue the MMAs (one row block each): while one waits on a barrier or
+  // does its per-stage bookkeeping, the other's queued MMAs keep the tensor pipe busy.
+  constexpr int NISS = MB >= 2 ? 2 : 1;
+  static_assert(MB % NISS == 0, "row blocks split evenly between the issuers");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ystage = smem + C::NST * C::STAGE;  // 1 KiB aligned
@@ -110,8 +115,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   uint64_t* drain = acc_empty + 1;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
-  volatile int* consumed_sh = abort_flag + 1;
-  volatile int* issued_sh = abort_flag + 2;
+  volatile int* consumed_sh = abort_flag + 1;  // one count per MMA issuer
+  volatile int* issued_sh = abort_flag + 3;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -128,13 +133,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NST; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+      mbar_init(&empty[i], NISS);  // one commit per MMA issuer
     }
-    mbar_init(acc_full, 1);
+    mbar_init(acc_full, NISS);
     mbar_init(acc_empty, 2 * EPI_WARPS);  // every epilogue warp of both CTAs of the pair
-    mbar_init(drain, 1);
+    mbar_init(drain, NISS);
     *abort_flag = 0;
-    *consumed_sh = 0;
+    consumed_sh[0] = 0;
+    consumed_sh[1] = 0;
     *issued_sh = 0;
     fence_mbar_init();
   }
@@ -217,9 +223,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       }
       *issued_sh = g;
     }
-  } else if (warp == 1) {
-    if (lane == 0 && leader) {
-      // ------------------------------------------------------------ MMA issuer (leader)
+  } else if (warp == 1 || warp == MMA_WARP2) {
+    const int k = warp == 1 ? 0 : 1;  // issuer index: row blocks h = k, k + NISS, ...
+    if (lane == 0 && leader && k < NISS) {
+      // ------------------------------------------------------------ MMA issuers (leader)
       // Descriptors and TMEM addresses are built once; each stage only adds offsets, so the issuing
       // thread's work per MMA stays well under the MMA's own duration.
       constexpr uint32_t IDESC = idesc_bf16(2 * BLOCK, TN, false);
@@ -255,10 +262,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             if constexpr (SPARSE) {
               const uint32_t grp0 = meta0 + (it & (META_RING - 1)) * (MB * META_GROUP_COLS);
 #pragma unroll
-              for (int h = 0; h < MB; ++h)
+              for (int hh = 0; hh < MB / NISS; ++hh) {
+                const int h = k + hh * NISS;
                 tc_cp_pair_128x128b(grp0 + h * META_GROUP_COLS, e0 + st * STEP + h * MCHUNK);
+              }
 #pragma unroll
-              for (int h = 0; h < MB; ++h) {
+              for (int hh = 0; hh < MB / NISS; ++hh) {
+                const int h = k + hh * NISS;
                 // MMA j: A bytes 32j of the 128-byte rows of row block h; W sub-tile j/2 at byte 64 (j%2);
                 // metadata column pair j/2 of row block h's group with selector j%2
                 const uint32_t d = tmem + h * TN, grp = grp0 + h * META_GROUP_COLS;
@@ -270,7 +280,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
               }
             } else {
 #pragma unroll
-              for (int h = 0; h < MB; ++h) {
+              for (int hh = 0; hh < MB / NISS; ++hh) {
+                const int h = k + hh * NISS;
                 const uint32_t d = tmem + h * TN;
                 const uint64_t ah = ad + h * ABLK;
                 tc_mma_pair(d, ah, bd, IDESC, acc0);
@@ -281,7 +292,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             }
           } else {  // LoRA-up: T' (128 x 64 per row block) against this CTA's half of LA, four K = 16 steps
 #pragma unroll
-            for (int h = 0; h < MB; ++h) {
+            for (int hh = 0; hh < MB / NISS; ++hh) {
+              const int h = k + hh * NISS;
               const uint32_t d = tmem + h * TN;
               const uint64_t ah = ad + h * ABLK;
               tc_mma_pair(d, ah, bd, IDESC, 1);
@@ -299,12 +311,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
         if (!stop) tc_commit_pair(acc_full, 0x3);
       }
-      *consumed_sh = g;
-      tc_commit_pair(drain, 0x1);  // every MMA this pair issued has completed once this fires
+      consumed_sh[k] = g;
+      tc_commit_pair(drain, 0x1);  // every MMA of both issuers has completed once this phase completes
       mbar_wait(drain, 0, a.ctl, SITE_DRAIN);
     }
   } else {
-    // -------------------------------------------------------------- epilogue (both CTAs)
+    // -------------------------------------------------------------- epilogue (both CTAs, warps 2..9)
     // Two warps per TMEM lane quarter q: with two row blocks each drains one block's 32 rows over all TN
     // columns; with one row block each drains half of the columns.  Chunks of 32 columns are read two at a
     // time; the accumulators are released as soon as the last read has landed.  With y_tma each chunk is
@@ -336,44 +348,59 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       tc_fence_after();
       __nv_bfloat16* yrow = static_cast<__nv_bfloat16*>(a.Y) + static_cast<int64_t>(row) * a.ldy;
       const bool live = row < a.M;
+      // Drain: the whole 32 x COLS slice is read into registers (converted to bf16 pairs) before anything is
+      // written out, so the accumulators are released after three TMEM round trips.
+      uint32_t pk[(NC - 2) * 16 + 1];
+      uint32_t r0[32], r1[32];
 #pragma unroll
       for (int c2 = 0; c2 < NC; c2 += 2) {
-        uint32_t r0[32], r1[32];
         tc_ld_32x32b_x32(taddr_warp + c2 * 32, r0);
         tc_ld_32x32b_x32(taddr_warp + (c2 + 1) * 32, r1);
         tc_wait_ld();
         if (c2 + 2 == NC) {
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(acc_empty_leader);  // the pair's accumulators may be overwritten
-        }
-        if (y_tma) {
-          if (lane == 0) bulk_wait_read_all();  // both staging boxes free again
-          __syncwarp();
+          // the pair's accumulators may be overwritten: this warp's TMEM reads have completed (wait::ld)
+          if (lane == 0) mbar_arrive_cluster_relaxed(acc_empty_leader);
         }
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          uint32_t* rr = u ? r1 : r0;
+        for (int j = 0; j < 16; ++j) {
+          __nv_bfloat162 v0 = __floats2bfloat162_rn(__uint_as_float(r0[2 * j]) * sc, __uint_as_float(r0[2 * j + 1]) * sc);
+          __nv_bfloat162 v1 = __floats2bfloat162_rn(__uint_as_float(r1[2 * j]) * sc, __uint_as_float(r1[2 * j + 1]) * sc);
+          r0[j] = *reinterpret_cast<uint32_t*>(&v0);
+          r1[j] = *reinterpret_cast<uint32_t*>(&v1);
+        }
+        if (c2 + 2 < NC) {
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(rr[2 * j]) * sc, __uint_as_float(rr[2 * j + 1]) * sc);
-            rr[j] = *reinterpret_cast<uint32_t*>(&v);
-          }
-          const int col0 = n0 + (c2 + u) * 32;
-          if (y_tma) {
-            uint8_t* box = ybuf + u * Y_BUF;
-#pragma unroll
-            for (int v = 0; v < 4; ++v)  // 16-byte piece v of this lane's 64-byte row, 64-byte swizzle
-              *reinterpret_cast<uint4*>(box + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4)) =
-                  make_uint4(rr[4 * v], rr[4 * v + 1], rr[4 * v + 2], rr[4 * v + 3]);
-            fence_proxy_async();
-            __syncwarp();
-            if (lane == 0 && col0 < a.N && row0 < a.M) tma_store_2d(&a.tmY, box, col0, row0);
-          } else if (live) {
-            store_chunk(yrow, col0, a.N, vec_ok, rr);
+            pk[c2 * 16 + j] = r0[j];
+            pk[(c2 + 1) * 16 + j] = r1[j];
           }
         }
-        if (y_tma && lane == 0) bulk_commit();
+      }
+      // Write-out, overlapping the next tile's main loop: one bulk group per chunk, the two staging boxes
+      // used alternately (NC is even, so every tile starts on box 0).
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        const uint32_t* p = c < NC - 2 ? pk + c * 16 : (c == NC - 2 ? r0 : r1);
+        const int col0 = n0 + c * 32;
+        if (y_tma) {
+          uint8_t* box = ybuf + (c & 1) * Y_BUF;
+          if (lane == 0) bulk_wait_read_one();  // the store that last used this box has read it
+          __syncwarp();
+#pragma unroll
+          for (int v = 0; v < 4; ++v)  // 16-byte piece v of this lane's 64-byte row, 64-byte swizzle
+            *reinterpret_cast<uint4*>(box + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4)) =
+                make_uint4(p[4 * v], p[4 * v + 1], p[4 * v + 2], p[4 * v + 3]);
+          fence_proxy_async();
+          __syncwarp();
+          if (lane == 0) {
+            if (col0 < a.N && row0 < a.M) tma_store_2d(&a.tmY, box, col0, row0);
+            bulk_commit();
+          }
+        } else if (live) {
+          store_chunk(yrow, col0, a.N, vec_ok, p);
+        }
       }
     }
     if (y_tma && lane == 0) bulk_wait_all();
@@ -384,7 +411,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   if (*abort_flag && leader && warp == 0 && lane == 0) {
     // Let every copy of this stage sequence land (both CTAs signal the leader's barriers).
     const int issued = *issued_sh;
-    for (int g = *consumed_sh; g < issued; ++g) {
+    const int consumed = NISS == 2 && consumed_sh[1] < consumed_sh[0] ? consumed_sh[1] : consumed_sh[0];
+    for (int g = consumed; g < issued; ++g) {
       if (a.ctl.inject == 1 && g == 0) continue;
       if (!mbar_wait(&full[g % C::NST], (g / C::NST) & 1, a.ctl, SITE_DRAIN)) break;
     }

@@ -57,6 +57,32 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint64_t* bar, uint32_t parity
       : "memory");
   return ok;
 }
+// Non-blocking probe of the phase with the given parity (never suspends the thread).
+__device__ __forceinline__ uint32_t mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok;
+}
+// Bounded spin on mbar_test_wait: for barriers completed by arrivals from the peer CTA, where a suspended
+// try_wait was seen to resume up to about a microsecond after the phase completed.
+__device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity, const DevCtl& c, int site) {
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_test_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > c.wait_ns) {
+      record_error(c, site);
+      return false;
+    }
+  }
+}
 // Bounded wait for the phase with the given parity.  Returns false (and records
 // `site` in the error word) once c.wait_ns has passed.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const DevCtl& c, int site) {
@@ -98,6 +124,7 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, const void* 
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until no bulk group of this thread still reads shared memory / until all have completed.
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_one() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
@@ -210,6 +237,13 @@ __device__ __forceinline__ uint32_t mapa_shared(const void* p, uint32_t rank) {
   uint32_t d;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(smem_u32(p)), "r"(rank));
   return d;
+}
+// Relaxed arrive on a cluster-mapped mbarrier: no release fence.  For arrivals that only announce that
+// work which has already completed (e.g. TMEM reads finished by tcgen05.wait::ld) may be overwritten;
+// the release form waits for the arriving thread's outstanding memory operations and was measured to
+// delay the waiter by over a microsecond.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
