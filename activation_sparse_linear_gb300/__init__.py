@@ -18,7 +18,8 @@ from ._build import LIB, build, up_to_date
 __all__ = [
     "LynxError", "lib", "LYNX_OK", "LYNX_ERR_TIMEOUT",
     "lynx_meta_bytes", "lynx_workspace_bytes", "lynx_dense_workspace_bytes",
-    "lynx_sparsify", "lynx_lora_down", "lynx_linear", "lynx_linear_dense",
+    "lynx_sparsify", "lynx_sparsify_lora", "lynx_lora_down", "lynx_linear",
+    "lynx_linear_dense",
     "lynx_sync_status", "lynx_status_string", "lynx_meta_to_canonical", "lynx_debug_set_fault",
     "lynx_profile_next", "lynx_linear_kernel_count", "lynx_mma_rate",
 ]
@@ -39,6 +40,7 @@ def _load() -> ctypes.CDLL:
         "lynx_dense_workspace_bytes": (_c_sz, [_c_i64, _c_i64]),
         "lynx_sparsify": (ctypes.c_int, [_c_p, _c_i64, _c_i64, _c_p, _c_p, _c_p, _c_p]),
         "lynx_lora_down": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_p]),
+        "lynx_sparsify_lora": (ctypes.c_int, [_c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_p, _c_p, _c_p, _c_p, _c_p]),
         "lynx_linear": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_i64, _c_p, _c_sz, _c_p]),
         "lynx_linear_dense": (ctypes.c_int,
                               [_c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_i64, _c_p, _c_sz, _c_p]),
@@ -119,6 +121,24 @@ def lynx_sparsify(X, vals=None, meta=None, s=None, stream=None):
     s = torch.empty(M, dtype=torch.float32, device=X.device) if s is None else s
     _check(lib.lynx_sparsify(_ptr(X), M, K, _ptr(vals), _ptr(meta), _ptr(s), _stream(stream)), "lynx_sparsify")
     return vals, meta, s
+
+
+def lynx_sparsify_lora(X, LB=None, vals=None, meta=None, s=None, T=None, stream=None):
+    """One pass over X: (vals, meta, s) as lynx_sparsify and, with LB, T = bf16(X LB^T / s) (else None)."""
+    torch = _torch()
+    _need(X, "X", torch.bfloat16)
+    M, K = X.shape
+    R = 64
+    if LB is not None:
+        _need(LB, "LB", torch.bfloat16)
+        R = LB.shape[0]
+        T = torch.empty((M, R), dtype=torch.bfloat16, device=X.device) if T is None else T
+    vals = torch.empty((M, K // 2), dtype=torch.bfloat16, device=X.device) if vals is None else vals
+    meta = torch.empty(lynx_meta_bytes(M, K), dtype=torch.uint8, device=X.device) if meta is None else meta
+    s = torch.empty(M, dtype=torch.float32, device=X.device) if s is None else s
+    _check(lib.lynx_sparsify_lora(_ptr(X), _ptr(LB), M, K, R, _ptr(vals), _ptr(meta), _ptr(s), _ptr(T),
+                                  _stream(stream)), "lynx_sparsify_lora")
+    return vals, meta, s, T
 
 
 def lynx_lora_down(X, LB, s=None, T=None, stream=None):

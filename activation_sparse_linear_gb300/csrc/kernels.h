@@ -44,7 +44,22 @@ __host__ __device__ inline int64_t meta_half_offset(int64_t r, int64_t c, int q,
   return (blk * blocks_k + c / 4) * kMetaChunkBytes + lane * 16 + (c % 4) * 4 + h * 2;
 }
 
-cudaError_t launch_sparsify(const void* X, int M, int K, void* vals, void* meta, float* s, cudaStream_t st);
+
+// Fused sparsification + LoRA down-projection (prologue.cu).
+constexpr int kRankLB = 64;            // LoRA rank handled by the tensor-core paths
+constexpr int kMaxPrologueSplit = 8;   // CTAs (one cluster) per row block
+struct ProArgs {
+  CUtensorMap tmX;   // X (M x K bf16), box 64 x 128, 128-byte swizzle
+  CUtensorMap tmLB;  // LB (64 x K bf16), box 64 x 64, 128-byte swizzle (LoRA branch only)
+  CUtensorMap tmV;   // compressed values (M x K/2 bf16), box 64 x 128, 128-byte swizzle (TMA store)
+  uint8_t* meta;     // metadata chunks (layout above)
+  float* s;          // s = sqrt(sum x^2 / sum kept x^2) (1 for an all-zero row), M floats
+  void* T;           // LoRA: T' = (X LB^T) / s, M x 64 bf16
+  int M, K, M_pad, split, nkb;  // M_pad = round_up(M, 256); split = cluster size; nkb = 128-channel blocks
+  DevCtl ctl;
+};
+int prologue_split(int M, int K);
+cudaError_t launch_prologue(const ProArgs& a, bool lora, cudaStream_t st);
 
 enum ScaleMode : int { SCALE_NONE = 0, SCALE_MUL = 1, SCALE_DIV = 2 };
 

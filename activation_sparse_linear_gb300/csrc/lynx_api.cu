@@ -116,14 +116,12 @@ DevCtl make_ctl() {
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? LYNX_OK : LYNX_ERR_CUDA; }
 
-constexpr int kMaxSplits = 8;  // split-K depth of the LoRA down-projection inside lynx_linear
 
 struct Workspace {
   void* vals;
   void* meta;
   float* s;
   void* T;
-  float* partial;
   size_t bytes;
 };
 
@@ -141,25 +139,13 @@ Workspace carve(void* base, int64_t M, int64_t K, int64_t R) {
   off += align256(static_cast<size_t>(M) * 4);
   w.T = reinterpret_cast<void*>(b + off);
   off += align256(static_cast<size_t>(M) * static_cast<size_t>(R) * 2);
-  w.partial = reinterpret_cast<float*>(b + off);
-  off += align256(static_cast<size_t>(kMaxSplits) * M * R * 4);
   w.bytes = off;
+  (void)R;
   return w;
 }
 
-// T = X LB^T [/ s] on the 64-wide tcgen05 tile.  With a `partial` buffer of
-// kMaxSplits x M x R fp32 the K loop is split so that about one tile per SM
-// runs, and a small kernel sums the partials.
-int lora_splits(int64_t M, int64_t K) {
-  const int64_t num_m = (M + 127) / 128, nk = (K + 63) / 64;
-  int64_t sp = sm_count() / num_m;
-  if (sp > kMaxSplits) sp = kMaxSplits;
-  if (sp > nk) sp = nk;
-  return sp < 1 ? 1 : static_cast<int>(sp);
-}
-
-int run_lora_down(const void* X, const void* LB, const float* s, void* T, int64_t M, int64_t K, cudaStream_t st,
-                  float* partial = nullptr) {
+// T = X LB^T [/ s] on the 64-wide tcgen05 tile (standalone down-projection and the dense path).
+int run_lora_down(const void* X, const void* LB, const float* s, void* T, int64_t M, int64_t K, cudaStream_t st) {
   GemmArgs g;
   std::memset(&g, 0, sizeof(g));
   if (!make_map(&g.tmA, X, K, M, K, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) return LYNX_ERR_CUDA;
@@ -177,16 +163,27 @@ int run_lora_down(const void* X, const void* LB, const float* s, void* T, int64_
   g.ctl = make_ctl();
   g.splits = 1;
   g.partial = nullptr;
-  if (partial) {
-    const int sp = lora_splits(M, K);
-    if (sp > 1) {
-      g.splits = static_cast<int>(sp);
-      g.partial = partial;
-      if (cudaError_t e = launch_gemm(4, g, st)) return cuda_status(e);
-      return cuda_status(launch_lora_finalize(partial, g.splits, s, T, g.M, kRank, st));
-    }
-  }
   return cuda_status(launch_gemm(4, g, st));
+}
+
+// Prologue arguments: X (and LB for the LoRA branch) in, vals / meta / s (/ T') out, shares in the workspace.
+int make_prologue(ProArgs* pa, const void* X, const void* LB, int64_t M, int64_t K, void* vals, void* meta, float* s,
+                  void* T) {
+  std::memset(pa, 0, sizeof(*pa));
+  if (!make_map(&pa->tmX, X, K, M, K, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&pa->tmV, vals, K / 2, M, K / 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      (LB && !make_map(&pa->tmLB, LB, K, kRank, K, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)))
+    return LYNX_ERR_CUDA;
+  pa->meta = static_cast<uint8_t*>(meta);
+  pa->s = s;
+  pa->T = T;
+  pa->M = static_cast<int>(M);
+  pa->K = static_cast<int>(K);
+  pa->M_pad = static_cast<int>(round_up(M, kMetaRowPad));
+  pa->split = prologue_split(pa->M, pa->K);
+  pa->nkb = static_cast<int>(meta_blocks_k(K));
+  pa->ctl = make_ctl();
+  return LYNX_OK;
 }
 
 }  // namespace
@@ -213,11 +210,7 @@ size_t lynx_dense_workspace_bytes(int64_t M, int64_t R) {
 }
 
 int lynx_sparsify(const void* X, int64_t M, int64_t K, void* vals, void* meta, float* s, void* stream) {
-  if (!X || !vals || !meta || !s) return LYNX_ERR_NULL;
-  if (int e = check_mk(M, K)) return e;
-  if (misaligned(X) || misaligned(vals) || misaligned(meta) || misaligned(s)) return LYNX_ERR_ALIGN;
-  return cuda_status(launch_sparsify(X, static_cast<int>(M), static_cast<int>(K), vals, meta, s,
-                                     static_cast<cudaStream_t>(stream)));
+  return lynx_sparsify_lora(X, nullptr, M, K, kRank, vals, meta, s, nullptr, stream);
 }
 
 int lynx_lora_down(const void* X, const void* LB, const float* s, void* T, int64_t M, int64_t K, int64_t R,
@@ -262,15 +255,29 @@ int lynx_linear(const void* X, const void* W, const void* LA, const void* LB, vo
   g.K = static_cast<int>(K);
   g.ctl = make_ctl();
 
-  StageEvents prof(4);
+  ProArgs pa;
+  if (int e = make_prologue(&pa, X, LB, M, K, ws.vals, ws.meta, ws.s, ws.T)) return e;
+
+  StageEvents prof(3);
   if (cudaError_t e = prof.mark(0, st)) return cuda_status(e);
-  if (cudaError_t e = launch_sparsify(X, static_cast<int>(M), static_cast<int>(K), ws.vals, ws.meta, ws.s, st))
-    return cuda_status(e);
+  if (cudaError_t e = launch_prologue(pa, true, st)) return cuda_status(e);
   if (cudaError_t e = prof.mark(1, st)) return cuda_status(e);
-  if (int e = run_lora_down(X, LB, ws.s, ws.T, M, K, st, ws.partial)) return e;
-  if (cudaError_t e = prof.mark(2, st)) return cuda_status(e);
   if (cudaError_t e = launch_gemm_pair(true, true, g, st)) return cuda_status(e);
-  return cuda_status(prof.mark(3, st));
+  return cuda_status(prof.mark(2, st));
+}
+
+int lynx_sparsify_lora(const void* X, const void* LB, int64_t M, int64_t K, int64_t R, void* vals, void* meta,
+                       float* s, void* T, void* stream) {
+  if (!X || !vals || !meta || !s) return LYNX_ERR_NULL;
+  if ((LB == nullptr) != (T == nullptr)) return LYNX_ERR_NULL;
+  if (int e = check_mk(M, K)) return e;
+  if (LB && R != kRank) return R < 1 ? LYNX_ERR_SHAPE : LYNX_ERR_UNSUPPORTED;
+  if (misaligned(X) || misaligned(vals) || misaligned(meta) || misaligned(s) ||
+      (LB && (misaligned(LB) || misaligned(T))))
+    return LYNX_ERR_ALIGN;
+  ProArgs pa;
+  if (int e = make_prologue(&pa, X, LB, M, K, vals, meta, s, T)) return e;
+  return cuda_status(launch_prologue(pa, LB != nullptr, static_cast<cudaStream_t>(stream)));
 }
 
 int lynx_linear_dense(const void* X, const void* W, const void* LA, const void* LB, void* Y, int64_t M,
@@ -371,7 +378,7 @@ int lynx_linear_kernel_count(int64_t M, int64_t N, int64_t K, int64_t R) {
   (void)N;
   (void)R;
   if (M < 1 || K < 1) return 0;
-  return lora_splits(M, K) > 1 ? 4 : 3;
+  return 2;
 }
 
 void lynx_profile_next(void* const* events, int count) {

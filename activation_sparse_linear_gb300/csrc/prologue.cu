@@ -1,0 +1,418 @@
+// Fused first half of the RT-Lynx linear layer: one pass over X produces
+//   - the 2:4 compressed activations and their metadata ("RT-Lynx" page,
+//     Method: top-2-of-4 activation selection, online, in the sparse tensor
+//     core's own format),
+//   - the row scale s = ||X||_2 / ||X~||_2 (Code examples, first formula),
+//   - T' = (X LB^T) / s, the LoRA down-projection (CUDA kernel optimisation:
+//     the low-rank branch is computed from the same X tile).
+//
+// CTA (rb, sp) handles rows 128 rb .. 128 rb + 127 and the sp-th share of the
+// 128-channel blocks.  Per 64-channel stage, TMA brings the X tile (128 x 64,
+// 128-byte swizzle) and, with the LoRA branch, the LB tile (64 x 64) into a
+// ring of shared-memory stages.  One thread issues four tcgen05.mma
+// (M = 128, N = 64, K = 16) per stage into a 64-column TMEM accumulator, while
+// sixteen selection warps (four threads per row, 16 channels each) read the same
+// X tile, keep the top two of every four channels, and stage the kept values
+// (128-byte swizzled, the layout the sparse GEMM loads) and the metadata
+// chunk of every 128-channel block; a TMA store and a bulk copy write them
+// out.  Rows of X are therefore read from HBM once for both branches.
+//
+// The channel blocks of a row block are split over a cluster of `split` CTAs
+// so that the grid covers the GPU; each CTA keeps its fp32 shares (x^2,
+// kept x^2, and its 128 x 64 share of X LB^T) in shared memory, and CTA j of
+// the cluster adds the split shares of its rows in rank order, reading them
+// through distributed shared memory, and writes s and T'.  With split = 1 the
+// CTA writes s and T' itself.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+#include "select.cuh"
+
+namespace lynx {
+namespace {
+
+constexpr int P_ROWS = 128;                       // rows per CTA = TMEM lanes
+constexpr int P_NST = 6;                          // pipeline stages
+constexpr int P_WORKERS = 16;                     // selection warps: four threads per row
+constexpr int P_TPR = 32 * P_WORKERS / 128;       // threads per row (16 of each stage's 64 channels each)
+constexpr int P_PUB_WARP = 2 + P_WORKERS;         // lane 0 of the warp after the selection warps writes blocks out
+constexpr int P_THREADS = 96 + 32 * P_WORKERS;    // warp 0 TMA, warp 1 MMA, warps 2..17 selection, warp 18
+static_assert(P_TPR == 4, "the selection code below assumes four threads per row");
+constexpr int P_XT = P_ROWS * 128;                // X tile: 128 rows x 64 channels (16 KiB)
+constexpr int P_LBT = kRankLB * 128;              // LB tile: 64 ranks x 64 channels (8 KiB)
+constexpr int P_STAGE = P_XT + P_LBT;
+constexpr int P_VBUF = P_ROWS * 128;              // kept values of one 128-channel block (16 KiB)
+constexpr int P_OBUF = P_VBUF + kMetaChunkBytes;  // + the block's metadata chunk
+constexpr int P_NOBUF = 3;                        // output staging buffers
+constexpr int P_SMALL = 2048;                     // barriers, s of the rows, norm shares of the rows
+constexpr int P_SMEM = P_NST * P_STAGE + P_NOBUF * P_OBUF + P_SMALL + 1024;  // + alignment
+constexpr int P_TSTRIDE = 68;                     // floats per row of the T' share (272 B: conflict-free rows)
+static_assert(P_ROWS * P_TSTRIDE * 4 <= P_NST * P_STAGE, "the T' share fits in the drained stage ring");
+static_assert(P_SMEM <= 232448, "shared memory budget");
+
+enum Site : int { SITE_P_PRODUCER = 21, SITE_P_MMA = 22, SITE_P_WORKER = 23, SITE_P_ACC = 24, SITE_P_PUB = 25 };
+
+__device__ __forceinline__ void named_sync_workers() {
+  asm volatile("bar.sync 1, %0;" ::"n"(32 * P_WORKERS) : "memory");
+}
+__device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_u32(ssrc)),
+               "r"(bytes)
+               : "memory");
+}
+
+template <bool LORA>
+__global__ void __launch_bounds__(P_THREADS, 1) prologue_kernel(const __grid_constant__ ProArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* obuf0 = smem + P_NST * P_STAGE;
+  uint64_t* full = reinterpret_cast<uint64_t*>(obuf0 + P_NOBUF * P_OBUF);
+  uint64_t* empty = full + P_NST;
+  uint64_t* acc_full = empty + P_NST;
+  uint64_t* done = acc_full + 1;        // [P_NOBUF] a block's staging buffer is written (one arrival per warp)
+  uint64_t* freed = done + P_NOBUF;     // [P_NOBUF] its store has read the buffer (publisher)
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(freed + P_NOBUF);
+  float* s_sh = reinterpret_cast<float*>(tslot + 4);  // direct mode: s of the CTA's rows (128 floats)
+  float2* npart = reinterpret_cast<float2*>(s_sh + P_ROWS);  // cluster mode: (sum x^2, sum kept x^2) per row
+  float* tpart = reinterpret_cast<float*>(smem);            // cluster mode: T' share [128][P_TSTRIDE]
+  static_assert(8 * (3 * P_NST + 2 * P_NOBUF) + 16 + 12 * P_ROWS <= P_SMALL, "small-state area");
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rb = blockIdx.x / a.split, sp = blockIdx.x % a.split;
+  const int r0 = rb * P_ROWS;
+  const int kb0 = static_cast<int>(static_cast<int64_t>(sp) * a.nkb / a.split);
+  const int kb1 = static_cast<int>(static_cast<int64_t>(sp + 1) * a.nkb / a.split);
+  const int nstages = 2 * (kb1 - kb0);  // >= 2: the host keeps split <= nkb
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < P_NST; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], P_WORKERS + (LORA ? 1 : 0));
+    }
+    mbar_init(acc_full, 1);
+    for (int i = 0; i < P_NOBUF; ++i) {
+      mbar_init(&done[i], P_WORKERS);
+      mbar_init(&freed[i], 1);
+    }
+    fence_mbar_init();
+  }
+  if (threadIdx.x == 32) {
+    prefetch_tmap(&a.tmX);
+    prefetch_tmap(&a.tmV);
+    if (LORA) prefetch_tmap(&a.tmLB);
+  }
+  if (LORA && warp == 1) {
+    tmem_alloc(tslot, 64);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = LORA ? *tslot : 0u;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // -------------------------------------------------------------- TMA producer
+      int it = 0;
+      for (; it < nstages; ++it) {
+        const int st = it % P_NST;
+        if (!mbar_wait(&empty[st], ((it / P_NST) & 1) ^ 1, a.ctl, SITE_P_PRODUCER)) break;
+        uint8_t* sx = smem + st * P_STAGE;
+        const int ch = kb0 * kMetaBlockCols + it * 64;
+        if (!(a.ctl.inject == 1 && it == 0)) {  // test hook: the first stage never arrives
+          mbar_arrive_expect_tx(&full[st], P_XT + (LORA ? P_LBT : 0));
+          tma_load_2d(sx, &a.tmX, &full[st], ch, r0);
+          if (LORA) tma_load_2d(sx + P_XT, &a.tmLB, &full[st], ch, 0);
+        }
+      }
+      // Every load issued must land before the CTA exits (after a timeout the consumers stop early).
+      // A slot holds at most one outstanding load: the last one issued into it, phase n - 1.
+      for (int st = 0; st < P_NST; ++st) {
+        int n = it > st ? (it - st + P_NST - 1) / P_NST : 0;
+        if (a.ctl.inject == 1 && st == 0 && n > 0) --n;  // stage 0 was never loaded
+        if (n > 0) mbar_wait(&full[st], (n - 1) & 1, a.ctl, SITE_P_PRODUCER);
+      }
+    }
+  } else if (warp == 1) {
+    if (LORA && lane == 0) {
+      // -------------------------------------------------------------- MMA issuer: T += X_tile LB_tile^T
+      constexpr uint32_t IDESC = idesc_bf16(P_ROWS, kRankLB, false);
+      constexpr uint64_t STEP = P_STAGE >> 4;
+      const uint64_t a0 = sdesc(smem_u32(smem), 16, 1024, SWZ_128B);
+      const uint64_t b0 = sdesc(smem_u32(smem) + P_XT, 16, 1024, SWZ_128B);
+      bool ok = true;
+      for (int it = 0; it < nstages && ok; ++it) {
+        const int st = it % P_NST;
+        ok = mbar_wait(&full[st], (it / P_NST) & 1, a.ctl, SITE_P_MMA);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t ad = a0 + st * STEP, bd = b0 + st * STEP;
+        tc_mma(tmem, ad, bd, IDESC, it != 0);
+        tc_mma(tmem, ad + 2, bd + 2, IDESC, 1);
+        tc_mma(tmem, ad + 4, bd + 4, IDESC, 1);
+        tc_mma(tmem, ad + 6, bd + 6, IDESC, 1);
+        tc_commit(&empty[st]);
+      }
+      tc_commit(acc_full);  // fires once every MMA issued above has completed
+      mbar_wait(acc_full, 0, a.ctl, SITE_P_ACC);  // no MMA may still run when TMEM is released
+    }
+  } else if (warp == P_PUB_WARP) {
+    if (lane == 0) {
+      // -------------------------------------------------------------- publisher: finished blocks -> global
+      const int64_t blocks_k = meta_blocks_k(a.K);
+      const int nblocks = kb1 - kb0;
+      for (int kbl = 0; kbl < nblocks; ++kbl) {
+        const int b = kbl % P_NOBUF;
+        if (!mbar_wait(&done[b], (kbl / P_NOBUF) & 1, a.ctl, SITE_P_PUB)) break;
+        uint8_t* vb = obuf0 + b * P_OBUF;
+        const int kb = kb0 + kbl;
+        tma_store_2d(&a.tmV, vb, kb * 64, r0);
+        bulk_store(a.meta + (static_cast<int64_t>(rb) * blocks_k + kb) * kMetaChunkBytes, vb + P_VBUF,
+                   kMetaChunkBytes);
+        bulk_commit();
+        if (kbl > 0) {
+          bulk_wait_read_one();                          // block kbl - 1's copies have read their buffer
+          mbar_arrive(&freed[(kbl - 1) % P_NOBUF]);
+        }
+      }
+      bulk_wait_all();
+    }
+  } else {
+    // ---------------------------------------------------------------- selection warps
+    const int tw = threadIdx.x - 64;
+    const int r = tw >> 2, qq = tw & 3;  // row of the tile; which 16 of each stage's 64 channels
+    const int row = r0 + r;
+    // this thread's 16-bit metadata half: groups 4 (qq & 1) .. +3 of a 32-channel word; rows r and r + 8 of a
+    // 16-row group share TMEM lanes (low halves in lanes 0-7 of the group, high halves in lanes 8-15)
+    const int mlane = (r / 16) * 16 + (qq & 1) * 8 + (r % 8), half_sel = (r % 16) / 8;
+    float sx = 0.f, skept = 0.f;  // running sums of x^2 and kept x^2 (groups added in channel order)
+    bool ok = true;
+    // one 128-channel block (two stages) per iteration: eight groups per thread
+    for (int kbl = 0; kbl < nstages / 2; ++kbl) {
+      uint4 v[4];
+#pragma unroll
+      for (int sub = 0; sub < 2; ++sub) {
+        const int it = 2 * kbl + sub, st = it % P_NST;
+        ok = mbar_wait(&full[st], (it / P_NST) & 1, a.ctl, SITE_P_WORKER);
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        if (!ok) break;
+        const uint8_t* xrow = smem + st * P_STAGE + r * 128;
+        v[2 * sub] = *reinterpret_cast<const uint4*>(xrow + (((2 * qq) ^ (r & 7)) << 4));
+        v[2 * sub + 1] = *reinterpret_cast<const uint4*>(xrow + (((2 * qq + 1) ^ (r & 7)) << 4));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);  // this warp no longer reads the stage
+      }
+      if (!ok) break;
+      uint32_t k[8], half[2];
+      float qa[8], qk[8];
+#pragma unroll
+      for (int sub = 0; sub < 2; ++sub) {
+        const uint4 u0 = v[2 * sub], u1 = v[2 * sub + 1];
+        const uint32_t n0 = select_group(u0.x, u0.y, k[4 * sub], qa[4 * sub], qk[4 * sub]);
+        const uint32_t n1 = select_group(u0.z, u0.w, k[4 * sub + 1], qa[4 * sub + 1], qk[4 * sub + 1]);
+        const uint32_t n2 = select_group(u1.x, u1.y, k[4 * sub + 2], qa[4 * sub + 2], qk[4 * sub + 2]);
+        const uint32_t n3 = select_group(u1.z, u1.w, k[4 * sub + 3], qa[4 * sub + 3], qk[4 * sub + 3]);
+        half[sub] = n0 | (n1 << 4) | (n2 << 8) | (n3 << 12);
+      }
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {  // the same additions for both sums: equal when nothing nonzero is dropped
+        sx += qa[g];
+        skept += qk[g];
+      }
+      uint8_t* vb = obuf0 + (kbl % P_NOBUF) * P_OBUF;
+      if (kbl >= P_NOBUF) {  // the buffer's previous block has been copied out
+        ok = mbar_wait(&freed[kbl % P_NOBUF], (kbl / P_NOBUF - 1) & 1, a.ctl, SITE_P_WORKER);
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        if (!ok) break;
+      }
+#pragma unroll
+      for (int sub = 0; sub < 2; ++sub) {
+        // 16-byte chunk 4 sub + qq of the row's 128 bytes of kept values, 128-byte swizzle
+        *reinterpret_cast<uint4*>(vb + r * 128 + (((4 * sub + qq) ^ (r & 7)) << 4)) =
+            make_uint4(k[4 * sub], k[4 * sub + 1], k[4 * sub + 2], k[4 * sub + 3]);
+        const int w = 2 * sub + (qq >> 1);  // 32-channel word of the chunk
+        *reinterpret_cast<uint16_t*>(vb + P_VBUF + mlane * 16 + w * 4 + half_sel * 2) =
+            static_cast<uint16_t>(half[sub]);
+      }
+      fence_proxy_async();  // block complete: hand the buffer to the publisher
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&done[kbl % P_NOBUF]);
+    }
+    // row sums: the four threads of a row are neighbouring lanes
+    sx += __shfl_xor_sync(0xFFFFFFFFu, sx, 1);
+    skept += __shfl_xor_sync(0xFFFFFFFFu, skept, 1);
+    sx += __shfl_xor_sync(0xFFFFFFFFu, sx, 2);
+    skept += __shfl_xor_sync(0xFFFFFFFFu, skept, 2);
+    if (qq == 0) {
+      if (a.split == 1) {
+        const float sv = skept > 0.f ? sqrtf(sx / skept) : 1.f;
+        s_sh[r] = sv;
+        if (row < a.M) a.s[row] = sv;
+      } else {
+        npart[r] = make_float2(sx, skept);
+      }
+    }
+    if (LORA) {
+      // s_sh complete; every worker is past the stage ring, which then holds the T' share (the MMAs are done
+      // with it once acc_full has fired)
+      named_sync_workers();
+      if (warp < 6) {
+        // TMEM lane quarter q = warp % 4 holds rows 32 q .. 32 q + 31
+        const int q = warp & 3;
+        bool got = ok && mbar_wait(acc_full, 0, a.ctl, SITE_P_ACC);
+        got = __all_sync(0xFFFFFFFFu, got);
+        if (got) {
+          tc_fence_after();
+          uint32_t t0[32], t1[32];
+          tc_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16), t0);
+          tc_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + 32, t1);
+          tc_wait_ld();
+          const int trow = q * 32 + lane, grow = r0 + trow;
+          if (a.split == 1) {
+            if (grow < a.M) {
+              const float sv = s_sh[trow];
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.T) + static_cast<int64_t>(grow) * kRankLB);
+#pragma unroll
+              for (int v8 = 0; v8 < 8; ++v8) {
+                const uint32_t* src = v8 < 4 ? t0 + 8 * v8 : t1 + 8 * (v8 - 4);
+                uint32_t pk[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(src[2 * j]) / sv,
+                                                            __uint_as_float(src[2 * j + 1]) / sv);
+                  pk[j] = *reinterpret_cast<uint32_t*>(&b2);
+                }
+                dst[v8] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              }
+            }
+          } else {
+            float4* dst = reinterpret_cast<float4*>(tpart + trow * P_TSTRIDE);  // 272-byte rows: no bank conflicts
+#pragma unroll
+            for (int v4 = 0; v4 < 16; ++v4) {
+              const uint32_t* src = v4 < 8 ? t0 + 4 * v4 : t1 + 4 * (v4 - 8);
+              dst[v4] = make_float4(__uint_as_float(src[0]), __uint_as_float(src[1]), __uint_as_float(src[2]),
+                                    __uint_as_float(src[3]));
+            }
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (a.split > 1) {
+    // ---------------------------------------------------------------- cluster reduction of the shares
+    // CTA j of the cluster finishes rows j * 128 / split .. : it adds the split CTAs' shares in rank order
+    // (deterministic), reading them from the peers' shared memory, and writes s and T'.
+    cluster_sync();  // every CTA's shares are in its shared memory
+    const int rows = P_ROWS / a.split, per_row = LORA ? 8 : 1;
+    for (int i = threadIdx.x; i < rows * per_row; i += P_THREADS) {
+      const int rr = sp * rows + i / per_row, g = i % per_row, grow = r0 + rr;
+      float sxs = 0.f, sks = 0.f;
+      float acc[8] = {};
+      for (int p = 0; p < a.split; ++p) {
+        const float2 n2 = ld_cluster_f32x2(mapa_shared(&npart[rr], p));
+        sxs += n2.x;
+        sks += n2.y;
+        if (LORA) {
+          const uint32_t t = mapa_shared(tpart + rr * P_TSTRIDE + 8 * g, p);
+          const float4 u = ld_cluster_f32x4(t), w = ld_cluster_f32x4(t + 16);
+          acc[0] += u.x;
+          acc[1] += u.y;
+          acc[2] += u.z;
+          acc[3] += u.w;
+          acc[4] += w.x;
+          acc[5] += w.y;
+          acc[6] += w.z;
+          acc[7] += w.w;
+        }
+      }
+      const float sv = sks > 0.f ? sqrtf(sxs / sks) : 1.f;
+      if (grow < a.M) {
+        if (g == 0) a.s[grow] = sv;
+        if (LORA) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * j] / sv, acc[2 * j + 1] / sv);
+            pk[j] = *reinterpret_cast<uint32_t*>(&b2);
+          }
+          reinterpret_cast<uint4*>(a.T)[static_cast<int64_t>(grow) * (kRankLB / 8) + g] =
+              make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+      }
+    }
+    cluster_sync();  // no CTA leaves while a peer may still read its shared memory
+  }
+  if (LORA && warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 64);
+  }
+}
+
+}  // namespace
+
+// CTAs per row block: the largest power of two <= kMaxPrologueSplit (and <= the channel blocks) whose
+// clusters all fit on the GPU at once and whose grid does not exceed the SM count; 1 otherwise.
+int prologue_split(int M, int K) {
+  const int row_blocks = static_cast<int>(round_up(M, kMetaRowPad) / P_ROWS);
+  const int nkb = static_cast<int>(meta_blocks_k(K));
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  static int fit[64][4] = {};  // resident clusters of 2, 4, 8 CTAs (index log2 size), per device
+  for (int split = kMaxPrologueSplit; split >= 2; split /= 2) {
+    if (split > nkb || row_blocks * split > sm_count()) continue;
+    const int li = split == 2 ? 1 : split == 4 ? 2 : 3;
+    if (!fit[dev][li]) {
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = split;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(split);
+      cfg.blockDim = dim3(P_THREADS);
+      cfg.dynamicSmemBytes = P_SMEM;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaFuncSetAttribute(prologue_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM) !=
+              cudaSuccess ||
+          cudaOccupancyMaxActiveClusters(&n, prologue_kernel<true>, &cfg) != cudaSuccess)
+        n = 0;
+      fit[dev][li] = n > 0 ? n : -1;
+    }
+    if (fit[dev][li] >= row_blocks) return split;
+  }
+  return 1;
+}
+
+cudaError_t launch_prologue(const ProArgs& args, bool lora, cudaStream_t st) {
+  auto* k = lora ? prologue_kernel<true> : prologue_kernel<false>;
+  static bool attr_set[2][64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[lora][dev]) {
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set[lora][dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = args.split;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3((args.M_pad / P_ROWS) * args.split);
+  cfg.blockDim = dim3(P_THREADS);
+  cfg.dynamicSmemBytes = P_SMEM;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, args);
+}
+
+}  // namespace lynx

@@ -98,14 +98,26 @@ LYNX_API int lynx_sparsify(const void* X, int64_t M, int64_t K, void* vals, void
 LYNX_API int lynx_lora_down(const void* X, const void* LB, const float* s, void* T, int64_t M, int64_t K, int64_t R,
                    void* stream);
 
+/* Fused first half of lynx_linear: one pass over X gives S(X) (exactly as
+ * lynx_sparsify) and, with LB, the LoRA down-projection divided by s:
+ *   T[m, r] = bf16( sum_k X[m,k] LB[r,k] / s[m] ),  R = 64.
+ * (RT-Lynx page, Method: top-2-of-4 selection and the row scale s; CUDA
+ * kernel optimisation: the low-rank branch reuses the activation tile.)
+ *   X [in] M x K bf16; LB [in] R x K bf16 or NULL (then T must be NULL);
+ *   vals, meta, s [out] as for lynx_sparsify; T [out] M x R bf16 or NULL.
+ * One kernel: a row block's channels may be shared by a cluster of CTAs, whose
+ * partial sums are added in a fixed order through distributed shared memory. */
+LYNX_API int lynx_sparsify_lora(const void* X, const void* LB, int64_t M, int64_t K, int64_t R, void* vals,
+                                void* meta, float* s, void* T, void* stream);
+
 /* The full RT-Lynx sparse linear: Y = bf16( s * (X~ W^T) + (X LB^T) LA^T ).
  *   X [in] M x K, W [in] N x K, LA [in] N x R, LB [in] R x K, Y [out] M x N bf16.
  *   workspace: >= lynx_workspace_bytes(M, N, K, R) bytes of device memory,
  *   16-byte aligned, not shared with a concurrent call.
- * Enqueues sparsify, the LoRA down-projection (split over K, plus a small
- * reduction kernel, when few row blocks would leave SMs idle) and the tcgen05
- * 2:4-sparse GEMM whose extra K-steps accumulate T' LA^T into the same
- * tensor-memory accumulator, with s applied in the epilogue.
+ * Enqueues two kernels: the fused sparsify + LoRA down-projection pass
+ * (lynx_sparsify_lora) and the tcgen05 2:4-sparse GEMM whose extra K-steps
+ * accumulate T' LA^T into the same tensor-memory accumulator, with s applied
+ * in the epilogue.
  * (RT-Lynx page, Method and CUDA kernel optimisation.) */
 LYNX_API int lynx_linear(const void* X, const void* W, const void* LA, const void* LB, void* Y, int64_t M, int64_t N,
                 int64_t K, int64_t R, void* workspace, size_t workspace_bytes, void* stream);

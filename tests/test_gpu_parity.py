@@ -66,6 +66,29 @@ def test_sparsify_special_values(lynx):
     assert np.all(s == 1.0)
 
 
+# the fused pass over X (lynx_sparsify_lora), as lynx_linear runs it: the sparsify outputs bit-exact, T' against
+# the oracle; (10000, 256) makes each CTA own whole rows (no split), the others split a row's channels
+FUSED_CASES = SPARSIFY_CASES + [(10000, 256, "act"), (4608, 3072, "act")]
+
+
+@pytest.mark.parametrize("M,K,kind", FUSED_CASES)
+@pytest.mark.parametrize("with_lb", [True, False])
+def test_sparsify_lora_fused(lynx, M, K, kind, with_lb):
+    X = _x(kind, M, K)
+    LB = synth.gaussian_bf16((M, K, 5), (64, K), 0.02) if with_lb else None
+    vals, meta, s, T = lynx.lynx_sparsify_lora(to_dev(X), to_dev(LB) if with_lb else None)
+    assert lynx.lynx_sync_status() == 0
+    ref = O.sparsify(X)
+    assert np.array_equal(to_bits(vals), ref["vals"])
+    meta_h = meta.cpu().numpy()
+    assert np.array_equal(meta_h, pack_meta_reference(ref["meta"], M, K))  # every byte, padding included
+    np.testing.assert_allclose(s.cpu().numpy(), ref["s"], rtol=S_RTOL, atol=0)
+    if with_lb:
+        assert_y_close(to_bits(T), O.lora_down(X, LB, ref["s"]), "T")
+    else:
+        assert T is None
+
+
 @pytest.mark.parametrize("M,K,scaled", [(256, 512, True), (300, 528, True), (5, 3072, False), (129, 12288, True)])
 def test_lora_down(lynx, M, K, scaled):
     X = _x("act", M, K, 3)
