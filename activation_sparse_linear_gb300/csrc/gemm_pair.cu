@@ -163,6 +163,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   cluster_sync();  // barriers of both CTAs initialised, TMEM allocated in both
   tc_fence_after();
   const uint32_t tmem = *tslot;
+  // The set-up above may overlap the previous kernel; nothing below touches global memory before it is done.
+  pdl_launch_dependents();
+  pdl_wait();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -444,8 +447,17 @@ cudaError_t launch(const PairArgs& a, cudaStream_t st) {
   int clusters = sm_count() / 2;
   if (clusters > ntiles) clusters = ntiles;
   if (clusters < 1) clusters = 1;
-  k<<<2 * clusters, THREADS, C::SMEM, st>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // may start while the previous kernel ends
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(2 * clusters);  // the cluster shape (2, 1, 1) is the kernel's own attribute
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, a);
 }
 
 }  // namespace

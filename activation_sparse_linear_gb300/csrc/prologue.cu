@@ -110,6 +110,9 @@ __global__ void __launch_bounds__(P_THREADS, 1) prologue_kernel(const __grid_con
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = LORA ? *tslot : 0u;
+  // The set-up above may overlap the previous kernel; nothing below touches global memory before it is done.
+  pdl_launch_dependents();
+  pdl_wait();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -401,17 +404,19 @@ cudaError_t launch_prologue(const ProArgs& args, bool lora, cudaStream_t st) {
     attr_set[lora][dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = args.split;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // may start while the previous kernel ends
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3((args.M_pad / P_ROWS) * args.split);
   cfg.blockDim = dim3(P_THREADS);
   cfg.dynamicSmemBytes = P_SMEM;
   cfg.stream = st;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, k, args);
 }
 

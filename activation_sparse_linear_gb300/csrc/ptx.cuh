@@ -245,6 +245,14 @@ __device__ __forceinline__ uint32_t mapa_shared(const void* p, uint32_t rank) {
 __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
+// Programmatic dependent launch: let the next kernel in the stream start its CTAs (they run their own
+// set-up and then wait), and wait until the previous kernel has completed and its writes are visible.
+// Both are no-ops for a kernel launched without the programmatic-serialization attribute.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Loads from a cluster-mapped shared-memory address (a peer CTA's shared memory).
 __device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t addr) {
   float4 v;
