@@ -64,24 +64,18 @@ cudaError_t launch_prologue(const ProArgs& a, bool lora, cudaStream_t st);
 enum ScaleMode : int { SCALE_NONE = 0, SCALE_MUL = 1, SCALE_DIV = 2 };
 
 struct GemmArgs {
-  CUtensorMap tmA;    // A operand: X (dense) or compressed values (sparse)
-  CUtensorMap tmB;    // B operand: W (N x K) or LB (R x K)
-  CUtensorMap tmT;    // LoRA-up A: T' (M x R)
-  CUtensorMap tmLA;   // LoRA-up B: LA (N x R)
-  const uint8_t* meta;
+  CUtensorMap tmA;    // A: X (M x K), box 64 x 128, 128-byte swizzle
+  CUtensorMap tmB;    // B: LB (64 x K), box 64 x 64, 128-byte swizzle
   const float* rowscale;
-  int scale_mode;
+  int scale_mode;     // SCALE_NONE or SCALE_DIV (T' = X LB^T / s)
   void* Y;
   int64_t ldy;
-  int M, N, K;
-  int splits;         // >1: split-K; each split writes an fp32 partial tile to `partial`
-  float* partial;     // splits x M x N fp32 (split-K only; no scale applied)
+  int M, N, K;        // N = 64
   DevCtl ctl;
 };
 
-// kind: 0 = dense, 256-wide tiles; 1 = dense + LoRA-up tail; 2 = sparse + LoRA-up tail;
-// 3 = sparse, no LoRA; 4 = dense, 64-wide tiles (LoRA down-projection).
-cudaError_t launch_gemm(int kind, const GemmArgs& a, cudaStream_t st);
+// The dense single-CTA tcgen05 GEMM on 128 x 64 tiles (gemm.cu).
+cudaError_t launch_proj_gemm(const GemmArgs& a, cudaStream_t st);
 
 // Pair-tile shapes: the sparse path gives each CTA two 128-row blocks (a 512 x 192 output tile per pair),
 // the dense path one (256 x 256).  W and LA are staged TileN/2 rows per CTA.
@@ -107,10 +101,6 @@ struct PairArgs {
 
 // The CTA-pair (cta_group::2) GEMM.
 cudaError_t launch_gemm_pair(bool sparse, bool lora, const PairArgs& a, cudaStream_t st);
-
-// T[m, r] = bf16( sum_s partial[s][m][r] / s[m] ) for the split-K LoRA down-projection.
-cudaError_t launch_lora_finalize(const float* partial, int splits, const float* s, void* T, int M, int R,
-                                 cudaStream_t st);
 
 int sm_count();
 

@@ -150,9 +150,6 @@ int run_lora_down(const void* X, const void* LB, const float* s, void* T, int64_
   std::memset(&g, 0, sizeof(g));
   if (!make_map(&g.tmA, X, K, M, K, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) return LYNX_ERR_CUDA;
   if (!make_map(&g.tmB, LB, K, kRank, K, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)) return LYNX_ERR_CUDA;
-  g.tmT = g.tmA;
-  g.tmLA = g.tmB;
-  g.meta = nullptr;
   g.rowscale = s;
   g.scale_mode = s ? SCALE_DIV : SCALE_NONE;
   g.Y = T;
@@ -161,9 +158,7 @@ int run_lora_down(const void* X, const void* LB, const float* s, void* T, int64_
   g.N = kRank;
   g.K = static_cast<int>(K);
   g.ctl = make_ctl();
-  g.splits = 1;
-  g.partial = nullptr;
-  return cuda_status(launch_gemm(4, g, st));
+  return cuda_status(launch_proj_gemm(g, st));
 }
 
 // Prologue arguments: X (and LB for the LoRA branch) in, vals / meta / s (/ T') out, shares in the workspace.
