@@ -366,6 +366,50 @@ def main() -> int:
     torch.cuda.synchronize()
     lynx_dense_ms = l0.elapsed_time(l1) / nd
 
+    # The other layer shapes of the DiT workloads (MLP up/down, the CFG batch, the largest stack M): step time
+    # of lynx_linear and of the dense cuBLAS GEMM at the same shape, two rotating device copies each.  Inputs
+    # are seeded normal draws generated on the device (timing only; the parity tests cover these shapes).
+    shapes = {}
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1234)
+    for name, (Ms, Ns, Ks) in (("mlp_up 4608x3072->12288", (4608, 12288, 3072)),
+                               ("mlp_down 4608x12288->3072", (4608, 3072, 12288)),
+                               ("cfg2_qkv 9216x3072->9216", (9216, 9216, 3072)),
+                               ("stack_qkv 16384x3072->9216", (16384, 9216, 3072))):
+        cs = []
+        for _ in range(2):
+            cs.append({"X": torch.randn((Ms, Ks), generator=gen, device=dev).to(torch.bfloat16),
+                       "W": (torch.randn((Ns, Ks), generator=gen, device=dev) / Ks ** 0.5).to(torch.bfloat16),
+                       "LA": (0.02 * torch.randn((Ns, R), generator=gen, device=dev)).to(torch.bfloat16),
+                       "LB": (0.02 * torch.randn((R, Ks), generator=gen, device=dev)).to(torch.bfloat16),
+                       "Y": torch.empty((Ms, Ns), dtype=torch.bfloat16, device=dev),
+                       "ws": torch.empty(asl.lynx_workspace_bytes(Ms, Ns, Ks, R), dtype=torch.uint8, device=dev)})
+
+        def one(c):
+            return L.lynx_linear(c["X"].data_ptr(), c["W"].data_ptr(), c["LA"].data_ptr(), c["LB"].data_ptr(),
+                                 c["Y"].data_ptr(), Ms, Ns, Ks, R, c["ws"].data_ptr(), c["ws"].numel(), sp)
+        ns = 100
+        times = []
+        for fn in (lambda c: one(c), lambda c: torch.matmul(c["X"], c["W"].t(), out=c["Y"])):
+            for i in range(5):
+                fn(cs[i % 2])
+            torch.cuda.synchronize()
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            for i in range(ns):
+                fn(cs[i % 2])
+            a1.record(stream)
+            torch.cuda.synchronize()
+            times.append(a0.elapsed_time(a1) / ns)
+        st = asl.lynx_sync_status()
+        assert st == 0, asl.lynx_status_string(st)
+        fl = 2.0 * Ms * Ns * Ks
+        shapes[name] = {"lynx_ms": times[0], "tflops": fl / (times[0] * 1e-3) / 1e12,
+                        "pct_of_sparse_peak": 100.0 * fl / (times[0] * 1e-3) / 1e12 / (2.0 * dense_tf),
+                        "cublas_dense_ms": times[1], "x_vs_dense_cublas": times[1] / times[0]}
+        del cs
+    torch.cuda.empty_cache()
+
     # End to end through the C-ABI with host buffers, pipelined as a serving loop runs it: every step copies
     # its X from pinned host memory, calls lynx_linear and copies its Y back to pinned host memory, on three
     # streams so that step i's copies overlap the neighbouring steps' compute.  Events order the reuse of the
@@ -453,6 +497,7 @@ def main() -> int:
             "x_vs_dense_cublas": dense_ms / ms_per_step,
             "lynx_dense_gemm_ms": lynx_dense_ms, "lynx_dense_gemm_tflops": flops / (lynx_dense_ms * 1e-3) / 1e12,
             "hbm_peak_GBs": hbm, "dense_bf16_peak_tflops": dense_tf,
+            "other_shapes": shapes,
             "mma_microbench": {"dense_tflops": mma_dense_tf, "sparse_tflops_effective": mma_sparse_tf,
                                "dense_macs_per_clk": mma_dense_mpc, "sparse_macs_per_clk_effective": mma_sparse_mpc,
                                "sparse_over_dense": mma_sparse_tf / mma_dense_tf,

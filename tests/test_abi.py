@@ -26,7 +26,8 @@ def declared_symbols():
 
 def test_header_declares_the_boundary():
     syms = declared_symbols()
-    for name in ("lynx_sparsify", "lynx_linear", "lynx_linear_dense", "lynx_sync_status", "lynx_meta_bytes",
+    for name in ("lynx_sparsify", "lynx_sparsify_lora", "lynx_linear", "lynx_linear_dense", "lynx_sync_status",
+                 "lynx_meta_bytes",
                  "lynx_workspace_bytes"):
         assert name in syms
 
@@ -80,6 +81,11 @@ def test_other_entry_points_reject_bad_arguments(asl):
     assert L.lynx_sparsify(None, 4, 16, A, A, A, None) == -1
     assert L.lynx_sparsify(A, 4, 20, A, A, A, None) == -2
     assert L.lynx_sparsify(A, 4, 16, A + 4, A, A, None) == -3
+    assert L.lynx_sparsify_lora(A, None, 4, 16, 64, A, A, A, A, None) == -1      # T without LB
+    assert L.lynx_sparsify_lora(A, A, 4, 16, 64, A, A, A, None, None) == -1      # LB without T
+    assert L.lynx_sparsify_lora(A, A, 4, 16, 32, A, A, A, A, None) == -7         # rank other than 64
+    assert L.lynx_sparsify_lora(A, A, 4, 16, 64, A, A, A, A + 8, None) == -3     # misaligned T
+    assert L.lynx_sparsify_lora(A, A, 0, 16, 64, A, A, A, A, None) == -2         # M = 0
     assert L.lynx_lora_down(A, A, None, A, 4, 16, 16, None) == -7
     assert L.lynx_linear_dense(A, A, A, None, A, 4, 16, 16, 64, A, 1 << 20, None) == -1   # one LoRA factor
     assert L.lynx_linear_dense(A, A, A, A, A, 4, 16, 16, 64, A, 10, None) == -4
