@@ -51,6 +51,8 @@ constexpr int P_TSTRIDE = 68;                     // floats per row of the T' sh
 static_assert(P_ROWS * P_TSTRIDE * 4 <= P_NST * P_STAGE, "the T' share fits in the drained stage ring");
 static_assert(P_SMEM <= 232448, "shared memory budget");
 
+__constant__ SelectTable c_select_table = make_select_table();
+
 enum Site : int { SITE_P_PRODUCER = 21, SITE_P_MMA = 22, SITE_P_WORKER = 23, SITE_P_ACC = 24, SITE_P_PUB = 25 };
 
 __device__ __forceinline__ void named_sync_workers() {
@@ -75,8 +77,9 @@ __global__ void __launch_bounds__(P_THREADS, 1) prologue_kernel(const __grid_con
   uint32_t* tslot = reinterpret_cast<uint32_t*>(freed + P_NOBUF);
   float* s_sh = reinterpret_cast<float*>(tslot + 4);  // direct mode: s of the CTA's rows (128 floats)
   float2* npart = reinterpret_cast<float2*>(s_sh + P_ROWS);  // cluster mode: (sum x^2, sum kept x^2) per row
+  uint32_t* sel_table = reinterpret_cast<uint32_t*>(npart + P_ROWS);  // the top-2-of-4 decision table
   float* tpart = reinterpret_cast<float*>(smem);            // cluster mode: T' share [128][P_TSTRIDE]
-  static_assert(8 * (3 * P_NST + 2 * P_NOBUF) + 16 + 12 * P_ROWS <= P_SMALL, "small-state area");
+  static_assert(8 * (3 * P_NST + 2 * P_NOBUF) + 16 + 12 * P_ROWS + 64 * 4 <= P_SMALL, "small-state area");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rb = blockIdx.x / a.split, sp = blockIdx.x % a.split;
@@ -97,6 +100,7 @@ __global__ void __launch_bounds__(P_THREADS, 1) prologue_kernel(const __grid_con
     }
     fence_mbar_init();
   }
+  if (threadIdx.x < 64) sel_table[threadIdx.x] = c_select_table.e[threadIdx.x];
   if (threadIdx.x == 32) {
     prefetch_tmap(&a.tmX);
     prefetch_tmap(&a.tmV);
@@ -212,10 +216,10 @@ __global__ void __launch_bounds__(P_THREADS, 1) prologue_kernel(const __grid_con
 #pragma unroll
       for (int sub = 0; sub < 2; ++sub) {
         const uint4 u0 = v[2 * sub], u1 = v[2 * sub + 1];
-        const uint32_t n0 = select_group(u0.x, u0.y, k[4 * sub], qa[4 * sub], qk[4 * sub]);
-        const uint32_t n1 = select_group(u0.z, u0.w, k[4 * sub + 1], qa[4 * sub + 1], qk[4 * sub + 1]);
-        const uint32_t n2 = select_group(u1.x, u1.y, k[4 * sub + 2], qa[4 * sub + 2], qk[4 * sub + 2]);
-        const uint32_t n3 = select_group(u1.z, u1.w, k[4 * sub + 3], qa[4 * sub + 3], qk[4 * sub + 3]);
+        const uint32_t n0 = select_group(u0.x, u0.y, sel_table, k[4 * sub], qa[4 * sub], qk[4 * sub]);
+        const uint32_t n1 = select_group(u0.z, u0.w, sel_table, k[4 * sub + 1], qa[4 * sub + 1], qk[4 * sub + 1]);
+        const uint32_t n2 = select_group(u1.x, u1.y, sel_table, k[4 * sub + 2], qa[4 * sub + 2], qk[4 * sub + 2]);
+        const uint32_t n3 = select_group(u1.z, u1.w, sel_table, k[4 * sub + 3], qa[4 * sub + 3], qk[4 * sub + 3]);
         half[sub] = n0 | (n1 << 4) | (n2 << 8) | (n3 << 12);
       }
 #pragma unroll
