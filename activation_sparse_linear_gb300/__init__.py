@@ -21,6 +21,7 @@ __all__ = [
     "lynx_sparsify", "lynx_sparsify_lora", "lynx_lora_down", "lynx_linear",
     "lynx_linear_dense",
     "lynx_sync_status", "lynx_status_string", "lynx_meta_to_canonical", "lynx_debug_set_fault",
+    "lynx_debug_force_tile",
     "lynx_profile_next", "lynx_linear_kernel_count", "lynx_mma_rate",
 ]
 
@@ -48,6 +49,7 @@ def _load() -> ctypes.CDLL:
         "lynx_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "lynx_meta_to_canonical": (ctypes.c_int, [_c_p, _c_p, _c_i64, _c_i64]),
         "lynx_debug_set_fault": (None, [ctypes.c_int, ctypes.c_uint64]),
+        "lynx_debug_force_tile": (None, [ctypes.c_int]),
         "lynx_profile_next": (None, [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]),
         "lynx_linear_kernel_count": (ctypes.c_int, [_c_i64, _c_i64, _c_i64, _c_i64]),
         "lynx_mma_rate": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_double),
@@ -236,3 +238,8 @@ _profile_keepalive: list = []
 
 def lynx_debug_set_fault(inject: int, wait_ns: int = 0) -> None:
     lib.lynx_debug_set_fault(inject, wait_ns)
+
+
+def lynx_debug_force_tile(row_blocks: int) -> None:
+    """Test hook: 2 or 1 forces the 512x192 or 256x256 sparse tile shape; 0 restores the automatic choice."""
+    lib.lynx_debug_force_tile(row_blocks)

@@ -462,10 +462,31 @@ cudaError_t launch(const PairArgs& a, cudaStream_t st) {
 
 }  // namespace
 
-cudaError_t launch_gemm_pair(bool sparse, bool lora, const PairArgs& a, cudaStream_t st) {
-  constexpr int MBs = kPairSparseRowBlocks, TNs = kPairSparseTileN, TNd = kPairDenseTileN;
-  if (sparse) return lora ? launch<true, true, MBs, TNs>(a, st) : launch<true, false, MBs, TNs>(a, st);
-  return lora ? launch<false, true, 1, TNd>(a, st) : launch<false, false, 1, TNd>(a, st);
+// Shared-memory traffic per thousand logical MACs of each sparse shape (TMA fill plus tensor-core operand
+// reads, the kernel's binding resource): 512 x 192 tiles 22.9 B, 256 x 256 tiles 23.8 B.  The shape with the
+// smaller (tile waves x tile work x traffic) wins; 512 x 192 for the large DiT shapes, 256 x 256 when few
+// row tiles would leave pairs idle (e.g. M = 1024).
+PairShape pair_shape(bool sparse, int M, int N) {
+  if (!sparse) return {1, 256};
+  const int64_t clusters = sm_count() / 2 > 0 ? sm_count() / 2 : 1;
+  auto cost = [&](int rb, int tn, double bytes_per_kmac) {
+    const int64_t tiles = ((M + 256 * rb - 1) / (256 * rb)) * static_cast<int64_t>((N + tn - 1) / tn);
+    const int64_t waves = (tiles + clusters - 1) / clusters;
+    return static_cast<double>(waves) * 256.0 * rb * tn * bytes_per_kmac;
+  };
+  return cost(2, 192, 22.9) <= cost(1, 256, 23.8) ? PairShape{2, 192} : PairShape{1, 256};
+}
+
+cudaError_t launch_gemm_pair(bool sparse, bool lora, PairShape shape, const PairArgs& a, cudaStream_t st) {
+  if (!sparse) {
+    if (shape.rb != 1 || shape.tn != 256) return cudaErrorInvalidValue;
+    return lora ? launch<false, true, 1, 256>(a, st) : launch<false, false, 1, 256>(a, st);
+  }
+  if (shape.rb == 2 && shape.tn == 192)
+    return lora ? launch<true, true, 2, 192>(a, st) : launch<true, false, 2, 192>(a, st);
+  if (shape.rb == 1 && shape.tn == 256)
+    return lora ? launch<true, true, 1, 256>(a, st) : launch<true, false, 1, 256>(a, st);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace lynx

@@ -77,11 +77,13 @@ struct GemmArgs {
 // The dense single-CTA tcgen05 GEMM on 128 x 64 tiles (gemm.cu).
 cudaError_t launch_proj_gemm(const GemmArgs& a, cudaStream_t st);
 
-// Pair-tile shapes: the sparse path gives each CTA two 128-row blocks (a 512 x 192 output tile per pair),
-// the dense path one (256 x 256).  W and LA are staged TileN/2 rows per CTA.
-constexpr int kPairSparseRowBlocks = 2;
-constexpr int kPairSparseTileN = 192;
-constexpr int kPairDenseTileN = 256;
+// Pair-tile shapes: rb = 128-row blocks per CTA (the pair covers 256 * rb rows), tn = output columns per tile
+// (W and LA are staged tn / 2 rows per CTA).  The sparse path uses 512 x 192 tiles, or 256 x 256 when that
+// gives fewer tile waves for the shape; the dense path uses 256 x 256.
+struct PairShape {
+  int rb, tn;
+};
+PairShape pair_shape(bool sparse, int M, int N);
 
 struct PairArgs {
   CUtensorMap tmA;     // sparse: compressed values; dense: X (both box 64 x 128, 128-byte swizzle)
@@ -99,8 +101,8 @@ struct PairArgs {
   DevCtl ctl;
 };
 
-// The CTA-pair (cta_group::2) GEMM.
-cudaError_t launch_gemm_pair(bool sparse, bool lora, const PairArgs& a, cudaStream_t st);
+// The CTA-pair (cta_group::2) GEMM with the given tile shape (one of those pair_shape returns).
+cudaError_t launch_gemm_pair(bool sparse, bool lora, PairShape shape, const PairArgs& a, cudaStream_t st);
 
 int sm_count();
 

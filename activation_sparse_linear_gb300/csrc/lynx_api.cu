@@ -24,6 +24,7 @@ constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 __device__ int g_error_word;
 
 std::atomic<int> g_inject{0};
+std::atomic<int> g_force_tile{0};  // 0: tile shape by problem shape; 1 or 2: forced row blocks per CTA
 thread_local void* const* t_prof_events = nullptr;
 thread_local int t_prof_count = 0;
 
@@ -232,13 +233,17 @@ int lynx_linear(const void* X, const void* W, const void* LA, const void* LB, vo
 
   PairArgs g;
   std::memset(&g, 0, sizeof(g));
+  const int forced = g_force_tile.load();
+  const PairShape shape = forced == 2   ? PairShape{2, 192}
+                          : forced == 1 ? PairShape{1, 256}
+                                        : pair_shape(true, static_cast<int>(M), static_cast<int>(N));
   const uint64_t meta_rows = 2 * static_cast<uint64_t>(meta_bytes(M, K) / kMetaChunkBytes);  // 1 KiB rows
   if (!make_map(&g.tmA, ws.vals, K / 2, M, K / 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&g.tmB, W, K, N, K, 64, kPairSparseTileN / 2, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&g.tmB, W, K, N, K, 64, shape.tn / 2, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&g.tmMeta, ws.meta, 256, meta_rows, 256, 256, 2, CU_TENSOR_MAP_SWIZZLE_NONE,
                 CU_TENSOR_MAP_DATA_TYPE_UINT32) ||
       !make_map(&g.tmT, ws.T, R, M, R, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&g.tmLA, LA, R, N, R, 64, kPairSparseTileN / 2, CU_TENSOR_MAP_SWIZZLE_128B))
+      !make_map(&g.tmLA, LA, R, N, R, 64, shape.tn / 2, CU_TENSOR_MAP_SWIZZLE_128B))
     return LYNX_ERR_CUDA;
   if (!set_y_map(&g, Y, M, N)) return LYNX_ERR_CUDA;
   g.rowscale = ws.s;
@@ -257,7 +262,7 @@ int lynx_linear(const void* X, const void* W, const void* LA, const void* LB, vo
   if (cudaError_t e = prof.mark(0, st)) return cuda_status(e);
   if (cudaError_t e = launch_prologue(pa, true, st)) return cuda_status(e);
   if (cudaError_t e = prof.mark(1, st)) return cuda_status(e);
-  if (cudaError_t e = launch_gemm_pair(true, true, g, st)) return cuda_status(e);
+  if (cudaError_t e = launch_gemm_pair(true, true, shape, g, st)) return cuda_status(e);
   return cuda_status(prof.mark(2, st));
 }
 
@@ -292,11 +297,11 @@ int lynx_linear_dense(const void* X, const void* W, const void* LA, const void* 
   PairArgs g;
   std::memset(&g, 0, sizeof(g));
   if (!make_map(&g.tmA, X, K, M, K, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&g.tmB, W, K, N, K, 64, kPairDenseTileN / 2, CU_TENSOR_MAP_SWIZZLE_128B))
+      !make_map(&g.tmB, W, K, N, K, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
     return LYNX_ERR_CUDA;
   if (lora) {
     if (!make_map(&g.tmT, workspace, R, M, R, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&g.tmLA, LA, R, N, R, 64, kPairDenseTileN / 2, CU_TENSOR_MAP_SWIZZLE_128B))
+        !make_map(&g.tmLA, LA, R, N, R, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
       return LYNX_ERR_CUDA;
   }
   if (!set_y_map(&g, Y, M, N)) return LYNX_ERR_CUDA;
@@ -313,10 +318,10 @@ int lynx_linear_dense(const void* X, const void* W, const void* LA, const void* 
   if (lora) {
     if (int e = run_lora_down(X, LB, nullptr, workspace, M, K, st)) return e;
     if (cudaError_t e = prof.mark(1, st)) return cuda_status(e);
-    if (cudaError_t e = launch_gemm_pair(false, true, g, st)) return cuda_status(e);
+    if (cudaError_t e = launch_gemm_pair(false, true, PairShape{1, 256}, g, st)) return cuda_status(e);
     return cuda_status(prof.mark(2, st));
   }
-  if (cudaError_t e = launch_gemm_pair(false, false, g, st)) return cuda_status(e);
+  if (cudaError_t e = launch_gemm_pair(false, false, PairShape{1, 256}, g, st)) return cuda_status(e);
   return cuda_status(prof.mark(1, st));
 }
 
@@ -385,6 +390,8 @@ void lynx_debug_set_fault(int inject, uint64_t wait_ns) {
   g_inject.store(inject);
   g_wait_ns.store(wait_ns ? wait_ns : kDefaultWaitNs);
 }
+
+void lynx_debug_force_tile(int row_blocks) { g_force_tile.store(row_blocks == 1 || row_blocks == 2 ? row_blocks : 0); }
 
 }  // extern "C"
 

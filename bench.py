@@ -410,6 +410,62 @@ def main() -> int:
         del cs
     torch.cuda.empty_cache()
 
+    # The block stack: 8 blocks x (QKV sparse 3072->9216, out dense 3072->3072, up dense 3072->12288,
+    # down sparse 12288->3072), rank-64 LoRA on the sparse layers, independent seeded weights per block; the
+    # total time of the 32 linears at each M against the same 32 layers run dense through cuBLAS.
+    stack = {}
+    wts = []
+    for b in range(8):
+        def w_(n, k):
+            return (torch.randn((n, k), generator=gen, device=dev) / k ** 0.5).to(torch.bfloat16)
+
+        def l_(a, c):
+            return (0.02 * torch.randn((a, c), generator=gen, device=dev)).to(torch.bfloat16)
+        wts.append({"qkv": w_(9216, 3072), "out": w_(3072, 3072), "up": w_(12288, 3072), "down": w_(3072, 12288),
+                    "la_qkv": l_(9216, R), "lb_qkv": l_(R, 3072), "la_down": l_(3072, R), "lb_down": l_(R, 12288)})
+    for Ms in (1024, 4608, 9216, 16384):
+        x3 = torch.randn((Ms, 3072), generator=gen, device=dev).to(torch.bfloat16)
+        x12 = torch.relu(torch.randn((Ms, 12288), generator=gen, device=dev)).to(torch.bfloat16)
+        y = {n: torch.empty((Ms, n), dtype=torch.bfloat16, device=dev) for n in (3072, 9216, 12288)}
+        ws_s = torch.empty(max(asl.lynx_workspace_bytes(Ms, 9216, 3072, R), asl.lynx_workspace_bytes(Ms, 3072, 12288, R)),
+                           dtype=torch.uint8, device=dev)
+
+        def lynx_stack():
+            for w in wts:
+                for xin, wt, la, lb, yo, kk in ((x3, w["qkv"], w["la_qkv"], w["lb_qkv"], y[9216], 3072),
+                                               (x12, w["down"], w["la_down"], w["lb_down"], y[3072], 12288)):
+                    if L.lynx_linear(xin.data_ptr(), wt.data_ptr(), la.data_ptr(), lb.data_ptr(), yo.data_ptr(), Ms,
+                                     wt.shape[0], kk, R, ws_s.data_ptr(), ws_s.numel(), sp) != 0:
+                        raise RuntimeError("lynx_linear failed")
+                for wt, yo in ((w["out"], y[3072]), (w["up"], y[12288])):
+                    if L.lynx_linear_dense(x3.data_ptr(), wt.data_ptr(), None, None, yo.data_ptr(), Ms, wt.shape[0],
+                                           3072, R, None, 0, sp) != 0:
+                        raise RuntimeError("lynx_linear_dense failed")
+
+        def dense_stack():
+            for w in wts:
+                torch.matmul(x3, w["qkv"].t(), out=y[9216])
+                torch.matmul(x3, w["out"].t(), out=y[3072])
+                torch.matmul(x3, w["up"].t(), out=y[12288])
+                torch.matmul(x12, w["down"].t(), out=y[3072])
+        tt = []
+        for fn in (lynx_stack, dense_stack):
+            fn()
+            torch.cuda.synchronize()
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            for _ in range(3):
+                fn()
+            a1.record(stream)
+            torch.cuda.synchronize()
+            tt.append(a0.elapsed_time(a1) / 3)
+        st = asl.lynx_sync_status()
+        assert st == 0, asl.lynx_status_string(st)
+        stack[f"M={Ms}"] = {"lynx_ms": tt[0], "all_dense_cublas_ms": tt[1], "x_vs_dense_cublas": tt[1] / tt[0]}
+        del x3, x12, y, ws_s
+    del wts
+    torch.cuda.empty_cache()
+
     # End to end through the C-ABI with host buffers, pipelined as a serving loop runs it: every step copies
     # its X from pinned host memory, calls lynx_linear and copies its Y back to pinned host memory, on three
     # streams so that step i's copies overlap the neighbouring steps' compute.  Events order the reuse of the
@@ -498,6 +554,7 @@ def main() -> int:
             "lynx_dense_gemm_ms": lynx_dense_ms, "lynx_dense_gemm_tflops": flops / (lynx_dense_ms * 1e-3) / 1e12,
             "hbm_peak_GBs": hbm, "dense_bf16_peak_tflops": dense_tf,
             "other_shapes": shapes,
+            "block_stack_32_linears": stack,
             "mma_microbench": {"dense_tflops": mma_dense_tf, "sparse_tflops_effective": mma_sparse_tf,
                                "dense_macs_per_clk": mma_dense_mpc, "sparse_macs_per_clk_effective": mma_sparse_mpc,
                                "sparse_over_dense": mma_sparse_tf / mma_dense_tf,
