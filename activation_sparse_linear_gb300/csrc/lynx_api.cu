@@ -15,8 +15,9 @@
 namespace lynx {
 namespace {
 
-constexpr int64_t kMaxM = 65535LL * 128;  // grid.y limit of the GEMM
+constexpr int64_t kMaxM = 65535LL * 128;  // keeps int row indices and TMA coordinates far inside 32 bits
 constexpr int64_t kMaxN = 1LL << 24;
+constexpr int64_t kMaxMN = 1LL << 40;     // keeps the GEMMs' int tile counts (<= M N / 2^15) inside 32 bits
 constexpr int64_t kMaxK = 1LL << 20;
 constexpr int kRank = 64;
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;
@@ -104,6 +105,11 @@ bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) !=
 
 int check_mk(int64_t M, int64_t K) {
   if (M < 1 || M > kMaxM || K < 16 || K > kMaxK || K % 16 != 0) return LYNX_ERR_SHAPE;
+  return LYNX_OK;
+}
+
+int check_n(int64_t M, int64_t N) {
+  if (N < 1 || N > kMaxN || M * N > kMaxMN) return LYNX_ERR_SHAPE;
   return LYNX_OK;
 }
 
@@ -223,7 +229,7 @@ int lynx_linear(const void* X, const void* W, const void* LA, const void* LB, vo
                 int64_t K, int64_t R, void* workspace, size_t workspace_bytes, void* stream) {
   if (!X || !W || !LA || !LB || !Y || !workspace) return LYNX_ERR_NULL;
   if (int e = check_mk(M, K)) return e;
-  if (N < 1 || N > kMaxN) return LYNX_ERR_SHAPE;
+  if (int e = check_n(M, N)) return e;
   if (R != kRank) return R < 1 ? LYNX_ERR_SHAPE : LYNX_ERR_UNSUPPORTED;
   if (misaligned(X) || misaligned(W) || misaligned(LA) || misaligned(LB) || misaligned(Y) || misaligned(workspace))
     return LYNX_ERR_ALIGN;
@@ -286,7 +292,7 @@ int lynx_linear_dense(const void* X, const void* W, const void* LA, const void* 
   const bool lora = LA || LB;
   if (lora && (!LA || !LB || !workspace)) return LYNX_ERR_NULL;
   if (int e = check_mk(M, K)) return e;
-  if (N < 1 || N > kMaxN) return LYNX_ERR_SHAPE;
+  if (int e = check_n(M, N)) return e;
   if (lora && R != kRank) return R < 1 ? LYNX_ERR_SHAPE : LYNX_ERR_UNSUPPORTED;
   if (misaligned(X) || misaligned(W) || misaligned(Y) ||
       (lora && (misaligned(LA) || misaligned(LB) || misaligned(workspace))))

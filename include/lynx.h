@@ -46,7 +46,9 @@ extern "C" {
 typedef enum {
   LYNX_OK = 0,
   LYNX_ERR_NULL = -1,        /* a required pointer is NULL */
-  LYNX_ERR_SHAPE = -2,       /* M, N, K or R out of range, or K % 16 != 0 */
+  LYNX_ERR_SHAPE = -2,       /* M, N, K or R out of range, or K % 16 != 0.  Ranges:
+                                1 <= M <= 8388480 (65535 * 128), 1 <= N <= 2^24,
+                                16 <= K <= 2^20, M * N <= 2^40, R >= 1 */
   LYNX_ERR_ALIGN = -3,       /* a pointer is not 16-byte aligned */
   LYNX_ERR_WORKSPACE = -4,   /* workspace smaller than lynx_*workspace_bytes() */
   LYNX_ERR_CUDA = -5,        /* a CUDA runtime/driver call failed */

@@ -66,6 +66,10 @@ A = 1 << 20  # a fake, 16-byte aligned address: never dereferenced by the host c
     ((A, A, A, A, A, 16, 16, 24, 64, A, 1 << 30), -2),            # K % 16
     ((A, A, A, A, A, 0, 16, 16, 64, A, 1 << 30), -2),             # M = 0
     ((A, A, A, A, A, 16, 0, 16, 64, A, 1 << 30), -2),             # N = 0
+    ((A, A, A, A, A, 16, (1 << 24) + 1, 16, 64, A, 1 << 62), -2), # N above 2^24
+    ((A, A, A, A, A, 65535 * 128 + 1, 16, 16, 64, A, 1 << 62), -2),  # M above 65535 * 128
+    ((A, A, A, A, A, 16, 16, (1 << 20) + 16, 64, A, 1 << 62), -2),   # K above 2^20
+    ((A, A, A, A, A, 65535 * 128, 1 << 24, 16, 64, A, 1 << 62), -2),  # M N above 2^40
     ((A, A, A, A, A, 16, 16, 16, 32, A, 1 << 30), -7),            # R != 64
     ((A + 8, A, A, A, A, 16, 16, 16, 64, A, 1 << 30), -3),        # misaligned X
     ((A, A, A, A, A + 2, 16, 16, 16, 64, A, 1 << 30), -3),        # misaligned Y
@@ -90,6 +94,7 @@ def test_other_entry_points_reject_bad_arguments(asl):
     assert L.lynx_linear_dense(A, A, A, None, A, 4, 16, 16, 64, A, 1 << 20, None) == -1   # one LoRA factor
     assert L.lynx_linear_dense(A, A, A, A, A, 4, 16, 16, 64, A, 10, None) == -4
     assert L.lynx_linear_dense(A, A, None, None, A, 4, 16, 17, 64, None, 0, None) == -2
+    assert L.lynx_linear_dense(A, A, None, None, A, 1 << 22, 1 << 19, 16, 64, None, 0, None) == -2   # M N > 2^40
     for code in range(-7, 1):
         assert L.lynx_status_string(code)
 
