@@ -49,7 +49,7 @@ def _load() -> ctypes.CDLL:
         "lynx_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "lynx_meta_to_canonical": (ctypes.c_int, [_c_p, _c_p, _c_i64, _c_i64]),
         "lynx_debug_set_fault": (None, [ctypes.c_int, ctypes.c_uint64]),
-        "lynx_debug_force_tile": (None, [ctypes.c_int]),
+        "lynx_debug_force_tile": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
         "lynx_profile_next": (None, [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]),
         "lynx_linear_kernel_count": (ctypes.c_int, [_c_i64, _c_i64, _c_i64, _c_i64]),
         "lynx_mma_rate": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_double),
@@ -240,6 +240,6 @@ def lynx_debug_set_fault(inject: int, wait_ns: int = 0) -> None:
     lib.lynx_debug_set_fault(inject, wait_ns)
 
 
-def lynx_debug_force_tile(row_blocks: int) -> None:
-    """Test hook: 2 or 1 forces the 512x192 or 256x256 sparse tile shape; 0 restores the automatic choice."""
-    lib.lynx_debug_force_tile(row_blocks)
+def lynx_debug_force_tile(tile_rows: int, tile_cols: int) -> None:
+    """Test hook: forces the 512x224, 512x192 or 256x256 sparse tile shape; (0, 0) restores the automatic choice."""
+    _check(lib.lynx_debug_force_tile(tile_rows, tile_cols), "lynx_debug_force_tile")

@@ -11,9 +11,10 @@
 // The shape is set by the bytes each SM must pull into shared memory per
 // multiply-add, which bounds this kernel: per 128-channel step a CTA stages
 // MB x 16 KiB of compressed A, TN/2 x 256 B of W and MB x 2 KiB of metadata.
-// The sparse path takes MB = 2, TN = 192 (60 KiB per 6.3 M logical MACs,
-// against 50 KiB per 4.2 M for MB = 1, TN = 256); the two accumulators and
-// the metadata ring fill 416 of the 512 TMEM columns.
+// The sparse path takes MB = 2 with TN = 224 (64 KiB per 7.3 M logical MACs;
+// the two accumulators and the metadata ring fill 480 of the 512 TMEM
+// columns) or TN = 192 (60 KiB per 6.3 M), or MB = 1, TN = 256 (50 KiB per
+// 4.2 M) for few row tiles.
 //
 // Sparse A (compressed values, 128-byte swizzle) goes through
 // tcgen05.mma.sp.cta_group::2 in steps of 128 channels: every stage carries
@@ -330,7 +331,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const int h = MB == 2 ? w2 : 0;
     constexpr int COLS = MB == 2 ? TN : TN / 2;
     constexpr int NC = COLS / 32;
-    static_assert(NC % 2 == 0, "chunks are drained in pairs");
     const int col_off = MB == 2 ? 0 : w2 * COLS;
     const bool vec_ok = (a.ldy % 8) == 0;
     const bool scaled = a.scale_mode == SCALE_MUL;
@@ -338,7 +338,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     uint8_t* ybuf = ystage + (warp - 2) * 2 * Y_BUF;
     const uint32_t acc_empty_leader = mapa_shared(acc_empty, 0);
     const uint32_t taddr_warp = tmem + (static_cast<uint32_t>(q * 32) << 16) + h * TN + col_off;
-    int tcount = 0;
+    int tcount = 0, ybox = 0;
     for (int tile = cluster; tile < ntiles; tile += nclusters, ++tcount) {
       const int mp = tile % num_mp, nb = tile / num_mp;
       const int row0 = mp * 2 * C::ROWS + static_cast<int>(rank) * C::ROWS + h * BLOCK + q * 32;
@@ -351,44 +351,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       tc_fence_after();
       __nv_bfloat16* yrow = static_cast<__nv_bfloat16*>(a.Y) + static_cast<int64_t>(row) * a.ldy;
       const bool live = row < a.M;
-      // Drain: the whole 32 x COLS slice is read into registers (converted to bf16 pairs) before anything is
-      // written out, so the accumulators are released after three TMEM round trips.
-      uint32_t pk[(NC - 2) * 16 + 1];
-      uint32_t r0[32], r1[32];
-#pragma unroll
-      for (int c2 = 0; c2 < NC; c2 += 2) {
-        tc_ld_32x32b_x32(taddr_warp + c2 * 32, r0);
-        tc_ld_32x32b_x32(taddr_warp + (c2 + 1) * 32, r1);
-        tc_wait_ld();
-        if (c2 + 2 == NC) {
-          tc_fence_before();
-          __syncwarp();
-          // the pair's accumulators may be overwritten: this warp's TMEM reads have completed (wait::ld)
-          if (lane == 0) mbar_arrive_cluster_relaxed(acc_empty_leader);
-        }
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          __nv_bfloat162 v0 = __floats2bfloat162_rn(__uint_as_float(r0[2 * j]) * sc, __uint_as_float(r0[2 * j + 1]) * sc);
-          __nv_bfloat162 v1 = __floats2bfloat162_rn(__uint_as_float(r1[2 * j]) * sc, __uint_as_float(r1[2 * j + 1]) * sc);
-          r0[j] = *reinterpret_cast<uint32_t*>(&v0);
-          r1[j] = *reinterpret_cast<uint32_t*>(&v1);
-        }
-        if (c2 + 2 < NC) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            pk[c2 * 16 + j] = r0[j];
-            pk[(c2 + 1) * 16 + j] = r1[j];
-          }
-        }
-      }
-      // Write-out, overlapping the next tile's main loop: one bulk group per chunk, the two staging boxes
-      // used alternately (NC is even, so every tile starts on box 0).
-#pragma unroll
-      for (int c = 0; c < NC; ++c) {
-        const uint32_t* p = c < NC - 2 ? pk + c * 16 : (c == NC - 2 ? r0 : r1);
+      // Drain: the 32 x COLS slice is read into registers (converted to bf16 pairs) before most of it is
+      // written out, so the accumulators are released after ceil(NC / 2) TMEM round trips.  At most HOLD
+      // chunks stay in registers (the register file holds no more without spilling); the first NC - HOLD
+      // chunks are written out as soon as they are converted.
+      constexpr int HOLD = 6;
+      constexpr int EARLY = NC > HOLD ? NC - HOLD : 0;
+      static_assert(EARLY <= 2, "early chunks use the warp's two staging boxes");
+      uint32_t pk[NC * 16];
+      auto write_chunk = [&](int c) {
+        const uint32_t* p = pk + c * 16;
         const int col0 = n0 + c * 32;
         if (y_tma) {
-          uint8_t* box = ybuf + (c & 1) * Y_BUF;
+          uint8_t* box = ybuf + ((ybox + c) & 1) * Y_BUF;
           if (lane == 0) bulk_wait_read_one();  // the store that last used this box has read it
           __syncwarp();
 #pragma unroll
@@ -404,7 +379,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         } else if (live) {
           store_chunk(yrow, col0, a.N, vec_ok, p);
         }
+      };
+#pragma unroll
+      for (int c2 = 0; c2 < NC; c2 += 2) {
+        const bool two = c2 + 1 < NC;
+        uint32_t r0[32], r1[32];
+        tc_ld_32x32b_x32(taddr_warp + c2 * 32, r0);
+        if (two) tc_ld_32x32b_x32(taddr_warp + (c2 + 1) * 32, r1);
+        tc_wait_ld();
+        if (c2 + 2 >= NC) {
+          tc_fence_before();
+          __syncwarp();
+          // the pair's accumulators may be overwritten: this warp's TMEM reads have completed (wait::ld)
+          if (lane == 0) mbar_arrive_cluster_relaxed(acc_empty_leader);
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          __nv_bfloat162 v0 = __floats2bfloat162_rn(__uint_as_float(r0[2 * j]) * sc, __uint_as_float(r0[2 * j + 1]) * sc);
+          pk[c2 * 16 + j] = *reinterpret_cast<uint32_t*>(&v0);
+          if (two) {
+            __nv_bfloat162 v1 = __floats2bfloat162_rn(__uint_as_float(r1[2 * j]) * sc, __uint_as_float(r1[2 * j + 1]) * sc);
+            pk[(c2 + 1) * 16 + j] = *reinterpret_cast<uint32_t*>(&v1);
+          }
+        }
+        if (c2 < EARLY) write_chunk(c2);
+        if (c2 + 1 < EARLY) write_chunk(c2 + 1);
       }
+      // Write-out of the rest, overlapping the next tile's main loop: one bulk group per chunk, the warp's two
+      // staging boxes used alternately over the whole tile sequence.
+#pragma unroll
+      for (int c = EARLY; c < NC; ++c) write_chunk(c);
+      ybox += NC;
     }
     if (y_tma && lane == 0) bulk_wait_all();
   }
@@ -463,8 +468,9 @@ cudaError_t launch(const PairArgs& a, cudaStream_t st) {
 }  // namespace
 
 // Shared-memory traffic per thousand logical MACs of each sparse shape (TMA fill plus tensor-core operand
-// reads, the kernel's binding resource): 512 x 192 tiles 22.9 B, 256 x 256 tiles 23.8 B.  The shape with the
-// smaller (tile waves x tile work x traffic) wins; 512 x 192 for the large DiT shapes, 256 x 256 when few
+// reads, the kernel's binding resource): 512 x 224 tiles 21.3 B, 512 x 192 tiles 22.9 B, 256 x 256 tiles
+// 23.8 B.  The shape with the smallest (tile waves x tile work x traffic) wins: 512 x 224 for the large DiT
+// QKV and MLP-up shapes, 512 x 192 where 224-wide column tiles would add a wave (N = 3072), 256 x 256 when few
 // row tiles would leave pairs idle (e.g. M = 1024).
 PairShape pair_shape(bool sparse, int M, int N) {
   if (!sparse) return {1, 256};
@@ -474,19 +480,33 @@ PairShape pair_shape(bool sparse, int M, int N) {
     const int64_t waves = (tiles + clusters - 1) / clusters;
     return static_cast<double>(waves) * 256.0 * rb * tn * bytes_per_kmac;
   };
-  return cost(2, 192, 22.9) <= cost(1, 256, 23.8) ? PairShape{2, 192} : PairShape{1, 256};
+  const PairShape cand[3] = {{2, 224}, {2, 192}, {1, 256}};
+  const double bytes[3] = {21.3, 22.9, 23.8};
+  int best = 0;
+  double best_cost = cost(cand[0].rb, cand[0].tn, bytes[0]);
+  for (int i = 1; i < 3; ++i) {
+    const double c = cost(cand[i].rb, cand[i].tn, bytes[i]);
+    if (c < best_cost) {
+      best = i;
+      best_cost = c;
+    }
+  }
+  return cand[best];
+}
+
+bool pair_shape_valid(bool sparse, PairShape shape) {
+  if (!sparse) return shape.rb == 1 && shape.tn == 256;
+  return (shape.rb == 2 && (shape.tn == 224 || shape.tn == 192)) || (shape.rb == 1 && shape.tn == 256);
 }
 
 cudaError_t launch_gemm_pair(bool sparse, bool lora, PairShape shape, const PairArgs& a, cudaStream_t st) {
-  if (!sparse) {
-    if (shape.rb != 1 || shape.tn != 256) return cudaErrorInvalidValue;
-    return lora ? launch<false, true, 1, 256>(a, st) : launch<false, false, 1, 256>(a, st);
-  }
-  if (shape.rb == 2 && shape.tn == 192)
+  if (!pair_shape_valid(sparse, shape)) return cudaErrorInvalidValue;
+  if (!sparse) return lora ? launch<false, true, 1, 256>(a, st) : launch<false, false, 1, 256>(a, st);
+  if (shape.rb == 2 && shape.tn == 224)
+    return lora ? launch<true, true, 2, 224>(a, st) : launch<true, false, 2, 224>(a, st);
+  if (shape.rb == 2)
     return lora ? launch<true, true, 2, 192>(a, st) : launch<true, false, 2, 192>(a, st);
-  if (shape.rb == 1 && shape.tn == 256)
-    return lora ? launch<true, true, 1, 256>(a, st) : launch<true, false, 1, 256>(a, st);
-  return cudaErrorInvalidValue;
+  return lora ? launch<true, true, 1, 256>(a, st) : launch<true, false, 1, 256>(a, st);
 }
 
 }  // namespace lynx

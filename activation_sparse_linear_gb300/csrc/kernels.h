@@ -78,12 +78,13 @@ struct GemmArgs {
 cudaError_t launch_proj_gemm(const GemmArgs& a, cudaStream_t st);
 
 // Pair-tile shapes: rb = 128-row blocks per CTA (the pair covers 256 * rb rows), tn = output columns per tile
-// (W and LA are staged tn / 2 rows per CTA).  The sparse path uses 512 x 192 tiles, or 256 x 256 when that
-// gives fewer tile waves for the shape; the dense path uses 256 x 256.
+// (W and LA are staged tn / 2 rows per CTA).  The sparse path uses 512 x 224, 512 x 192 or 256 x 256 tiles,
+// whichever costs the fewest tile waves x shared-memory bytes for the shape; the dense path uses 256 x 256.
 struct PairShape {
   int rb, tn;
 };
 PairShape pair_shape(bool sparse, int M, int N);
+bool pair_shape_valid(bool sparse, PairShape shape);
 
 struct PairArgs {
   CUtensorMap tmA;     // sparse: compressed values; dense: X (both box 64 x 128, 128-byte swizzle)

@@ -25,7 +25,7 @@ constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 __device__ int g_error_word;
 
 std::atomic<int> g_inject{0};
-std::atomic<int> g_force_tile{0};  // 0: tile shape by problem shape; 1 or 2: forced row blocks per CTA
+std::atomic<int> g_force_tile{0};  // 0: tile shape by problem shape; else a forced shape, rb << 16 | tn
 thread_local void* const* t_prof_events = nullptr;
 thread_local int t_prof_count = 0;
 
@@ -240,9 +240,8 @@ int lynx_linear(const void* X, const void* W, const void* LA, const void* LB, vo
   PairArgs g;
   std::memset(&g, 0, sizeof(g));
   const int forced = g_force_tile.load();
-  const PairShape shape = forced == 2   ? PairShape{2, 192}
-                          : forced == 1 ? PairShape{1, 256}
-                                        : pair_shape(true, static_cast<int>(M), static_cast<int>(N));
+  const PairShape shape = forced ? PairShape{forced >> 16, forced & 0xFFFF}
+                                 : pair_shape(true, static_cast<int>(M), static_cast<int>(N));
   const uint64_t meta_rows = 2 * static_cast<uint64_t>(meta_bytes(M, K) / kMetaChunkBytes);  // 1 KiB rows
   if (!make_map(&g.tmA, ws.vals, K / 2, M, K / 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&g.tmB, W, K, N, K, 64, shape.tn / 2, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -397,7 +396,16 @@ void lynx_debug_set_fault(int inject, uint64_t wait_ns) {
   g_wait_ns.store(wait_ns ? wait_ns : kDefaultWaitNs);
 }
 
-void lynx_debug_force_tile(int row_blocks) { g_force_tile.store(row_blocks == 1 || row_blocks == 2 ? row_blocks : 0); }
+int lynx_debug_force_tile(int tile_rows, int tile_cols) {
+  if (tile_rows == 0 && tile_cols == 0) {
+    g_force_tile.store(0);
+    return LYNX_OK;
+  }
+  const PairShape shape{tile_rows / 256, tile_cols};
+  if (tile_rows % 256 != 0 || !pair_shape_valid(true, shape)) return LYNX_ERR_UNSUPPORTED;
+  g_force_tile.store(shape.rb << 16 | shape.tn);
+  return LYNX_OK;
+}
 
 }  // extern "C"
 

@@ -213,9 +213,10 @@ LYNX_API int lynx_mma_rate(int mode, int iters, double* tflops, double* macs_per
  * restores normal operation; wait_ns = 0 restores the default bound (2 s). */
 LYNX_API void lynx_debug_set_fault(int inject, uint64_t wait_ns);
 
-/* Test hook.  row_blocks = 2 or 1 makes lynx_linear use 512 x 192 or 256 x 256 sparse pair tiles for every
- * shape (both must give the same result); 0 restores the automatic choice by shape. */
-LYNX_API void lynx_debug_force_tile(int row_blocks);
+/* Test hook.  Makes lynx_linear use sparse pair tiles of tile_rows x tile_cols for every shape: 512 x 224,
+ * 512 x 192 or 256 x 256 (all must give the same result); 0 x 0 restores the automatic choice by shape.
+ * Returns LYNX_OK, or LYNX_ERR_UNSUPPORTED (setting unchanged) for any other shape. */
+LYNX_API int lynx_debug_force_tile(int tile_rows, int tile_cols);
 
 #ifdef __cplusplus
 }

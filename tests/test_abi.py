@@ -99,6 +99,17 @@ def test_other_entry_points_reject_bad_arguments(asl):
         assert L.lynx_status_string(code)
 
 
+def test_force_tile_accepts_only_built_shapes(asl):
+    L = asl.lib
+    try:
+        for rows, cols in [(512, 256), (256, 192), (384, 224), (1, 1), (0, 224)]:
+            assert L.lynx_debug_force_tile(rows, cols) == -7
+        for rows, cols in [(512, 224), (512, 192), (256, 256)]:
+            assert L.lynx_debug_force_tile(rows, cols) == 0
+    finally:
+        assert L.lynx_debug_force_tile(0, 0) == 0
+
+
 @pytest.mark.parametrize("M,K", [(1, 16), (5, 136), (130, 256), (17, 96), (300, 512)])
 def test_meta_to_canonical_matches_documented_layout(asl, M, K):
     from helpers import pack_meta_reference

@@ -114,16 +114,16 @@ def _layer(M, N, K, seed=7, xkind="act"):
     return X, W, LA, LB
 
 
-@pytest.mark.parametrize("tile", [2, 1])  # 512 x 192 and 256 x 256 sparse pair tiles
+@pytest.mark.parametrize("tile", [(512, 224), (512, 192), (256, 256)])  # sparse pair tile shapes
 @pytest.mark.parametrize("M,N,K", LINEAR_CASES)
 def test_linear_full_comparison(lynx, M, N, K, tile):
     X, W, LA, LB = _layer(M, N, K)
-    lynx.lynx_debug_force_tile(tile)
+    lynx.lynx_debug_force_tile(*tile)
     try:
         Y = lynx.lynx_linear(to_dev(X), to_dev(W), to_dev(LA), to_dev(LB))
         assert lynx.lynx_sync_status() == 0
     finally:
-        lynx.lynx_debug_force_tile(0)
+        lynx.lynx_debug_force_tile(0, 0)
     assert_y_close(to_bits(Y), O.linear(X, W, LA, LB))
 
 
