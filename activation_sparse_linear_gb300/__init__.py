@@ -23,12 +23,23 @@ __all__ = [
     "lynx_sync_status", "lynx_status_string", "lynx_meta_to_canonical", "lynx_debug_set_fault",
     "lynx_debug_force_tile",
     "lynx_profile_next", "lynx_linear_kernel_count", "lynx_mma_rate",
+    "LynxLayer", "lynx_layer", "lynx_layers_workspace_bytes", "lynx_run_layers", "LynxGraph",
 ]
 
 LYNX_OK = 0
 LYNX_ERR_TIMEOUT = -6
 
 _c_i64, _c_sz, _c_p = ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p
+
+
+class LynxLayer(ctypes.Structure):
+    """``lynx_layer`` of include/lynx.h: one sparse (lynx_linear) or dense (lynx_linear_dense) layer."""
+    _fields_ = [("sparse", ctypes.c_int32), ("X", _c_p), ("W", _c_p), ("LA", _c_p), ("LB", _c_p), ("Y", _c_p),
+                ("M", _c_i64), ("N", _c_i64), ("K", _c_i64), ("R", _c_i64)]
+
+
+_c_layers = ctypes.POINTER(LynxLayer)
+_c_i32p = ctypes.POINTER(ctypes.c_int32)
 
 
 def _load() -> ctypes.CDLL:
@@ -54,6 +65,11 @@ def _load() -> ctypes.CDLL:
         "lynx_linear_kernel_count": (ctypes.c_int, [_c_i64, _c_i64, _c_i64, _c_i64]),
         "lynx_mma_rate": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_double),
                                          ctypes.POINTER(ctypes.c_double), _c_p]),
+        "lynx_layers_workspace_bytes": (_c_sz, [_c_layers, ctypes.c_int32]),
+        "lynx_run_layers": (ctypes.c_int, [_c_layers, ctypes.c_int32, _c_p, _c_sz, _c_p, _c_i32p]),
+        "lynx_graph_create": (ctypes.c_int, [_c_layers, ctypes.c_int32, _c_p, _c_sz, ctypes.POINTER(_c_p), _c_i32p]),
+        "lynx_graph_launch": (ctypes.c_int, [_c_p, _c_p]),
+        "lynx_graph_destroy": (ctypes.c_int, [_c_p]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -243,3 +259,76 @@ def lynx_debug_set_fault(inject: int, wait_ns: int = 0) -> None:
 def lynx_debug_force_tile(tile_rows: int, tile_cols: int) -> None:
     """Test hook: forces the 512x224, 512x192 or 256x256 sparse tile shape; (0, 0) restores the automatic choice."""
     _check(lib.lynx_debug_force_tile(tile_rows, tile_cols), "lynx_debug_force_tile")
+
+
+# ------------------------------------------------------------------ layer sequences and their CUDA graphs
+def lynx_layer(X, W, LA=None, LB=None, Y=None, sparse: bool = True) -> dict:
+    """One layer of a sequence: Y = lynx_linear(X, W, LA, LB) (sparse) or lynx_linear_dense(X, W, LA, LB).
+    Allocates Y (M x N bf16) when not given.  The dict keeps the tensors alive."""
+    torch = _torch()
+    _need(X, "X", torch.bfloat16)
+    _need(W, "W", torch.bfloat16)
+    M, K = X.shape
+    N = W.shape[0]
+    R = 64 if LB is None else LB.shape[0]
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device) if Y is None else Y
+    return {"sparse": bool(sparse), "X": X, "W": W, "LA": LA, "LB": LB, "Y": Y, "M": M, "N": N, "K": K, "R": R}
+
+
+def _c_layer_array(layers):
+    arr = (LynxLayer * max(len(layers), 1))()
+    for i, l in enumerate(layers):
+        arr[i] = LynxLayer(int(l["sparse"]), _ptr(l["X"]), _ptr(l["W"]), _ptr(l["LA"]), _ptr(l["LB"]), _ptr(l["Y"]),
+                           l["M"], l["N"], l["K"], l["R"])
+    return arr
+
+
+def lynx_layers_workspace_bytes(layers) -> int:
+    return lib.lynx_layers_workspace_bytes(_c_layer_array(layers), len(layers))
+
+
+def _layer_error(status: int, failed: ctypes.c_int32, where: str) -> None:
+    if status != LYNX_OK:
+        raise LynxError(status, f"{where} (layer {failed.value})" if failed.value >= 0 else where)
+
+
+def lynx_run_layers(layers, workspace=None, stream=None):
+    """Runs the layers in order on one stream; returns the list of their Y tensors."""
+    torch = _torch()
+    if workspace is None and layers:
+        workspace = torch.empty(max(lynx_layers_workspace_bytes(layers), 1), dtype=torch.uint8,
+                                device=layers[0]["X"].device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    failed = ctypes.c_int32(-1)
+    _layer_error(lib.lynx_run_layers(_c_layer_array(layers), len(layers), _ptr(workspace), wbytes, _stream(stream),
+                                     ctypes.byref(failed)), failed, "lynx_run_layers")
+    return [l["Y"] for l in layers]
+
+
+class LynxGraph:
+    """A layer sequence captured once into a CUDA graph; ``launch()`` replays all of its kernels.
+    Holds references to every tensor of the layers and to the workspace, whose addresses the graph uses."""
+
+    def __init__(self, layers, workspace=None):
+        torch = _torch()
+        self.layers = list(layers)
+        if workspace is None:
+            workspace = torch.empty(max(lynx_layers_workspace_bytes(self.layers), 1), dtype=torch.uint8,
+                                    device=self.layers[0]["X"].device)
+        self.workspace = workspace
+        handle, failed = _c_p(), ctypes.c_int32(-1)
+        _layer_error(lib.lynx_graph_create(_c_layer_array(self.layers), len(self.layers), _ptr(workspace),
+                                           workspace.numel() * workspace.element_size(), ctypes.byref(handle),
+                                           ctypes.byref(failed)), failed, "lynx_graph_create")
+        self._handle = handle
+
+    def launch(self, stream=None) -> None:
+        if not self._handle:
+            raise LynxError(-1, "LynxGraph.launch after close")
+        _check(lib.lynx_graph_launch(self._handle, _stream(stream)), "lynx_graph_launch")
+
+    def close(self) -> None:
+        """Frees the graph; call after the replays have completed."""
+        if self._handle:
+            _check(lib.lynx_graph_destroy(self._handle), "lynx_graph_destroy")
+            self._handle = _c_p()

@@ -107,4 +107,13 @@ cudaError_t launch_gemm_pair(bool sparse, bool lora, PairShape shape, const Pair
 
 int sm_count();
 
+// Host argument checks of lynx_linear and lynx_linear_dense (lynx_api.cu): the status either call would return
+// before launching anything, LYNX_OK when it would launch.
+int linear_arg_status(const void* X, const void* W, const void* LA, const void* LB, const void* Y, int64_t M,
+                      int64_t N, int64_t K, int64_t R, const void* workspace, size_t workspace_bytes);
+int dense_arg_status(const void* X, const void* W, const void* LA, const void* LB, const void* Y, int64_t M,
+                     int64_t N, int64_t K, int64_t R, const void* workspace, size_t workspace_bytes);
+// Drops this thread's pending stage-timing request (lynx_profile_next), so that a graph capture records none.
+void clear_stage_request();
+
 }  // namespace lynx

@@ -189,6 +189,40 @@ int make_prologue(ProArgs* pa, const void* X, const void* LB, int64_t M, int64_t
 }
 
 }  // namespace
+
+int linear_arg_status(const void* X, const void* W, const void* LA, const void* LB, const void* Y, int64_t M,
+                      int64_t N, int64_t K, int64_t R, const void* workspace, size_t workspace_bytes) {
+  if (!X || !W || !LA || !LB || !Y || !workspace) return LYNX_ERR_NULL;
+  if (int e = check_mk(M, K)) return e;
+  if (int e = check_n(M, N)) return e;
+  if (R != kRank) return R < 1 ? LYNX_ERR_SHAPE : LYNX_ERR_UNSUPPORTED;
+  if (misaligned(X) || misaligned(W) || misaligned(LA) || misaligned(LB) || misaligned(Y) || misaligned(workspace))
+    return LYNX_ERR_ALIGN;
+  if (workspace_bytes < carve(nullptr, M, K, R).bytes) return LYNX_ERR_WORKSPACE;
+  return LYNX_OK;
+}
+
+int dense_arg_status(const void* X, const void* W, const void* LA, const void* LB, const void* Y, int64_t M,
+                     int64_t N, int64_t K, int64_t R, const void* workspace, size_t workspace_bytes) {
+  if (!X || !W || !Y) return LYNX_ERR_NULL;
+  const bool lora = LA || LB;
+  if (lora && (!LA || !LB || !workspace)) return LYNX_ERR_NULL;
+  if (int e = check_mk(M, K)) return e;
+  if (int e = check_n(M, N)) return e;
+  if (lora && R != kRank) return R < 1 ? LYNX_ERR_SHAPE : LYNX_ERR_UNSUPPORTED;
+  if (misaligned(X) || misaligned(W) || misaligned(Y) ||
+      (lora && (misaligned(LA) || misaligned(LB) || misaligned(workspace))))
+    return LYNX_ERR_ALIGN;
+  if (lora && workspace_bytes < align256(static_cast<size_t>(M) * static_cast<size_t>(R) * 2))
+    return LYNX_ERR_WORKSPACE;
+  return LYNX_OK;
+}
+
+void clear_stage_request() {
+  t_prof_events = nullptr;
+  t_prof_count = 0;
+}
+
 }  // namespace lynx
 
 using namespace lynx;
@@ -227,14 +261,8 @@ int lynx_lora_down(const void* X, const void* LB, const float* s, void* T, int64
 
 int lynx_linear(const void* X, const void* W, const void* LA, const void* LB, void* Y, int64_t M, int64_t N,
                 int64_t K, int64_t R, void* workspace, size_t workspace_bytes, void* stream) {
-  if (!X || !W || !LA || !LB || !Y || !workspace) return LYNX_ERR_NULL;
-  if (int e = check_mk(M, K)) return e;
-  if (int e = check_n(M, N)) return e;
-  if (R != kRank) return R < 1 ? LYNX_ERR_SHAPE : LYNX_ERR_UNSUPPORTED;
-  if (misaligned(X) || misaligned(W) || misaligned(LA) || misaligned(LB) || misaligned(Y) || misaligned(workspace))
-    return LYNX_ERR_ALIGN;
+  if (int e = linear_arg_status(X, W, LA, LB, Y, M, N, K, R, workspace, workspace_bytes)) return e;
   Workspace ws = carve(workspace, M, K, R);
-  if (workspace_bytes < ws.bytes) return LYNX_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   PairArgs g;
@@ -287,16 +315,8 @@ int lynx_sparsify_lora(const void* X, const void* LB, int64_t M, int64_t K, int6
 
 int lynx_linear_dense(const void* X, const void* W, const void* LA, const void* LB, void* Y, int64_t M,
                       int64_t N, int64_t K, int64_t R, void* workspace, size_t workspace_bytes, void* stream) {
-  if (!X || !W || !Y) return LYNX_ERR_NULL;
+  if (int e = dense_arg_status(X, W, LA, LB, Y, M, N, K, R, workspace, workspace_bytes)) return e;
   const bool lora = LA || LB;
-  if (lora && (!LA || !LB || !workspace)) return LYNX_ERR_NULL;
-  if (int e = check_mk(M, K)) return e;
-  if (int e = check_n(M, N)) return e;
-  if (lora && R != kRank) return R < 1 ? LYNX_ERR_SHAPE : LYNX_ERR_UNSUPPORTED;
-  if (misaligned(X) || misaligned(W) || misaligned(Y) ||
-      (lora && (misaligned(LA) || misaligned(LB) || misaligned(workspace))))
-    return LYNX_ERR_ALIGN;
-  if (lora && workspace_bytes < lynx_dense_workspace_bytes(M, R)) return LYNX_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   PairArgs g;

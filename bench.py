@@ -448,8 +448,24 @@ def main() -> int:
                 torch.matmul(x3, w["out"].t(), out=y[3072])
                 torch.matmul(x3, w["up"].t(), out=y[12288])
                 torch.matmul(x12, w["down"].t(), out=y[3072])
+
+        # The same 32 linears as one CUDA graph each: the library's layer-sequence graph and a captured
+        # torch/cuBLAS graph of the dense stack, so that neither side pays a host call per layer.
+        layers = []
+        for w in wts:
+            layers += [asl.lynx_layer(x3, w["qkv"], w["la_qkv"], w["lb_qkv"], y[9216], sparse=True),
+                       asl.lynx_layer(x12, w["down"], w["la_down"], w["lb_down"], y[3072], sparse=True),
+                       asl.lynx_layer(x3, w["out"], None, None, y[3072], sparse=False),
+                       asl.lynx_layer(x3, w["up"], None, None, y[12288], sparse=False)]
+        lgraph = asl.LynxGraph(layers, ws_s)
+        dense_stack()  # cuBLAS workspace and kernels chosen before capture
+        torch.cuda.synchronize()
+        dgraph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(dgraph):
+            dense_stack()
+        torch.cuda.synchronize()
         tt = []
-        for fn in (lynx_stack, dense_stack):
+        for fn in (lynx_stack, dense_stack, lambda: lgraph.launch(stream), dgraph.replay):
             fn()
             torch.cuda.synchronize()
             a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -461,8 +477,11 @@ def main() -> int:
             tt.append(a0.elapsed_time(a1) / 3)
         st = asl.lynx_sync_status()
         assert st == 0, asl.lynx_status_string(st)
-        stack[f"M={Ms}"] = {"lynx_ms": tt[0], "all_dense_cublas_ms": tt[1], "x_vs_dense_cublas": tt[1] / tt[0]}
-        del x3, x12, y, ws_s
+        lgraph.close()
+        stack[f"M={Ms}"] = {"lynx_ms": tt[0], "all_dense_cublas_ms": tt[1], "x_vs_dense_cublas": tt[1] / tt[0],
+                            "lynx_graph_ms": tt[2], "all_dense_cublas_graph_ms": tt[3],
+                            "x_vs_dense_cublas_graph": tt[3] / tt[2]}
+        del x3, x12, y, ws_s, layers, lgraph, dgraph
     del wts
     torch.cuda.empty_cache()
 

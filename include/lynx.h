@@ -161,6 +161,61 @@ LYNX_API int lynx_linear_noalloc(const void* X, const void* W, const void* LA, c
 LYNX_API int lynx_linear_dense(const void* X, const void* W, const void* LA, const void* LB, void* Y, int64_t M,
                       int64_t N, int64_t K, int64_t R, void* workspace, size_t workspace_bytes, void* stream);
 
+/* ---------------------------------------------------------------- layer sequences
+ * A DiT block stack with selective layer skipping (RT-Lynx page, Method:
+ * Selective Layer Skipping) is a fixed sequence of sparse and dense linears.
+ * These calls run such a sequence in order on one stream, or capture it once
+ * into a CUDA graph that replays every kernel of it with one host call.
+ * (The graph is a deployment convenience, not part of the paper.) */
+
+/* One layer.  sparse = 1: Y = lynx_linear(X, W, LA, LB) (LA and LB required,
+ * R = 64); sparse = 0: Y = lynx_linear_dense(X, W, LA, LB) (LA and LB both
+ * NULL, or both given with R = 64).  Device pointers and layouts as for those
+ * calls.  A layer may read the Y of an earlier layer of the same sequence. */
+typedef struct {
+  int32_t sparse;
+  const void* X;
+  const void* W;
+  const void* LA;
+  const void* LB;
+  void* Y;
+  int64_t M, N, K, R;
+} lynx_layer;
+
+/* Workspace for a sequence: the largest any one layer needs (the layers run
+ * one after another and reuse it).  0 if layers is NULL or n < 1. */
+LYNX_API size_t lynx_layers_workspace_bytes(const lynx_layer* layers, int32_t n);
+
+/* Enqueues the n layers in order on `stream` (asynchronous).  Every layer is
+ * checked on the host first: if one fails, nothing is enqueued, its status is
+ * returned and its index is stored in *failed_layer (when failed_layer is not
+ * NULL; -1 otherwise).  n = 0 enqueues nothing and returns LYNX_OK. */
+LYNX_API int lynx_run_layers(const lynx_layer* layers, int32_t n, void* workspace, size_t workspace_bytes,
+                             void* stream, int32_t* failed_layer);
+
+/* An instantiated CUDA graph of a layer sequence. */
+typedef struct lynx_graph_s* lynx_graph;
+
+/* Captures lynx_run_layers(layers, n, workspace, workspace_bytes) on a
+ * private stream and instantiates the graph into *graph_out.  Pointers,
+ * shapes and the workspace are baked in: the caller keeps every buffer alive
+ * and at the same address while the graph exists (their contents may change
+ * between launches).  Returns the first failing layer's status (nothing
+ * captured) as lynx_run_layers does, LYNX_ERR_SHAPE for n < 1, LYNX_ERR_NULL
+ * for a NULL layers or graph_out, LYNX_ERR_CUDA if capture or instantiation
+ * fails.  Call it once before any other capture is open on this thread. */
+LYNX_API int lynx_graph_create(const lynx_layer* layers, int32_t n, void* workspace, size_t workspace_bytes,
+                               lynx_graph* graph_out, int32_t* failed_layer);
+
+/* Enqueues one replay of the whole sequence on `stream` (asynchronous).
+ * Replays on one stream run in order; concurrent replays of one graph, or of
+ * graphs sharing a workspace, race. */
+LYNX_API int lynx_graph_launch(lynx_graph graph, void* stream);
+
+/* Frees the graph (NULL is a no-op).  Call it after the replays it enqueued
+ * have completed (e.g. after lynx_sync_status on their stream). */
+LYNX_API int lynx_graph_destroy(lynx_graph graph);
+
 /* Waits for `stream`, then reads and clears the device error word of the
  * current device.  Returns LYNX_OK, LYNX_ERR_TIMEOUT or LYNX_ERR_CUDA. */
 LYNX_API int lynx_sync_status(void* stream);
@@ -174,14 +229,15 @@ LYNX_API const char* lynx_status_string(int status);
 LYNX_API int lynx_meta_to_canonical(const void* meta, uint8_t* canonical, int64_t M, int64_t K);
 
 /* Number of kernels lynx_linear enqueues for these sizes on the current
- * device (3, or 4 when the LoRA down-projection is split over K). */
+ * device: 2 (the fused sparsify + LoRA down-projection pass and the sparse
+ * GEMM). */
 LYNX_API int lynx_linear_kernel_count(int64_t M, int64_t N, int64_t K, int64_t R);
 
 /* Stage-timing hook.  The next lynx_linear or lynx_linear_dense call made
  * from this host thread records events[0] on its stream before its first
  * stage and events[i] right after its i-th stage; count must be the number
- * of stages + 1 (4 for lynx_linear: sparsify, LoRA down-projection, sparse
- * GEMM; 3 for lynx_linear_dense with LoRA, 2 without).  The events are
+ * of stages + 1 (3 for lynx_linear: the fused sparsify + LoRA down-projection
+ * pass, the sparse GEMM; 3 for lynx_linear_dense with LoRA, 2 without).  The events are
  * cudaEvent_t handles owned by the caller.  The setting is used by that one
  * call and then cleared; a count that does not match is ignored. */
 LYNX_API void lynx_profile_next(void* const* events, int count);

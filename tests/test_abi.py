@@ -137,3 +137,45 @@ def test_meta_layout_pairs_rows_r_and_r_plus_8():
     assert words[0, 1] == 0x4444 | ((row8 & 0xFFFF) << 16)          # lane 0, chunk 1
     assert words[8, 1] == 0x4444 | ((row8 >> 16) << 16)             # lane 8, chunk 1
     assert words[1, 0] == 0x44444444 and words[9, 3] == 0x44444444
+
+
+def _layers(asl, specs):
+    arr = (asl.LynxLayer * len(specs))()
+    for i, sp in enumerate(specs):
+        arr[i] = asl.LynxLayer(*sp)
+    return arr
+
+
+def test_layer_sequences_check_every_layer_before_launching(asl):
+    import ctypes
+    L = asl.lib
+    sparse = (1, A, A, A, A, A, 300, 384, 512, 64)
+    dense = (0, A, A, None, None, A, 300, 256, 384, 64)
+    dense_lora = (0, A, A, A, A, A, 300, 528, 256, 64)
+    ok = _layers(asl, [sparse, dense, dense_lora])
+    need = max(asl.lynx_workspace_bytes(300, 384, 512, 64), asl.lynx_dense_workspace_bytes(300, 64))
+    assert L.lynx_layers_workspace_bytes(ok, 3) == need
+    assert L.lynx_layers_workspace_bytes(ok, 0) == 0
+    failed = ctypes.c_int32(7)
+    # a bad layer anywhere: its status and index, nothing launched (no GPU here)
+    for bad, status in [((0, A, A, None, None, A, 300, 256, 250, 64), -2),   # K % 16
+                        ((1, A, A, None, A, A, 300, 256, 512, 64), -1),      # sparse without LA
+                        ((0, A, A, A, None, A, 300, 256, 512, 64), -1),      # one LoRA factor
+                        ((1, A, A, A, A, A + 8, 300, 256, 512, 64), -3),     # misaligned Y
+                        ((1, A, A, A, A, A, 300, 256, 512, 32), -7)]:        # rank other than 64
+        seq = _layers(asl, [sparse, dense, bad])
+        assert L.lynx_run_layers(seq, 3, A, need, None, ctypes.byref(failed)) == status
+        assert failed.value == 2
+    assert L.lynx_run_layers(ok, 3, A, 100, None, ctypes.byref(failed)) == -4     # workspace too small
+    assert failed.value == 0
+    assert L.lynx_run_layers(ok, 0, None, 0, None, ctypes.byref(failed)) == 0     # nothing to do
+    assert failed.value == -1
+    assert L.lynx_run_layers(None, 2, A, need, None, None) == -1
+    handle = ctypes.c_void_p(123)
+    bad = _layers(asl, [sparse, (0, A, A, None, None, A, 0, 256, 384, 64)])  # M = 0
+    assert L.lynx_graph_create(bad, 2, A, need, ctypes.byref(handle), ctypes.byref(failed)) == -2
+    assert failed.value == 1 and not handle.value
+    assert L.lynx_graph_create(ok, 0, A, need, ctypes.byref(handle), None) == -2
+    assert L.lynx_graph_create(ok, 3, A, need, None, None) == -1
+    assert L.lynx_graph_launch(None, None) == -1
+    assert L.lynx_graph_destroy(None) == 0
