@@ -21,7 +21,7 @@ __all__ = [
     "lynx_sparsify", "lynx_sparsify_lora", "lynx_lora_down", "lynx_linear",
     "lynx_linear_dense",
     "lynx_sync_status", "lynx_status_string", "lynx_meta_to_canonical", "lynx_debug_set_fault",
-    "lynx_debug_force_tile",
+    "lynx_debug_force_tile", "lynx_debug_force_split", "lynx_debug_prologue_split",
     "lynx_profile_next", "lynx_linear_kernel_count", "lynx_mma_rate",
     "LynxLayer", "lynx_layer", "lynx_layers_workspace_bytes", "lynx_run_layers", "LynxGraph",
 ]
@@ -61,6 +61,8 @@ def _load() -> ctypes.CDLL:
         "lynx_meta_to_canonical": (ctypes.c_int, [_c_p, _c_p, _c_i64, _c_i64]),
         "lynx_debug_set_fault": (None, [ctypes.c_int, ctypes.c_uint64]),
         "lynx_debug_force_tile": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
+        "lynx_debug_force_split": (ctypes.c_int, [ctypes.c_int]),
+        "lynx_debug_prologue_split": (ctypes.c_int, [_c_i64, _c_i64]),
         "lynx_profile_next": (None, [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]),
         "lynx_linear_kernel_count": (ctypes.c_int, [_c_i64, _c_i64, _c_i64, _c_i64]),
         "lynx_mma_rate": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_double),
@@ -259,6 +261,16 @@ def lynx_debug_set_fault(inject: int, wait_ns: int = 0) -> None:
 def lynx_debug_force_tile(tile_rows: int, tile_cols: int) -> None:
     """Test hook: forces the 512x224, 512x192 or 256x256 sparse tile shape; (0, 0) restores the automatic choice."""
     _check(lib.lynx_debug_force_tile(tile_rows, tile_cols), "lynx_debug_force_tile")
+
+
+def lynx_debug_force_split(split: int) -> None:
+    """Test hook: the sparsify pass runs each 128-row block on a cluster of ``split`` CTAs; 0 = automatic."""
+    _check(lib.lynx_debug_force_split(split), "lynx_debug_force_split")
+
+
+def lynx_debug_prologue_split(M: int, K: int) -> int:
+    """Cluster size the sparsify pass picks on this device for an M x K activation."""
+    return lib.lynx_debug_prologue_split(M, K)
 
 
 # ------------------------------------------------------------------ layer sequences and their CUDA graphs

@@ -51,7 +51,6 @@ constexpr int THREADS = 96 + 32 * EPI_WARPS;
 constexpr int SMEM_LIMIT = 232448;
 constexpr int Y_BOX = 32;                          // output staging box: 32 rows x 32 columns bf16 (64-byte rows)
 constexpr int Y_BUF = Y_BOX * Y_BOX * 2;
-constexpr int Y_STAGING = EPI_WARPS * 2 * Y_BUF;   // two boxes per epilogue warp
 
 enum Site : int { SITE_PRODUCER = 11, SITE_MMA = 12, SITE_EPILOGUE = 13, SITE_DRAIN = 14 };
 
@@ -70,6 +69,11 @@ struct PairCfg {
   static constexpr int B_SLOT = SPARSE ? 2 * SUB : SUB;
   static constexpr int M_SLOT = SPARSE ? MB * kMetaChunkBytes : 0;
   static constexpr int STAGE = A_SLOT + B_SLOT + M_SLOT;
+  // Output staging boxes per epilogue warp: two, so that a box is refilled while the other is stored; one
+  // for the sparse 256 x 256 tile, whose short 128-channel steps need a fourth operand stage in its place
+  // (its few row tiles share each W tile between few CTA pairs, so its loads often come from DRAM).
+  static constexpr int Y_BOXES = (SPARSE && MB == 1) ? 1 : 2;
+  static constexpr int Y_STAGING = EPI_WARPS * Y_BOXES * Y_BUF;
   static constexpr int NST = (SMEM_LIMIT - 1280 - Y_STAGING) / STAGE;
   static constexpr int SMEM = NST * STAGE + Y_STAGING + 256 + 1024;
   static constexpr int META_COL = MB * TN;   // first metadata column (after the accumulators)
@@ -109,7 +113,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ystage = smem + C::NST * C::STAGE;  // 1 KiB aligned
-  uint64_t* full = reinterpret_cast<uint64_t*>(ystage + Y_STAGING);
+  uint64_t* full = reinterpret_cast<uint64_t*>(ystage + C::Y_STAGING);
   uint64_t* empty = full + C::NST;
   uint64_t* acc_full = empty + C::NST;
   uint64_t* acc_empty = acc_full + 1;
@@ -335,7 +339,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const bool vec_ok = (a.ldy % 8) == 0;
     const bool scaled = a.scale_mode == SCALE_MUL;
     const bool y_tma = a.y_tma != 0;
-    uint8_t* ybuf = ystage + (warp - 2) * 2 * Y_BUF;
+    uint8_t* ybuf = ystage + (warp - 2) * C::Y_BOXES * Y_BUF;
     const uint32_t acc_empty_leader = mapa_shared(acc_empty, 0);
     const uint32_t taddr_warp = tmem + (static_cast<uint32_t>(q * 32) << 16) + h * TN + col_off;
     int tcount = 0, ybox = 0;
@@ -357,14 +361,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       // chunks are written out as soon as they are converted.
       constexpr int HOLD = 6;
       constexpr int EARLY = NC > HOLD ? NC - HOLD : 0;
-      static_assert(EARLY <= 2, "early chunks use the warp's two staging boxes");
+      static_assert(EARLY == 0 || (EARLY <= 2 && C::Y_BOXES == 2), "early chunks use the warp's two staging boxes");
       uint32_t pk[NC * 16];
       auto write_chunk = [&](int c) {
         const uint32_t* p = pk + c * 16;
         const int col0 = n0 + c * 32;
         if (y_tma) {
-          uint8_t* box = ybuf + ((ybox + c) & 1) * Y_BUF;
-          if (lane == 0) bulk_wait_read_one();  // the store that last used this box has read it
+          uint8_t* box = ybuf + ((ybox + c) % C::Y_BOXES) * Y_BUF;
+          if (lane == 0) {  // the store that last used this box has read it
+            if constexpr (C::Y_BOXES == 2) bulk_wait_read_one();
+            else bulk_wait_read_all();
+          }
           __syncwarp();
 #pragma unroll
           for (int v = 0; v < 4; ++v)  // 16-byte piece v of this lane's 64-byte row, 64-byte swizzle
@@ -405,8 +412,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         if (c2 < EARLY) write_chunk(c2);
         if (c2 + 1 < EARLY) write_chunk(c2 + 1);
       }
-      // Write-out of the rest, overlapping the next tile's main loop: one bulk group per chunk, the warp's two
-      // staging boxes used alternately over the whole tile sequence.
+      // Write-out of the rest, overlapping the next tile's main loop: one bulk group per chunk, the warp's
+      // staging boxes used in turn over the whole tile sequence.
 #pragma unroll
       for (int c = EARLY; c < NC; ++c) write_chunk(c);
       ybox += NC;

@@ -47,7 +47,7 @@ __host__ __device__ inline int64_t meta_half_offset(int64_t r, int64_t c, int q,
 
 // Fused sparsification + LoRA down-projection (prologue.cu).
 constexpr int kRankLB = 64;            // LoRA rank handled by the tensor-core paths
-constexpr int kMaxPrologueSplit = 8;   // CTAs (one cluster) per row block
+constexpr int kMaxPrologueSplit = 16;  // CTAs (one cluster) per row block; 16 is a non-portable cluster size
 struct ProArgs {
   CUtensorMap tmX;   // X (M x K bf16), box 64 x 128, 128-byte swizzle
   CUtensorMap tmLB;  // LB (64 x K bf16), box 64 x 64, 128-byte swizzle (LoRA branch only)

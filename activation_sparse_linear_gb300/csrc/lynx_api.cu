@@ -26,6 +26,7 @@ __device__ int g_error_word;
 
 std::atomic<int> g_inject{0};
 std::atomic<int> g_force_tile{0};  // 0: tile shape by problem shape; else a forced shape, rb << 16 | tn
+std::atomic<int> g_force_split{0};  // 0: pre-pass cluster size by occupancy; else a forced size
 thread_local void* const* t_prof_events = nullptr;
 thread_local int t_prof_count = 0;
 
@@ -182,8 +183,9 @@ int make_prologue(ProArgs* pa, const void* X, const void* LB, int64_t M, int64_t
   pa->M = static_cast<int>(M);
   pa->K = static_cast<int>(K);
   pa->M_pad = static_cast<int>(round_up(M, kMetaRowPad));
-  pa->split = prologue_split(pa->M, pa->K);
   pa->nkb = static_cast<int>(meta_blocks_k(K));
+  const int forced = g_force_split.load();
+  pa->split = forced ? (forced < pa->nkb ? forced : pa->nkb) : prologue_split(pa->M, pa->K);
   pa->ctl = make_ctl();
   return LYNX_OK;
 }
@@ -414,6 +416,17 @@ void lynx_profile_next(void* const* events, int count) {
 void lynx_debug_set_fault(int inject, uint64_t wait_ns) {
   g_inject.store(inject);
   g_wait_ns.store(wait_ns ? wait_ns : kDefaultWaitNs);
+}
+
+int lynx_debug_force_split(int split) {
+  if (split < 0 || split > kMaxPrologueSplit) return LYNX_ERR_UNSUPPORTED;
+  g_force_split.store(split);
+  return LYNX_OK;
+}
+
+int lynx_debug_prologue_split(int64_t M, int64_t K) {
+  if (check_mk(M, K) != LYNX_OK) return 0;
+  return prologue_split(static_cast<int>(M), static_cast<int>(K));
 }
 
 int lynx_debug_force_tile(int tile_rows, int tile_cols) {

@@ -310,12 +310,12 @@ __global__ void __launch_bounds__(P_THREADS, 1) prologue_kernel(const __grid_con
   __syncthreads();
   if (a.split > 1) {
     // ---------------------------------------------------------------- cluster reduction of the shares
-    // CTA j of the cluster finishes rows j * 128 / split .. : it adds the split CTAs' shares in rank order
+    // CTA j of the cluster finishes rows [j * 128 / split, (j + 1) * 128 / split): it adds the split CTAs' shares in rank order
     // (deterministic), reading them from the peers' shared memory, and writes s and T'.
     cluster_sync();  // every CTA's shares are in its shared memory
-    const int rows = P_ROWS / a.split, per_row = LORA ? 8 : 1;
+    const int row_lo = sp * P_ROWS / a.split, rows = (sp + 1) * P_ROWS / a.split - row_lo, per_row = LORA ? 8 : 1;
     for (int i = threadIdx.x; i < rows * per_row; i += P_THREADS) {
-      const int rr = sp * rows + i / per_row, g = i % per_row, grow = r0 + rr;
+      const int rr = row_lo + i / per_row, g = i % per_row, grow = r0 + rr;
       float sxs = 0.f, sks = 0.f;
       float acc[8] = {};
       for (int p = 0; p < a.split; ++p) {
@@ -358,20 +358,42 @@ __global__ void __launch_bounds__(P_THREADS, 1) prologue_kernel(const __grid_con
   }
 }
 
+// Kernel attributes, once per device: the dynamic shared memory and, for clusters of 16 CTAs (beyond the
+// portable 8), the non-portable cluster size.
+cudaError_t set_prologue_attrs() {
+  static bool done[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (done[dev]) return cudaSuccess;
+  for (auto* k : {prologue_kernel<true>, prologue_kernel<false>}) {
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  done[dev] = true;
+  return cudaSuccess;
+}
+
 }  // namespace
 
-// CTAs per row block: the largest power of two <= kMaxPrologueSplit (and <= the channel blocks) whose
-// clusters all fit on the GPU at once and whose grid does not exceed the SM count; 1 otherwise.
+// CTAs per row block: among the cluster sizes (2 .. kMaxPrologueSplit, at most one per channel block) whose
+// clusters all fit on the GPU at once and whose grid does not exceed the SM count, the smallest one that gives
+// the fewest channel blocks per CTA; 1 when none fits.  Cluster sizes above 8 are non-portable: the GPU
+// reports how many of them it holds (a 16-CTA cluster needs 16 SMs of one GPC).
 int prologue_split(int M, int K) {
   const int row_blocks = static_cast<int>(round_up(M, kMetaRowPad) / P_ROWS);
   const int nkb = static_cast<int>(meta_blocks_k(K));
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
-  static int fit[64][4] = {};  // resident clusters of 2, 4, 8 CTAs (index log2 size), per device
-  for (int split = kMaxPrologueSplit; split >= 2; split /= 2) {
-    if (split > nkb || row_blocks * split > sm_count()) continue;
-    const int li = split == 2 ? 1 : split == 4 ? 2 : 3;
-    if (!fit[dev][li]) {
+  if (set_prologue_attrs() != cudaSuccess) return 1;
+  static int fit[64][kMaxPrologueSplit + 1] = {};  // resident clusters of each size, per device (-1: none)
+  int best = 1, best_per = nkb;
+  for (int split = 2; split <= kMaxPrologueSplit && split <= nkb; ++split) {
+    if (row_blocks * split > sm_count()) break;
+    if (!fit[dev][split]) {
       cudaLaunchConfig_t cfg = {};
       cudaLaunchAttribute attr[1];
       attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -384,29 +406,24 @@ int prologue_split(int M, int K) {
       cfg.attrs = attr;
       cfg.numAttrs = 1;
       int n = 0;
-      if (cudaFuncSetAttribute(prologue_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM) !=
-              cudaSuccess ||
-          cudaOccupancyMaxActiveClusters(&n, prologue_kernel<true>, &cfg) != cudaSuccess)
+      if (cudaOccupancyMaxActiveClusters(&n, prologue_kernel<true>, &cfg) != cudaSuccess) {
+        cudaGetLastError();  // an unsupported cluster size is an answer, not an error to keep
         n = 0;
-      fit[dev][li] = n > 0 ? n : -1;
+      }
+      fit[dev][split] = n > 0 ? n : -1;
     }
-    if (fit[dev][li] >= row_blocks) return split;
+    const int per = (nkb + split - 1) / split;
+    if (fit[dev][split] >= row_blocks && per < best_per) {
+      best = split;
+      best_per = per;
+    }
   }
-  return 1;
+  return best;
 }
 
 cudaError_t launch_prologue(const ProArgs& args, bool lora, cudaStream_t st) {
   auto* k = lora ? prologue_kernel<true> : prologue_kernel<false>;
-  static bool attr_set[2][64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_set[lora][dev]) {
-    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set[lora][dev] = true;
-  }
+  if (cudaError_t e = set_prologue_attrs()) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;

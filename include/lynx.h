@@ -269,6 +269,16 @@ LYNX_API int lynx_mma_rate(int mode, int iters, double* tflops, double* macs_per
  * restores normal operation; wait_ns = 0 restores the default bound (2 s). */
 LYNX_API void lynx_debug_set_fault(int inject, uint64_t wait_ns);
 
+/* Test hook.  split = 1 .. 16 makes the sparsify pass of every later call run each 128-row block on a
+ * cluster of that many CTAs (at most one per 128-channel block; a size the GPU cannot hold makes the launch
+ * fail with LYNX_ERR_CUDA); 0 restores the automatic choice.  Returns LYNX_OK, or LYNX_ERR_UNSUPPORTED
+ * (setting unchanged) for other values. */
+LYNX_API int lynx_debug_force_split(int split);
+
+/* The cluster size the sparsify pass picks on the current device for an M x K activation (1 = no cluster:
+ * each CTA owns whole rows); 0 for sizes out of range. */
+LYNX_API int lynx_debug_prologue_split(int64_t M, int64_t K);
+
 /* Test hook.  Makes lynx_linear use sparse pair tiles of tile_rows x tile_cols for every shape: 512 x 224,
  * 512 x 192 or 256 x 256 (all must give the same result); 0 x 0 restores the automatic choice by shape.
  * Returns LYNX_OK, or LYNX_ERR_UNSUPPORTED (setting unchanged) for any other shape. */

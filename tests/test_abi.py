@@ -99,6 +99,18 @@ def test_other_entry_points_reject_bad_arguments(asl):
         assert L.lynx_status_string(code)
 
 
+def test_force_split_range(asl):
+    L = asl.lib
+    try:
+        for bad in (-1, 17, 100):
+            assert L.lynx_debug_force_split(bad) == -7
+        for ok in (1, 2, 3, 12, 16):
+            assert L.lynx_debug_force_split(ok) == 0
+    finally:
+        assert L.lynx_debug_force_split(0) == 0
+    assert L.lynx_debug_prologue_split(0, 3072) == 0 and L.lynx_debug_prologue_split(64, 24) == 0  # host checks
+
+
 def test_force_tile_accepts_only_built_shapes(asl):
     L = asl.lib
     try:

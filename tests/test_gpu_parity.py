@@ -127,6 +127,39 @@ def test_linear_full_comparison(lynx, M, N, K, tile):
     assert_y_close(to_bits(Y), O.linear(X, W, LA, LB))
 
 
+@pytest.mark.parametrize("split", [1, 2, 3, 5, 7, 12])
+def test_sparsify_lora_any_cluster_size(lynx, split):
+    """The pre-pass gives the same bits for vals and metadata, and s and T' within tolerance, whatever number
+    of CTAs (cluster size, not only powers of two) shares a row block's channels; Y follows."""
+    M, N, K = 300, 520, 3072
+    X, W, LA, LB = _layer(M, N, K, seed=5)
+    lynx.lynx_debug_force_split(split)
+    try:
+        vals, meta, s, T = lynx.lynx_sparsify_lora(to_dev(X), to_dev(LB))
+        Y = lynx.lynx_linear(to_dev(X), to_dev(W), to_dev(LA), to_dev(LB))
+        assert lynx.lynx_sync_status() == 0
+    finally:
+        lynx.lynx_debug_force_split(0)
+    ref = O.sparsify(X)
+    assert np.array_equal(to_bits(vals), ref["vals"])
+    assert np.array_equal(meta.cpu().numpy(), pack_meta_reference(ref["meta"], M, K))  # every byte
+    np.testing.assert_allclose(s.cpu().numpy(), ref["s"], rtol=S_RTOL, atol=0)
+    assert_y_close(to_bits(T), O.lora_down(X, LB, ref["s"]), "T")
+    assert_y_close(to_bits(Y), O.linear(X, W, LA, LB))
+
+
+def test_prologue_split_choice(lynx):
+    """The automatic cluster size never exceeds the channel blocks or the SM budget and is 1 for large M."""
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for M, K in [(1024, 3072), (1024, 12288), (4608, 3072), (9216, 3072), (16384, 3072), (100, 256)]:
+        sp = lynx.lynx_debug_prologue_split(M, K)
+        rb = -(-M // 256) * 2
+        assert 1 <= sp <= min(16, -(-K // 128)), (M, K, sp)
+        assert sp == 1 or rb * sp <= sms, (M, K, sp)
+    assert lynx.lynx_debug_prologue_split(16384, 3072) == 1
+
+
 @pytest.mark.parametrize("kind", ["mixed", "equal", "two4", "ties", "gelu"])
 def test_linear_structured_inputs(lynx, kind):
     X, W, LA, LB = _layer(160, 384, 256, 11, kind)
