@@ -410,6 +410,46 @@ def main() -> int:
         del cs
     torch.cuda.empty_cache()
 
+    # The sparsify pass alone (lynx_sparsify, and lynx_sparsify_lora with the LoRA down-projection), back to back
+    # on inputs rotated over copies larger than L2: algorithmic bytes per call / time against the HBM peak, at
+    # the QKV input and at the largest activations of the workloads (the CFG batch's MLP-down input and the
+    # stack's largest M).
+    sparsify_alone = {}
+    for Ms, Ks in ((4608, 3072), (9216, 12288), (16384, 3072)):
+        nset = int(400e6 // (Ms * Ks * 2)) + 2
+        xs = [torch.randn((Ms, Ks), generator=gen, device=dev).to(torch.bfloat16) for _ in range(nset)]
+        lb = (0.02 * torch.randn((R, Ks), generator=gen, device=dev)).to(torch.bfloat16)
+        vals = torch.empty((Ms, Ks // 2), dtype=torch.bfloat16, device=dev)
+        meta = torch.empty(asl.lynx_meta_bytes(Ms, Ks), dtype=torch.uint8, device=dev)
+        sv = torch.empty(Ms, dtype=torch.float32, device=dev)
+        tv = torch.empty((Ms, R), dtype=torch.bfloat16, device=dev)
+        res = {"cluster_ctas": asl.lynx_debug_prologue_split(Ms, Ks)}
+        base = Ms * Ks * 2 + Ms * Ks + asl.lynx_meta_bytes(Ms, Ks) + 4 * Ms
+        for key, fn, nbytes in (
+                ("sparsify", lambda x: L.lynx_sparsify(x.data_ptr(), Ms, Ks, vals.data_ptr(), meta.data_ptr(),
+                                                       sv.data_ptr(), sp), base),
+                ("sparsify_lora_down", lambda x: L.lynx_sparsify_lora(x.data_ptr(), lb.data_ptr(), Ms, Ks, R,
+                                                                      vals.data_ptr(), meta.data_ptr(), sv.data_ptr(),
+                                                                      tv.data_ptr(), sp), base + R * Ks * 2 + Ms * R * 2)):
+            for i in range(3):
+                fn(xs[i % nset])
+            torch.cuda.synchronize()
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            nrep = 60
+            a0.record(stream)
+            for i in range(nrep):
+                if fn(xs[i % nset]) != 0:
+                    raise RuntimeError(key + " failed")
+            a1.record(stream)
+            torch.cuda.synchronize()
+            us = a0.elapsed_time(a1) / nrep * 1e3
+            res[key] = {"us": us, "GBs": nbytes / us / 1e3, "frac_hbm": nbytes / us / 1e3 / hbm}
+        sparsify_alone[f"{Ms}x{Ks}"] = res
+        del xs, lb, vals, meta, sv, tv
+    st = asl.lynx_sync_status()
+    assert st == 0, asl.lynx_status_string(st)
+    torch.cuda.empty_cache()
+
     # The block stack: 8 blocks x (QKV sparse 3072->9216, out dense 3072->3072, up dense 3072->12288,
     # down sparse 12288->3072), rank-64 LoRA on the sparse layers, independent seeded weights per block; the
     # total time of the 32 linears at each M against the same 32 layers run dense through cuBLAS.
@@ -573,6 +613,7 @@ def main() -> int:
             "lynx_dense_gemm_ms": lynx_dense_ms, "lynx_dense_gemm_tflops": flops / (lynx_dense_ms * 1e-3) / 1e12,
             "hbm_peak_GBs": hbm, "dense_bf16_peak_tflops": dense_tf,
             "other_shapes": shapes,
+            "sparsify_alone": sparsify_alone,
             "block_stack_32_linears": stack,
             "mma_microbench": {"dense_tflops": mma_dense_tf, "sparse_tflops_effective": mma_sparse_tf,
                                "dense_macs_per_clk": mma_dense_mpc, "sparse_macs_per_clk_effective": mma_sparse_mpc,
