@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(P_THREADS, 1) prologue_kernel(const __grid_con
     // this thread's 16-bit metadata half: groups 4 (qq & 1) .. +3 of a 32-channel word; rows r and r + 8 of a
     // 16-row group share TMEM lanes (low halves in lanes 0-7 of the group, high halves in lanes 8-15)
     const int mlane = (r / 16) * 16 + (qq & 1) * 8 + (r % 8), half_sel = (r % 16) / 8;
-    float sx = 0.f, skept = 0.f;  // running sums of x^2 and kept x^2 (groups added in channel order)
+    float sx = 0.f, skept = 0.f;  // running sums of x^2 and kept x^2 (terms added in channel order)
     bool ok = true;
     // one 128-channel block (two stages) per iteration: eight groups per thread
     for (int kbl = 0; kbl < nstages / 2; ++kbl) {
@@ -212,20 +212,14 @@ __global__ void __launch_bounds__(P_THREADS, 1) prologue_kernel(const __grid_con
       }
       if (!ok) break;
       uint32_t k[8], half[2];
-      float qa[8], qk[8];
 #pragma unroll
-      for (int sub = 0; sub < 2; ++sub) {
+      for (int sub = 0; sub < 2; ++sub) {  // groups in channel order: both sums see their terms in that order
         const uint4 u0 = v[2 * sub], u1 = v[2 * sub + 1];
-        const uint32_t n0 = select_group(u0.x, u0.y, sel_table, k[4 * sub], qa[4 * sub], qk[4 * sub]);
-        const uint32_t n1 = select_group(u0.z, u0.w, sel_table, k[4 * sub + 1], qa[4 * sub + 1], qk[4 * sub + 1]);
-        const uint32_t n2 = select_group(u1.x, u1.y, sel_table, k[4 * sub + 2], qa[4 * sub + 2], qk[4 * sub + 2]);
-        const uint32_t n3 = select_group(u1.z, u1.w, sel_table, k[4 * sub + 3], qa[4 * sub + 3], qk[4 * sub + 3]);
+        const uint32_t n0 = select_group(u0.x, u0.y, sel_table, k[4 * sub], sx, skept);
+        const uint32_t n1 = select_group(u0.z, u0.w, sel_table, k[4 * sub + 1], sx, skept);
+        const uint32_t n2 = select_group(u1.x, u1.y, sel_table, k[4 * sub + 2], sx, skept);
+        const uint32_t n3 = select_group(u1.z, u1.w, sel_table, k[4 * sub + 3], sx, skept);
         half[sub] = n0 | (n1 << 4) | (n2 << 8) | (n3 << 12);
-      }
-#pragma unroll
-      for (int g = 0; g < 8; ++g) {  // the same additions for both sums: equal when nothing nonzero is dropped
-        sx += qa[g];
-        skept += qk[g];
       }
       uint8_t* vb = obuf0 + (kbl % P_NOBUF) * P_OBUF;
       if (kbl >= P_NOBUF) {  // the buffer's previous block has been copied out

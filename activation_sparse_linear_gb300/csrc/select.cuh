@@ -45,17 +45,26 @@ __device__ __forceinline__ uint32_t fma_bf16x2(uint32_t a, uint32_t b, uint32_t 
   return d;
 }
 
+// acc + x * x for a bf16 x (the low 16 bits of `bits`) in one fused multiply-add with fp32 accumulation:
+// the product of two bf16 values is exact in fp32, so this equals fmaf(float(x), float(x), acc).
+__device__ __forceinline__ float fma_sq_bf16(uint32_t bits, float acc) {
+  float d;
+  asm("{ .reg .b16 h; cvt.u16.u32 h, %1; fma.rn.f32.bf16 %0, h, h, %2; }" : "=f"(d) : "r"(bits), "f"(acc));
+  return d;
+}
+
 // Kept pair of one group of four bf16 values (raw bits lo = x1:x0, hi = x3:x2).  The six comparisons run
 // as three packed bf16x2 compares of the sign-cleared values (the bit patterns of |x| order like the
 // magnitudes; +0 and -0 compare equal); a packed multiply-add turns their 1.0 / 0.0 results into the table
 // index (small integers, exact in bf16: lane 0 holds 128 + c02 + 4 c03 + 16 c01, lane 1 holds
 // 2 c13 + 8 c12 + 32 c23, and the bf16 pattern of their sum, 128 + index, carries the index in its low
 // mantissa bits).  `table` is the decision table in shared memory.  Returns the metadata nibble, writes the
-// kept bf16 pair (lower index in the low half) and the group's fp32 sums of x^2 and kept x^2.  Squares of
-// bf16 values are exact in fp32, so when the dropped entries are zero both sums add the same two terms in
-// the same order and are equal bit for bit (s = 1 exactly for an input that is already 2:4).
+// kept bf16 pair (lower index in the low half) and adds the squares to the running fp32 sums: x0^2 .. x3^2
+// to sum_all, the kept pair's (lower index first) to sum_kept, one rounding per term.  A dropped zero adds
+// +0 and leaves a sum unchanged, so when every dropped entry is zero both sums take the same terms in the
+// same order and stay equal bit for bit (s = 1 exactly for an input that is already 2:4).
 __device__ __forceinline__ uint32_t select_group(uint32_t lo, uint32_t hi, const uint32_t* table, uint32_t& kept,
-                                                 float& q_all, float& q_kept) {
+                                                 float& sum_all, float& sum_kept) {
   const uint32_t m01 = lo & 0x7FFF7FFFu, m23 = hi & 0x7FFF7FFFu;
   const uint32_t m32 = __byte_perm(m23, 0u, 0x1032u);  // |x3| : |x2| -> |x2| : |x3|
   const uint32_t m02 = __byte_perm(m01, m23, 0x5410u), m13 = __byte_perm(m01, m23, 0x7632u);
@@ -68,11 +77,11 @@ __device__ __forceinline__ uint32_t select_group(uint32_t lo, uint32_t hi, const
   const uint32_t v = fma_bf16x2(__byte_perm(w, 0u, 0x1032u), 0x3F803F80u, w);  // lane 0: the sum of both lanes
   const uint32_t ent = table[v & 0x3Fu];
   kept = __byte_perm(lo, hi, ent);
-  const float x0 = __uint_as_float(lo << 16), x1 = __uint_as_float(lo & 0xFFFF0000u);
-  const float x2 = __uint_as_float(hi << 16), x3 = __uint_as_float(hi & 0xFFFF0000u);
-  q_all = fmaf(x1, x1, x0 * x0) + fmaf(x3, x3, x2 * x2);
-  const float k0 = __uint_as_float(kept << 16), k1 = __uint_as_float(kept & 0xFFFF0000u);
-  q_kept = fmaf(k1, k1, k0 * k0);
+  float sa = fma_sq_bf16(lo, sum_all);
+  sa = fma_sq_bf16(lo >> 16, sa);
+  sa = fma_sq_bf16(hi, sa);
+  sum_all = fma_sq_bf16(hi >> 16, sa);
+  sum_kept = fma_sq_bf16(kept >> 16, fma_sq_bf16(kept, sum_kept));
   return (ent >> 16) & 0xFu;
 }
 
