@@ -234,7 +234,7 @@ def lynx_mma_rate(mode: int, iters: int = 20000, stream=None) -> tuple[float, fl
     mode 0 dense, 1 2:4 sparse, 2 2:4 sparse with a metadata tcgen05.cp per MMA,
     3 sparse with a commit per two MMAs, 4 sparse with two commits per four MMAs, 5 sparse with
     64-byte-swizzled A; 6-8 on CTA pairs: 6 sparse (A 128-byte swizzle), 7 sparse (A 64-byte swizzle),
-    8 dense."""
+    8 dense; the higher modes (variations of 7) are listed with lynx_mma_rate in include/lynx.h."""
     tf, mpc = ctypes.c_double(), ctypes.c_double()
     _check(lib.lynx_mma_rate(int(mode), iters, ctypes.byref(tf), ctypes.byref(mpc), _stream(stream)), "lynx_mma_rate")
     return tf.value, mpc.value

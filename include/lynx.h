@@ -58,23 +58,24 @@ typedef enum {
 } lynx_status;
 
 /* Bytes of 2:4 metadata for an M x K activation:
- *     ceil(M/128) * (ceil(K/64)*64/32) * 2048.
+ *     (ceil(M/256) * 2) * ceil(K/128) * 2048.
  * Layout (the one the sparse GEMM copies into tensor memory): one 2 KiB chunk
- * per (128-row block, 32-channel chunk), row blocks outermost.  A chunk holds
- * 128 lanes of 16 bytes; only the first little-endian 32-bit word of a lane
- * is metadata (the other 12 bytes are never written).  A row's 32-bit word
- * carries group g (channels 4g..4g+3 of the chunk) in bits 4g..4g+3 as
- * i0 | (i1 << 2), i0 < i1 the kept positions.  Inside each 16-row block the
- * words of rows r and r+8 are stored by 16-bit halves: lane 16b+i (i < 8)
- * holds the low halves of rows 16b+i (bits 0-15) and 16b+8+i (bits 16-31),
- * lane 16b+8+i their high halves -- the order in which tcgen05.mma.sp reads
- * metadata from tensor memory.  Padding rows and channels (up to multiples
- * of 128 and 64) hold the pattern of an all-zero group (0x4). */
+ * per (128-row block, 128-channel block), row blocks outermost.  A chunk holds
+ * 128 lanes of 16 bytes: little-endian 32-bit word w of a lane is the tensor
+ * memory word of that lane for channels 32w..32w+31 of the block.  A row's
+ * word for 32 channels carries group g (channels 4g..4g+3 of them) in bits
+ * 4g..4g+3 as i0 | (i1 << 2), i0 < i1 the kept positions.  Inside each
+ * 16-row block the words of rows r and r+8 are stored by 16-bit halves: lane
+ * 16b+i (i < 8) holds the low halves of rows 16b+i (bits 0-15) and 16b+8+i
+ * (bits 16-31), lane 16b+8+i their high halves -- the order in which
+ * tcgen05.mma.sp reads metadata from tensor memory.  Padding rows and
+ * channels (up to multiples of 256 and 128) hold the pattern of an all-zero
+ * group (0x4). */
 LYNX_API size_t lynx_meta_bytes(int64_t M, int64_t K);
 
-/* Workspace bytes needed by lynx_linear: compressed values, metadata, s,
- * the M x R LoRA intermediate and up to 8 fp32 split-K partials of it, each
- * 256-byte aligned. */
+/* Workspace bytes needed by lynx_linear: compressed values (M x K/2 bf16),
+ * metadata (lynx_meta_bytes), s (M fp32) and the M x R LoRA intermediate T'
+ * (bf16), each 256-byte aligned.  Independent of N. */
 LYNX_API size_t lynx_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t R);
 
 /* Workspace bytes needed by lynx_linear_dense when a LoRA branch is given
