@@ -30,9 +30,12 @@
 // (X LB^T)/s.
 //
 // Roles per CTA: warp 0 lane 0 TMA producer (both CTAs), warp 1 lane 0 MMA
-// issuer (leader only), warps 2-9 epilogue (two warps per TMEM lane quarter:
-// TMEM -> registers -> scale -> bf16 -> global).  Every mbarrier wait is
-// bounded.
+// issuer (leader only; with two row blocks warp 10 lane 0 issues the second
+// block's MMAs), warps 2-9 epilogue (two warps per TMEM lane quarter:
+// TMEM -> registers -> scale -> bf16 -> shared staging -> TMA store).  The
+// operand ring is as deep as shared memory allows: three stages for the
+// 512-row tiles and the dense tile's six, four for the sparse 256 x 256 tile.
+// Every mbarrier wait is bounded.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
