@@ -19,7 +19,7 @@ __all__ = [
     "LynxError", "lib", "LYNX_OK", "LYNX_ERR_TIMEOUT",
     "lynx_meta_bytes", "lynx_workspace_bytes", "lynx_dense_workspace_bytes",
     "lynx_sparsify", "lynx_sparsify_lora", "lynx_lora_down", "lynx_linear",
-    "lynx_linear_dense",
+    "lynx_linear_dense", "lynx_prune_weight", "lynx_linear_wsparse",
     "lynx_sync_status", "lynx_status_string", "lynx_meta_to_canonical", "lynx_debug_set_fault",
     "lynx_debug_force_tile", "lynx_debug_force_split", "lynx_debug_prologue_split",
     "lynx_profile_next", "lynx_linear_kernel_count", "lynx_mma_rate",
@@ -56,6 +56,8 @@ def _load() -> ctypes.CDLL:
         "lynx_linear": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_i64, _c_p, _c_sz, _c_p]),
         "lynx_linear_dense": (ctypes.c_int,
                               [_c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_i64, _c_p, _c_sz, _c_p]),
+        "lynx_linear_wsparse": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_i64,
+                                                _c_p, _c_sz, _c_p]),
         "lynx_sync_status": (ctypes.c_int, [_c_p]),
         "lynx_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "lynx_meta_to_canonical": (ctypes.c_int, [_c_p, _c_p, _c_i64, _c_i64]),
@@ -204,6 +206,29 @@ def lynx_linear_dense(X, W, LA=None, LB=None, Y=None, workspace=None, stream=Non
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib.lynx_linear_dense(_ptr(X), _ptr(W), _ptr(LA), _ptr(LB), _ptr(Y), M, N, K, R, _ptr(workspace), wbytes,
                                  _stream(stream)), "lynx_linear_dense")
+    return Y
+
+
+def lynx_prune_weight(W, stream=None):
+    """W~ of the weight-2:4 comparator, compressed: (values N x K/2 bf16, metadata) via lynx_sparsify."""
+    vals, meta, _ = lynx_sparsify(W, stream=stream)
+    return vals, meta
+
+
+def lynx_linear_wsparse(X, Wvals, Wmeta, LA=None, LB=None, Y=None, workspace=None, stream=None):
+    """Y = bf16(X W~^T [+ (X LB^T) LA^T]): the weight-2:4 comparator on pruned, compressed W (lynx_prune_weight)."""
+    torch = _torch()
+    _need(X, "X", torch.bfloat16)
+    _need(Wvals, "Wvals", torch.bfloat16)
+    M, K = X.shape
+    N = Wvals.shape[0]
+    R = 0 if LB is None else LB.shape[0]
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device) if Y is None else Y
+    if LA is not None and workspace is None:
+        workspace = torch.empty(lynx_dense_workspace_bytes(M, R), dtype=torch.uint8, device=X.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.lynx_linear_wsparse(_ptr(X), _ptr(Wvals), _ptr(Wmeta), _ptr(LA), _ptr(LB), _ptr(Y), M, N, K, R,
+                                   _ptr(workspace), wbytes, _stream(stream)), "lynx_linear_wsparse")
     return Y
 
 

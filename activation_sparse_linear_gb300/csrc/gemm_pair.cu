@@ -105,7 +105,22 @@ __device__ __forceinline__ void store_chunk(__nv_bfloat16* yrow, int col0, int N
   }
 }
 
-template <bool SPARSE, bool LORA, int MB, int TN>
+// Transposed output: this lane's accumulator row is output column `zrow`; its 32 bf16 values (16 packed pairs)
+// belong to output rows zcol0 .. zcol0 + 31 (clipped to nz, the output's row count).
+__device__ __forceinline__ void store_chunk_t(void* Y, int64_t ldy, int zrow, int zcol0, int nz, const uint32_t* p) {
+  uint16_t* y = static_cast<uint16_t*>(Y) + zrow;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    if (zcol0 + j < nz) {
+      const uint32_t w = p[j / 2];
+      y[static_cast<int64_t>(zcol0 + j) * ldy] = (j & 1) ? static_cast<uint16_t>(w >> 16) : static_cast<uint16_t>(w & 0xFFFFu);
+    }
+  }
+}
+
+// TRANS: the accumulator tile is the transpose of the output (the weight-sparse variant multiplies the pruned
+// W, as the sparse operand, by X); the epilogue writes it transposed.
+template <bool SPARSE, bool LORA, int MB, int TN, bool TRANS>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ PairArgs a) {
   using C = PairCfg<SPARSE, MB, TN>;
@@ -362,7 +377,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       // written out, so the accumulators are released after ceil(NC / 2) TMEM round trips.  At most HOLD
       // chunks stay in registers (the register file holds no more without spilling); the first NC - HOLD
       // chunks are written out as soon as they are converted.
-      constexpr int HOLD = 6;
+      constexpr int HOLD = TRANS ? 5 : 6;  // the transposed write-out needs a few more registers
       constexpr int EARLY = NC > HOLD ? NC - HOLD : 0;
       static_assert(EARLY == 0 || (EARLY <= 2 && C::Y_BOXES == 2), "early chunks use the warp's two staging boxes");
       uint32_t pk[NC * 16];
@@ -376,18 +391,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             else bulk_wait_read_all();
           }
           __syncwarp();
+          if constexpr (TRANS) {
+            // box row i = output row col0 + i (accumulator column); element `lane` of it = output column
+            // row0 + lane: byte 2 lane of the 64-byte row, whose 16-byte piece lane / 8 is swizzled by row
+            const int piece = lane >> 3, off = (lane & 7) * 2;
 #pragma unroll
-          for (int v = 0; v < 4; ++v)  // 16-byte piece v of this lane's 64-byte row, 64-byte swizzle
-            *reinterpret_cast<uint4*>(box + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4)) =
-                make_uint4(p[4 * v], p[4 * v + 1], p[4 * v + 2], p[4 * v + 3]);
+            for (int j = 0; j < 16; ++j) {
+              const int i0 = 2 * j, i1 = 2 * j + 1;
+              *reinterpret_cast<uint16_t*>(box + i0 * 64 + ((piece ^ ((i0 >> 1) & 3)) << 4) + off) =
+                  static_cast<uint16_t>(p[j] & 0xFFFFu);
+              *reinterpret_cast<uint16_t*>(box + i1 * 64 + ((piece ^ ((i1 >> 1) & 3)) << 4) + off) =
+                  static_cast<uint16_t>(p[j] >> 16);
+            }
+          } else {
+#pragma unroll
+            for (int v = 0; v < 4; ++v)  // 16-byte piece v of this lane's 64-byte row, 64-byte swizzle
+              *reinterpret_cast<uint4*>(box + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4)) =
+                  make_uint4(p[4 * v], p[4 * v + 1], p[4 * v + 2], p[4 * v + 3]);
+          }
           fence_proxy_async();
           __syncwarp();
           if (lane == 0) {
-            if (col0 < a.N && row0 < a.M) tma_store_2d(&a.tmY, box, col0, row0);
+            if (col0 < a.N && row0 < a.M) {
+              if constexpr (TRANS) tma_store_2d(&a.tmY, box, row0, col0);
+              else tma_store_2d(&a.tmY, box, col0, row0);
+            }
             bulk_commit();
           }
         } else if (live) {
-          store_chunk(yrow, col0, a.N, vec_ok, p);
+          if constexpr (TRANS) store_chunk_t(a.Y, a.ldy, row, col0, a.N, p);
+          else store_chunk(yrow, col0, a.N, vec_ok, p);
         }
       };
 #pragma unroll
@@ -444,10 +477,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   }
 }
 
-template <bool SPARSE, bool LORA, int MB, int TN>
+template <bool SPARSE, bool LORA, int MB, int TN, bool TRANS = false>
 cudaError_t launch(const PairArgs& a, cudaStream_t st) {
   using C = PairCfg<SPARSE, MB, TN>;
-  auto* k = gemm_pair_kernel<SPARSE, LORA, MB, TN>;
+  auto* k = gemm_pair_kernel<SPARSE, LORA, MB, TN, TRANS>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -517,6 +550,15 @@ cudaError_t launch_gemm_pair(bool sparse, bool lora, PairShape shape, const Pair
   if (shape.rb == 2)
     return lora ? launch<true, true, 2, 192>(a, st) : launch<true, false, 2, 192>(a, st);
   return lora ? launch<true, true, 1, 256>(a, st) : launch<true, false, 1, 256>(a, st);
+}
+
+cudaError_t launch_gemm_pair_transposed(bool lora, PairShape shape, const PairArgs& a, cudaStream_t st) {
+  if (!pair_shape_valid(true, shape)) return cudaErrorInvalidValue;
+  if (shape.rb == 2 && shape.tn == 224)
+    return lora ? launch<true, true, 2, 224, true>(a, st) : launch<true, false, 2, 224, true>(a, st);
+  if (shape.rb == 2)
+    return lora ? launch<true, true, 2, 192, true>(a, st) : launch<true, false, 2, 192, true>(a, st);
+  return lora ? launch<true, true, 1, 256, true>(a, st) : launch<true, false, 1, 256, true>(a, st);
 }
 
 }  // namespace lynx

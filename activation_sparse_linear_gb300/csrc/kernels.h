@@ -104,6 +104,9 @@ struct PairArgs {
 
 // The CTA-pair (cta_group::2) GEMM with the given tile shape (one of those pair_shape returns).
 cudaError_t launch_gemm_pair(bool sparse, bool lora, PairShape shape, const PairArgs& a, cudaStream_t st);
+// The sparse pair GEMM whose accumulator tile is the transpose of Y: a.M and a.N count the accumulator's rows
+// and columns (Y's columns and rows), tmY and ldy describe Y itself (rows of ldy elements).
+cudaError_t launch_gemm_pair_transposed(bool lora, PairShape shape, const PairArgs& a, cudaStream_t st);
 
 int sm_count();
 

@@ -352,6 +352,59 @@ int lynx_linear_dense(const void* X, const void* W, const void* LA, const void* 
   return cuda_status(prof.mark(1, st));
 }
 
+int lynx_linear_wsparse(const void* X, const void* Wvals, const void* Wmeta, const void* LA, const void* LB, void* Y,
+                        int64_t M, int64_t N, int64_t K, int64_t R, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+  if (!X || !Wvals || !Wmeta || !Y) return LYNX_ERR_NULL;
+  const bool lora = LA || LB;
+  if (lora && (!LA || !LB || !workspace)) return LYNX_ERR_NULL;
+  if (int e = check_mk(M, K)) return e;
+  if (int e = check_n(M, N)) return e;
+  if (N > kMaxM) return LYNX_ERR_SHAPE;  // W's rows are the GEMM's row blocks
+  if (lora && R != kRank) return R < 1 ? LYNX_ERR_SHAPE : LYNX_ERR_UNSUPPORTED;
+  if (misaligned(X) || misaligned(Wvals) || misaligned(Wmeta) || misaligned(Y) ||
+      (lora && (misaligned(LA) || misaligned(LB) || misaligned(workspace))))
+    return LYNX_ERR_ALIGN;
+  if (lora && workspace_bytes < lynx_dense_workspace_bytes(M, R)) return LYNX_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  // The sparse operand is W~ (N rows), the dense one X (M rows): the accumulator tile is Y^T.  The LoRA stage
+  // swaps likewise: LA (N x 64) on the sparse operand's side, T = X LB^T (M x 64) on the other.
+  PairArgs g;
+  std::memset(&g, 0, sizeof(g));
+  const int forced = g_force_tile.load();
+  const PairShape shape = forced ? PairShape{forced >> 16, forced & 0xFFFF}
+                                 : pair_shape(true, static_cast<int>(N), static_cast<int>(M));
+  const uint64_t meta_rows = 2 * static_cast<uint64_t>(meta_bytes(N, K) / kMetaChunkBytes);
+  if (!make_map(&g.tmA, Wvals, K / 2, N, K / 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&g.tmB, X, K, M, K, 64, shape.tn / 2, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&g.tmMeta, Wmeta, 256, meta_rows, 256, 256, 2, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_DATA_TYPE_UINT32))
+    return LYNX_ERR_CUDA;
+  if (lora && (!make_map(&g.tmT, LA, R, N, R, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+               !make_map(&g.tmLA, workspace, R, M, R, 64, shape.tn / 2, CU_TENSOR_MAP_SWIZZLE_128B)))
+    return LYNX_ERR_CUDA;
+  if (!set_y_map(&g, Y, M, N)) return LYNX_ERR_CUDA;
+  g.rowscale = nullptr;
+  g.scale_mode = SCALE_NONE;
+  g.Y = Y;
+  g.ldy = N;
+  g.M = static_cast<int>(N);
+  g.N = static_cast<int>(M);
+  g.K = static_cast<int>(K);
+  g.ctl = make_ctl();
+  StageEvents prof(lora ? 3 : 2);
+  if (cudaError_t e = prof.mark(0, st)) return cuda_status(e);
+  if (lora) {
+    if (int e = run_lora_down(X, LB, nullptr, workspace, M, K, st)) return e;
+    if (cudaError_t e = prof.mark(1, st)) return cuda_status(e);
+    if (cudaError_t e = launch_gemm_pair_transposed(true, shape, g, st)) return cuda_status(e);
+    return cuda_status(prof.mark(2, st));
+  }
+  if (cudaError_t e = launch_gemm_pair_transposed(false, shape, g, st)) return cuda_status(e);
+  return cuda_status(prof.mark(1, st));
+}
+
 int lynx_sync_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return LYNX_ERR_CUDA;

@@ -366,6 +366,31 @@ def main() -> int:
     torch.cuda.synchronize()
     lynx_dense_ms = l0.elapsed_time(l1) / nd
 
+    # The weight-2:4 comparator at the same shape (W pruned and compressed once, outside the timed region):
+    # the same sparse tensor-core path with W~ as the sparse operand, with the same rank-64 LoRA branch.
+    wpruned = [asl.lynx_prune_weight(sets[i]["W"]) for i in range(ROTATE)]
+    ws_w = torch.empty(asl.lynx_dense_workspace_bytes(M, R), dtype=torch.uint8, device=dev)
+
+    def wsparse(i):
+        s = sets[i % ROTATE]
+        wv, wm = wpruned[i % ROTATE]
+        return L.lynx_linear_wsparse(s["X"].data_ptr(), wv.data_ptr(), wm.data_ptr(), s["LA"].data_ptr(),
+                                     s["LB"].data_ptr(), s["Y"].data_ptr(), M, N, K, R, ws_w.data_ptr(),
+                                     ws_w.numel(), sp)
+    for i in range(args.warmup):
+        wsparse(i)
+    torch.cuda.synchronize()
+    l0.record(stream)
+    for i in range(nd):
+        if wsparse(i) != 0:
+            raise RuntimeError("lynx_linear_wsparse failed")
+    l1.record(stream)
+    torch.cuda.synchronize()
+    wsparse_ms = l0.elapsed_time(l1) / nd
+    st = asl.lynx_sync_status()
+    assert st == 0, asl.lynx_status_string(st)
+    del wpruned, ws_w
+
     # The other layer shapes of the DiT workloads (MLP up/down, the CFG batch, the largest stack M): step time
     # of lynx_linear and of the dense cuBLAS GEMM at the same shape, two rotating device copies each.  Inputs
     # are seeded normal draws generated on the device (timing only; the parity tests cover these shapes).
@@ -612,6 +637,9 @@ def main() -> int:
             "x_vs_dense_cublas": dense_ms / ms_per_step,
             "lynx_dense_gemm_ms": lynx_dense_ms, "lynx_dense_gemm_tflops": flops / (lynx_dense_ms * 1e-3) / 1e12,
             "hbm_peak_GBs": hbm, "dense_bf16_peak_tflops": dense_tf,
+            "weight_2to4_comparator": {"ms": wsparse_ms, "tflops": flops / (wsparse_ms * 1e-3) / 1e12,
+                                       "x_vs_dense_cublas": dense_ms / wsparse_ms,
+                                       "note": "Y = X W~^T + X (LA LB)^T, W~ = 2:4-pruned W as the sparse operand"},
             "other_shapes": shapes,
             "sparsify_alone": sparsify_alone,
             "block_stack_32_linears": stack,

@@ -217,6 +217,22 @@ LYNX_API int lynx_graph_launch(lynx_graph graph, void* stream);
  * have completed (e.g. after lynx_sync_status on their stream). */
 LYNX_API int lynx_graph_destroy(lynx_graph graph);
 
+/* The weight-2:4 comparator: Y = bf16( X W~^T [+ (X LB^T) LA^T] ), W~ keeping
+ * the two largest |w| of every 4 consecutive input channels of each row of W
+ * (ties to the lower index), with no rescaling.  (RT-Lynx page, Main results:
+ * the "Sparse Weight" baseline; Key idea: weight against activation
+ * sparsity.  Provided as a speed comparator of the same tensor-core path.)
+ *   X [in] M x K bf16; Y [out] M x N bf16.
+ *   Wvals, Wmeta [in]: W~ compressed as lynx_sparsify(W, N, K, ...) writes it
+ *     (its s output is not used); prune once, reuse for every call.
+ *   LA, LB: both NULL (no LoRA) or both given (R = 64; the workspace then holds
+ *     lynx_dense_workspace_bytes(M, R) bytes).
+ * Enqueues the LoRA down-projection (with LoRA) and one 2:4-sparse GEMM whose
+ * sparse operand is W~: its accumulator tile is Y^T, written out transposed. */
+LYNX_API int lynx_linear_wsparse(const void* X, const void* Wvals, const void* Wmeta, const void* LA, const void* LB,
+                                 void* Y, int64_t M, int64_t N, int64_t K, int64_t R, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
 /* Waits for `stream`, then reads and clears the device error word of the
  * current device.  Returns LYNX_OK, LYNX_ERR_TIMEOUT or LYNX_ERR_CUDA. */
 LYNX_API int lynx_sync_status(void* stream);
@@ -280,7 +296,8 @@ LYNX_API int lynx_debug_force_split(int split);
  * each CTA owns whole rows); 0 for sizes out of range. */
 LYNX_API int lynx_debug_prologue_split(int64_t M, int64_t K);
 
-/* Test hook.  Makes lynx_linear use sparse pair tiles of tile_rows x tile_cols for every shape: 512 x 224,
+/* Test hook.  Makes lynx_linear (and lynx_linear_wsparse, whose tile rows are output columns) use sparse
+ * pair tiles of tile_rows x tile_cols for every shape: 512 x 224,
  * 512 x 192 or 256 x 256 (all must give the same result); 0 x 0 restores the automatic choice by shape.
  * Returns LYNX_OK, or LYNX_ERR_UNSUPPORTED (setting unchanged) for any other shape. */
 LYNX_API int lynx_debug_force_tile(int tile_rows, int tile_cols);

@@ -36,7 +36,7 @@ import numpy as np
 
 __all__ = [
     "widen", "select_2of4", "keep_mask", "norm_scale", "sparsify", "canonical_meta",
-    "linear", "linear_dense", "lora_down", "NIBBLE_OF_PAIR",
+    "linear", "linear_dense", "linear_wsparse", "lora_down", "NIBBLE_OF_PAIR",
 ]
 
 #: 4-bit metadata of a kept index pair (i0 < i1): i0 in bits 0-1, i1 in bits 2-3.
@@ -161,6 +161,27 @@ def linear_dense(X, W, LA=None, LB=None, rows=None) -> np.ndarray:
         Xb = Xb[np.asarray(rows)]
     x = widen(Xb)
     y = x @ widen(W).T
+    if LA is not None and LB is not None:
+        y = y + (x @ widen(LB).T) @ widen(LA).T
+    return y
+
+
+def linear_wsparse(X, W, LA=None, LB=None, rows=None) -> np.ndarray:
+    """Y = X W~^T (+ X (LA LB)^T when LoRA factors are given): the weight-2:4 comparator.
+
+    The RT-Lynx page compares its activation sparsity with 2:4 weight sparsity ("Sparse Weight" in Main
+    results; Key idea: weight sparsity degrades DiT outputs more than activation sparsity).  Reading: W~ keeps
+    the two largest |w| of every 4 consecutive input channels of each output row, ties to the lower index
+    (the activation rule applied to the rows of W, along K as the sparse tensor core requires), with no norm
+    compensation; the optional LoRA branch is the dense layer's.
+    """
+    Xb = np.asarray(X, dtype=np.uint16)
+    if rows is not None:
+        Xb = Xb[np.asarray(rows)]
+    x = widen(Xb)
+    w = widen(W)
+    wt = np.where(keep_mask(w), w, 0.0)
+    y = x @ wt.T
     if LA is not None and LB is not None:
         y = y + (x @ widen(LB).T) @ widen(LA).T
     return y

@@ -95,6 +95,12 @@ def test_other_entry_points_reject_bad_arguments(asl):
     assert L.lynx_linear_dense(A, A, A, A, A, 4, 16, 16, 64, A, 10, None) == -4
     assert L.lynx_linear_dense(A, A, None, None, A, 4, 16, 17, 64, None, 0, None) == -2
     assert L.lynx_linear_dense(A, A, None, None, A, 1 << 22, 1 << 19, 16, 64, None, 0, None) == -2   # M N > 2^40
+    assert L.lynx_linear_wsparse(A, None, A, None, None, A, 4, 16, 16, 64, None, 0, None) == -1       # no W values
+    assert L.lynx_linear_wsparse(A, A, A, A, None, A, 4, 16, 16, 64, A, 1 << 20, None) == -1          # one LoRA factor
+    assert L.lynx_linear_wsparse(A, A, A, None, None, A, 4, 16, 24, 64, None, 0, None) == -2          # K % 16
+    assert L.lynx_linear_wsparse(A, A + 8, A, None, None, A, 4, 16, 16, 64, None, 0, None) == -3      # misaligned
+    assert L.lynx_linear_wsparse(A, A, A, A, A, A, 4, 16, 16, 64, A, 10, None) == -4                  # workspace
+    assert L.lynx_linear_wsparse(A, A, A, A, A, A, 4, 16, 16, 32, A, 1 << 20, None) == -7             # rank
     for code in range(-7, 1):
         assert L.lynx_status_string(code)
 

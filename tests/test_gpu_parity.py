@@ -237,3 +237,40 @@ def test_mma_rate_microbenchmark_runs(lynx):
     for mode in (0, 1, 2):
         tf, mpc = lynx.lynx_mma_rate(mode, 2000)
         assert tf > 100 and mpc > 0
+
+
+# ------------------------------------------------------------------ the weight-2:4 comparator
+WSPARSE_CASES = [(256, 512, 512), (300, 520, 528), (1, 8, 16), (200, 1003, 256), (600, 1160, 384), (129, 136, 3072)]
+
+
+@pytest.mark.parametrize("tile", [(512, 224), (512, 192), (256, 256)])
+@pytest.mark.parametrize("M,N,K", WSPARSE_CASES)
+def test_weight_sparse_linear(lynx, M, N, K, tile):
+    """Y = X W~^T + X (LA LB)^T with W pruned and compressed by the sparsify pass: the GEMM runs W~ as the
+    sparse operand and writes its transposed tile (N % 8 != 0 takes the per-lane stores)."""
+    X, W, LA, LB = _layer(M, N, K, seed=9)
+    Wv, Wm = lynx.lynx_prune_weight(to_dev(W))
+    lynx.lynx_debug_force_tile(*tile)
+    try:
+        Y = lynx.lynx_linear_wsparse(to_dev(X), Wv, Wm, to_dev(LA), to_dev(LB))
+        Y0 = lynx.lynx_linear_wsparse(to_dev(X), Wv, Wm)
+        assert lynx.lynx_sync_status() == 0
+    finally:
+        lynx.lynx_debug_force_tile(0, 0)
+    assert_y_close(to_bits(Y), O.linear_wsparse(X, W, LA, LB))
+    assert_y_close(to_bits(Y0), O.linear_wsparse(X, W), "Y without LoRA")
+
+
+def test_weight_sparse_on_24_weights_matches_dense_layer(lynx):
+    """Weights that are already 2:4 lose nothing: the result equals the dense layer's."""
+    import torch
+    M, N, K = 300, 264, 512
+    X = _x("act", M, K, 4)
+    W = synth.structured_x("two4", N, K, seed=4)
+    Wv, Wm = lynx.lynx_prune_weight(to_dev(W))
+    Y = lynx.lynx_linear_wsparse(to_dev(X), Wv, Wm)
+    Yd = lynx.lynx_linear_dense(to_dev(X), to_dev(W))
+    assert lynx.lynx_sync_status() == 0
+    assert_y_close(to_bits(Y), O.linear_dense(X, W))
+    assert float((Y.float() - Yd.float()).abs().max()) <= float(Yd.float().abs().max()) * 2 ** -7
+    torch.cuda.synchronize()

@@ -225,6 +225,51 @@ def test_dense_layer_with_lora_against_loops():
     assert np.allclose(O.linear_dense(X, W, LA, LB), want, rtol=1e-13, atol=1e-13)
 
 
+def pin_wsparse_loops(seed, M=3, N=4, K=12, R=2):
+    """The weight-2:4 layer with Python loops: brute-force pair per group of each W row, no rescale."""
+    g = np.random.default_rng(100 + seed)
+    X, W, LA, LB = (bits(g.standard_normal(sh)) for sh in [(M, K), (N, K), (N, R), (R, K)])
+    x, w, la, lb = (O.widen(a).tolist() for a in (X, W, LA, LB))
+    wk = []
+    for n in range(N):
+        kept = [0.0] * K
+        for gi in range(K // 4):
+            i, j = brute_pair(w[n][4 * gi:4 * gi + 4])
+            kept[4 * gi + i] = w[n][4 * gi + i]
+            kept[4 * gi + j] = w[n][4 * gi + j]
+        wk.append(kept)
+    want = [[sum(x[m][k] * wk[n][k] for k in range(K)) +
+             sum(sum(x[m][k] * lb[r][k] for k in range(K)) * la[n][r] for r in range(R))
+             for n in range(N)] for m in range(M)]
+    assert np.allclose(O.linear_wsparse(X, W, LA, LB), want, rtol=1e-13, atol=1e-13)
+    want_plain = [[sum(x[m][k] * wk[n][k] for k in range(K)) for n in range(N)] for m in range(M)]
+    assert np.allclose(O.linear_wsparse(X, W), want_plain, rtol=1e-13, atol=1e-13)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_weight_sparse_layer_against_python_loops(seed):
+    pin_wsparse_loops(seed)
+
+
+def test_weight_sparse_on_24_weights_is_the_dense_layer():
+    """W that is already 2:4 (two zeros per group) is left unchanged: the dense layer's result."""
+    W = synth.structured_x("two4", 24, 64, seed=3)
+    X = synth.act_bf16((8, 1), 10, 64, 0.05, 8.0)
+    LA, LB = synth.gaussian_bf16((8, 2), (24, 2), 0.1), synth.gaussian_bf16((8, 3), (2, 64), 0.1)
+    assert np.array_equal(O.linear_wsparse(X, W, LA, LB), O.linear_dense(X, W, LA, LB))
+
+
+def test_weight_sparse_is_the_transposed_activation_product():
+    """X W~^T = (W~ X^T)^T, and W~ X^T is the activation path on W without its row scale: the same
+    selection reached through the sparsified-activation functions."""
+    X = synth.act_bf16((9, 1), 7, 32, 0.05, 8.0)
+    W = synth.act_bf16((9, 2), 5, 32, 0.05, 8.0)
+    zero_la, zero_lb = np.zeros((7, 2), np.uint16), np.zeros((2, 32), np.uint16)
+    s_w = O.sparsify(W)["s"]
+    via_activation = O.linear(W, X, zero_la, zero_lb) / s_w[:, None]
+    assert np.allclose(O.linear_wsparse(X, W), via_activation.T, rtol=1e-12, atol=1e-12)
+
+
 def test_lora_down_hand_case_and_recombination():
     case = GOLD["linear"][0]
     X, LB, LA, W = (bits(case[k]) for k in ("X", "LB", "LA", "W"))
@@ -295,6 +340,10 @@ def _unscaled_sparse(X, W, LA, LB, rows=None):
     return np.where(mask, x, 0.0) @ O.widen(W).T + (x @ O.widen(LB).T) @ O.widen(LA).T
 
 
+def _wsparse_keeps_all(X, W, LA=None, LB=None, rows=None):
+    return O.linear_dense(X, W, LA, LB, rows=rows)
+
+
 _REAL = {"norm_scale": O.norm_scale, "linear": O.linear}
 
 
@@ -305,6 +354,8 @@ _REAL = {"norm_scale": O.norm_scale, "linear": O.linear}
     ("linear", _no_lora, ["hand_linear", "loops"]),
     ("linear", _reversed_lora_rows, ["loops"]),
     ("linear", _unscaled_sparse, ["hand_linear", "loops"]),
+    ("select_2of4", _smallest_two, ["wsparse_loops"]),
+    ("linear_wsparse", _wsparse_keeps_all, ["wsparse_loops"]),
 ])
 def test_planted_mistake_is_caught(monkeypatch, attr, fake, pins):
     monkeypatch.setattr(O, attr, fake)
@@ -314,6 +365,7 @@ def test_planted_mistake_is_caught(monkeypatch, attr, fake, pins):
         "hand_linear": pin_hand_linear,
         "norm": lambda: pin_norm_restoration(synth.act_bf16((5, 6), 16, 64, 0.03, 10.0)),
         "loops": lambda: pin_loops(0),
+        "wsparse_loops": lambda: pin_wsparse_loops(0),
     }
     for p in pins:
         with pytest.raises(AssertionError):
