@@ -13,6 +13,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "kernels.h"
 
 namespace lynx {
@@ -236,15 +238,15 @@ __global__ void __launch_bounds__(192, 1) gemm_kernel(const __grid_constant__ Ge
 }  // namespace
 
 int sm_count() {
-  static int counts[64] = {};
+  static std::atomic<int> counts[64] = {};  // per device; racing first calls store the same value
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
-  if (!counts[dev]) {
-    int n = 0;
+  int n = counts[dev].load(std::memory_order_relaxed);
+  if (!n) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
-    counts[dev] = n;
+    counts[dev].store(n, std::memory_order_relaxed);
   }
-  return counts[dev];
+  return n;
 }
 
 namespace {
@@ -253,7 +255,7 @@ template <int BN>
 cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
   using C = Cfg<BN>;
   auto* k = gemm_kernel<BN>;
-  static bool attr_set[64] = {};  // per device; setting it twice from racing threads is harmless
+  static std::atomic<bool> attr_set[64] = {};  // per device; setting it twice from racing threads is harmless
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;

@@ -39,6 +39,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "kernels.h"
 
 namespace lynx {
@@ -481,7 +483,7 @@ template <bool SPARSE, bool LORA, int MB, int TN, bool TRANS = false>
 cudaError_t launch(const PairArgs& a, cudaStream_t st) {
   using C = PairCfg<SPARSE, MB, TN>;
   auto* k = gemm_pair_kernel<SPARSE, LORA, MB, TN, TRANS>;
-  static bool attr_set[64] = {};
+  static std::atomic<bool> attr_set[64] = {};  // per device; setting it twice from racing threads is harmless
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;

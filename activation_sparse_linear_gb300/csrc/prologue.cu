@@ -26,6 +26,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "kernels.h"
 #include "select.cuh"
 
@@ -355,7 +357,7 @@ __global__ void __launch_bounds__(P_THREADS, 1) prologue_kernel(const __grid_con
 // Kernel attributes, once per device: the dynamic shared memory and, for clusters of 16 CTAs (beyond the
 // portable 8), the non-portable cluster size.
 cudaError_t set_prologue_attrs() {
-  static bool done[64] = {};
+  static std::atomic<bool> done[64] = {};  // setting the attributes twice from racing threads is harmless
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -383,7 +385,7 @@ int prologue_split(int M, int K) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
   if (set_prologue_attrs() != cudaSuccess) return 1;
-  static int fit[64][kMaxPrologueSplit + 1] = {};  // resident clusters of each size, per device (-1: none)
+  static std::atomic<int> fit[64][kMaxPrologueSplit + 1] = {};  // resident clusters per size and device (-1: none)
   int best = 1, best_per = nkb;
   for (int split = 2; split <= kMaxPrologueSplit && split <= nkb; ++split) {
     if (row_blocks * split > sm_count()) break;
