@@ -369,3 +369,12 @@ class LynxGraph:
         if self._handle:
             _check(lib.lynx_graph_destroy(self._handle), "lynx_graph_destroy")
             self._handle = _c_p()
+
+    def __enter__(self) -> "LynxGraph":
+        return self
+
+    def __exit__(self, *exc) -> None:
+        """Waits for the current stream (the replays' usual stream), then frees the graph."""
+        if self._handle:
+            lynx_sync_status()
+            self.close()
