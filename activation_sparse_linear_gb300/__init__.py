@@ -374,7 +374,8 @@ class LynxGraph:
         return self
 
     def __exit__(self, *exc) -> None:
-        """Waits for the current stream (the replays' usual stream), then frees the graph."""
+        """Waits for the current stream (the replays' usual stream), then frees the graph.  The device error
+        word is left for the caller's lynx_sync_status."""
         if self._handle:
-            lynx_sync_status()
+            _torch().cuda.current_stream().synchronize()
             self.close()
