@@ -259,7 +259,7 @@ def lynx_mma_rate(mode: int, iters: int = 20000, stream=None) -> tuple[float, fl
     mode 0 dense, 1 2:4 sparse, 2 2:4 sparse with a metadata tcgen05.cp per MMA,
     3 sparse with a commit per two MMAs, 4 sparse with two commits per four MMAs, 5 sparse with
     64-byte-swizzled A; 6-8 on CTA pairs: 6 sparse (A 128-byte swizzle), 7 sparse (A 64-byte swizzle),
-    8 dense; the higher modes (variations of 7) are listed with lynx_mma_rate in include/lynx.h."""
+    8 dense."""
     tf, mpc = ctypes.c_double(), ctypes.c_double()
     _check(lib.lynx_mma_rate(int(mode), iters, ctypes.byref(tf), ctypes.byref(mpc), _stream(stream)), "lynx_mma_rate")
     return tf.value, mpc.value
@@ -353,6 +353,7 @@ class LynxGraph:
             workspace = torch.empty(max(lynx_layers_workspace_bytes(self.layers), 1), dtype=torch.uint8,
                                     device=self.layers[0]["X"].device)
         self.workspace = workspace
+        self._streams = {}  # every stream a replay was enqueued on (by handle), for __exit__
         handle, failed = _c_p(), ctypes.c_int32(-1)
         _layer_error(lib.lynx_graph_create(_c_layer_array(self.layers), len(self.layers), _ptr(workspace),
                                            workspace.numel() * workspace.element_size(), ctypes.byref(handle),
@@ -362,7 +363,10 @@ class LynxGraph:
     def launch(self, stream=None) -> None:
         if not self._handle:
             raise LynxError(-1, "LynxGraph.launch after close")
-        _check(lib.lynx_graph_launch(self._handle, _stream(stream)), "lynx_graph_launch")
+        torch = _torch()
+        s = torch.cuda.current_stream() if stream is None else stream
+        self._streams[s.cuda_stream] = s
+        _check(lib.lynx_graph_launch(self._handle, s.cuda_stream), "lynx_graph_launch")
 
     def close(self) -> None:
         """Frees the graph; call after the replays have completed."""
@@ -373,9 +377,22 @@ class LynxGraph:
     def __enter__(self) -> "LynxGraph":
         return self
 
-    def __exit__(self, *exc) -> None:
-        """Waits for the current stream (the replays' usual stream), then frees the graph.  The device error
-        word is left for the caller's lynx_sync_status."""
-        if self._handle:
-            _torch().cuda.current_stream().synchronize()
-            self.close()
+    def __exit__(self, exc_type, exc, tb) -> None:
+        """Waits for every stream a replay was launched on, then frees the graph (always, even when a wait
+        fails).  A failure here is raised only when no exception is already leaving the with-block.  The
+        device error word is left for the caller's lynx_sync_status."""
+        if not self._handle:
+            return
+        try:
+            for s in self._streams.values():
+                s.synchronize()
+        except Exception:
+            if exc_type is None:
+                raise
+        finally:
+            self._streams.clear()
+            try:
+                self.close()
+            except Exception:
+                if exc_type is None:
+                    raise

@@ -525,6 +525,11 @@ void* noalloc_scratch() {
 
 extern "C" int lynx_linear_noalloc(const void* X, const void* W, const void* LA, const void* LB, void* Y, int64_t M,
                                    int64_t N, int64_t K, int64_t R, void* stream) {
+  // The arguments are checked as lynx_linear checks them (with a stand-in workspace that passes every workspace
+  // check, never dereferenced), so that a bad pointer or shape reports its own status; only a valid problem is
+  // then measured against the fixed array.
+  static const uint8_t stand_in[16] __attribute__((aligned(16))) = {};
+  if (int e = lynx::linear_arg_status(X, W, LA, LB, Y, M, N, K, R, stand_in, SIZE_MAX)) return e;
   if (lynx_workspace_bytes(M, N, K, R) > LYNX_NOALLOC_SCRATCH_BYTES) return LYNX_ERR_TOO_LARGE;
   void* ws = lynx::noalloc_scratch();
   if (!ws) return LYNX_ERR_CUDA;

@@ -94,13 +94,7 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int mode, int iters, D
   }
 }
 
-// CTA-pair variant: modes 6 (sparse, A 128-byte swizzle), 7 (sparse, A 64-byte swizzle), 8 (dense),
-// 9 (as 7 with pseudo-random operands), 10 (as 7 with varied metadata), 11 (both), 12 (as 7 with the
-// GEMM's per-stage barrier wait, fence and multicast commit), 13 (wait only), 14 (fence only),
-// 15 (multicast commit only), 16 (commit to the issuing CTA only), 17-19 (the full sequence of 12 once
-// every 4, 8, 16 MMAs), 20 (as 7, selector alternating 0/1), 21 (as 7, metadata column alternating
-// 256/258), 22 (as 7, metadata address walking like the GEMM's ring), 23 (the sequence of 12 with
-// descriptors built once);
+// CTA-pair variant: modes 6 (sparse, A 128-byte swizzle), 7 (sparse, A 64-byte swizzle), 8 (dense);
 // M = 256 across the pair, N = 256 (each CTA holds 128 rows of B).
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
     mma_rate_pair_kernel(int mode, int iters, DevCtl ctl, unsigned long long* cycles) {
@@ -112,22 +106,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
   __shared__ uint32_t slot;
   const int t = threadIdx.x, warp = t >> 5;
   const bool leader = cluster_ctarank() == 0;
-  const bool rnd_data = mode == 9 || mode == 11, rnd_meta = mode == 10 || mode == 11;
-  for (int i = t; i < 256 * 128 / 4; i += blockDim.x) {
-    uint32_t v = 0x3F803F80u;
-    if (rnd_data) {  // pseudo-random bf16 pairs with magnitudes in [1, 2) and random signs
-      uint32_t h = (static_cast<uint32_t>(i) + 0x9E3779B9u * (blockIdx.x + 1)) * 2654435761u;
-      h ^= h >> 15;
-      h *= 2246822519u;
-      h ^= h >> 13;
-      v = 0x3F803F80u | (h & 0x807F807Fu);
-    }
-    reinterpret_cast<uint32_t*>(smem)[i] = v;
-  }
-  __shared__ __align__(8) uint64_t step_bar;
+  for (int i = t; i < 256 * 128 / 4; i += blockDim.x) reinterpret_cast<uint32_t*>(smem)[i] = 0x3F803F80u;
   if (t == 0) {
     mbar_init(&bar, 1);
-    mbar_init(&step_bar, 1);
     fence_mbar_init();
   }
   fence_proxy_async();
@@ -140,71 +121,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
   cluster_sync();
   tc_fence_after();
   const uint32_t tm = slot;
-  {
-    uint32_t mw = 0x44444444u;
-    if (rnd_meta) {  // a valid but varied nibble in every group of every lane
-      const uint32_t nibs[6] = {0x4, 0x8, 0xC, 0x9, 0xD, 0xE};
-      mw = 0;
-      for (int g = 0; g < 8; ++g) mw |= nibs[(t * 7 + g * 5 + (t >> 3)) % 6] << (4 * g);
-    }
-    for (int col = 256; col < 288; ++col) tc_st_32x32b_x1(tm + (static_cast<uint32_t>(warp * 32) << 16) + col, mw);
-  }
+  for (int col = 256; col < 288; ++col) tc_st_32x32b_x1(tm + (static_cast<uint32_t>(warp * 32) << 16) + col, 0x44444444u);
   tc_wait_st();
   tc_fence_before();
   __syncthreads();
   cluster_sync();
   tc_fence_after();
-  if (t == 0 && leader && mode == 23) {
-    // the per-two-MMA wait, fence and multicast commit of mode 12, with the descriptors built once and
-    // advanced by single additions (the issuing thread's instruction stream kept short)
-    constexpr uint32_t IDS = idesc_bf16(256, 256, true);
-    mbar_arrive(&step_bar);
-    const uint64_t a0 = sdesc(smem_u32(A), 16, 512, SWZ_64B), b0 = sdesc(smem_u32(B), 16, 1024, SWZ_128B);
-    const uint32_t meta = tm + 256;
-    const uint64_t t0 = clock64();
-    for (int i = 0; i < iters; i += 2) {
-      mbar_wait(&step_bar, 0, ctl, 8);
-      tc_fence_after();
-      tc_mma_sp_pair(tm, a0, b0, meta, IDS, i != 0);
-      tc_mma_sp_pair(tm, a0 + 2, b0 + 4, meta, IDS | 1u, 1);
-      tc_commit_pair(&bar, 0x3);
-    }
-    tc_commit_pair(&step_bar, 0x1);
-    const bool ok = mbar_wait(&step_bar, 1, ctl, 9);
-    const uint64_t t1 = clock64();
-    if (ok) atomicMax(cycles, static_cast<unsigned long long>(t1 - t0));
-  } else if (t == 0 && leader && mode >= 12 && mode <= 19) {
-    // per pair of MMAs: a wait on an mbarrier phase that has already completed, a tcgen05 fence and a
-    // multicast commit, as the GEMM's MMA warp does per stage
-    constexpr uint32_t IDS = idesc_bf16(256, 256, true);
-    mbar_arrive(&step_bar);  // complete phase 0 so every wait below succeeds at once
-    const uint64_t t0 = clock64();
-    for (int i = 0; i < iters; ++i) {
-      // modes 17-19: the full per-stage sequence once every 4, 8 or 16 MMAs
-      const int every = mode == 17 ? 4 : mode == 18 ? 8 : mode == 19 ? 16 : 2;
-      const bool full_seq = mode == 12 || mode >= 17;
-      const bool do_wait = full_seq || mode == 13, do_fence = full_seq || mode == 14;
-      const bool do_mcommit = full_seq || mode == 15, do_commit = mode == 16;
-      if ((i % every) == 0) {
-        if (do_wait) mbar_wait(&step_bar, 0, ctl, 8);
-        if (do_fence) tc_fence_after();
-      }
-      const uint32_t k = i & 3;
-      tc_mma_sp_pair(tm, sdesc(smem_u32(A) + (k & 1) * 32, 16, 512, SWZ_64B),
-                     sdesc(smem_u32(B) + (k & 1) * 64, 16, 1024, SWZ_128B), tm + 256, IDS | (i & 1), i != 0);
-      if ((i % every) == every - 1 && do_mcommit) tc_commit_pair(&bar, 0x3);
-      if ((i % every) == every - 1 && do_commit)
-        asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                         smem_u32(&bar))
-                     : "memory");
-    }
-    tc_commit_pair(&bar, 0x3);
-    // the commits above complete many phases of `bar`; wait for the drain with a fresh barrier instead
-    tc_commit_pair(&step_bar, 0x1);
-    const bool ok = mbar_wait(&step_bar, 1, ctl, 9);
-    const uint64_t t1 = clock64();
-    if (ok) atomicMax(cycles, static_cast<unsigned long long>(t1 - t0));
-  } else if (t == 0 && leader) {
+  if (t == 0 && leader) {
     constexpr uint32_t ID = idesc_bf16(256, 256, false), IDS = idesc_bf16(256, 256, true);
     const uint64_t t0 = clock64();
     for (int i = 0; i < iters; ++i) {
@@ -212,17 +135,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
       if (mode == 6)
         tc_mma_sp_pair(tm, sdesc(smem_u32(A) + (k & 1) * 32, 16, 1024, SWZ_128B),
                        sdesc(smem_u32(B) + (k & 1) * 64, 16, 1024, SWZ_128B), tm + 256, IDS, i != 0);
-      else if (mode == 20)  // alternating selector: columns 256, 257, 256, ...
-        tc_mma_sp_pair(tm, sdesc(smem_u32(A) + (k & 1) * 32, 16, 512, SWZ_64B),
-                       sdesc(smem_u32(B) + (k & 1) * 64, 16, 1024, SWZ_128B), tm + 256, IDS | (i & 1), i != 0);
-      else if (mode == 21)  // alternating even columns 256, 258 with selector 0
-        tc_mma_sp_pair(tm, sdesc(smem_u32(A) + (k & 1) * 32, 16, 512, SWZ_64B),
-                       sdesc(smem_u32(B) + (k & 1) * 64, 16, 1024, SWZ_128B), tm + 256 + 2 * (i & 1), IDS, i != 0);
-      else if (mode == 22)  // the GEMM's walk: 8 groups of 4 columns, pair (i/2)%2, selector i%2
-        tc_mma_sp_pair(tm, sdesc(smem_u32(A) + (k & 1) * 32, 16, 512, SWZ_64B),
-                       sdesc(smem_u32(B) + (k & 1) * 64, 16, 1024, SWZ_128B),
-                       tm + 256 + 4 * ((i / 4) % 8) + 2 * ((i / 2) % 2), IDS | (i & 1), i != 0);
-      else if (mode == 7 || mode == 9 || mode == 10 || mode == 11)
+      else if (mode == 7)
         tc_mma_sp_pair(tm, sdesc(smem_u32(A) + (k & 1) * 32, 16, 512, SWZ_64B),
                        sdesc(smem_u32(B) + (k & 1) * 64, 16, 1024, SWZ_128B), tm + 256, IDS, i != 0);
       else
@@ -235,7 +148,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
     if (ok) atomicMax(cycles, static_cast<unsigned long long>(t1 - t0));
   }
   __syncwarp();
-  if (!leader && (mode < 12 || mode > 19) && mode != 23) mbar_wait(&bar, 0, ctl, 7);
+  if (!leader) mbar_wait(&bar, 0, ctl, 7);
   tc_fence_before();
   __syncthreads();
   cluster_sync();
@@ -251,8 +164,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
 using namespace lynx;
 
 extern "C" int lynx_mma_rate(int mode, int iters, double* tflops, double* macs_per_clock, void* stream) {
-  if (mode < 0 || mode > 23) return LYNX_ERR_UNSUPPORTED;
-  const bool pair = mode >= 6;  // 6..16
+  if (mode < 0 || mode > 8) return LYNX_ERR_UNSUPPORTED;
+  const bool pair = mode >= 6;
   const int sparse = mode != 0;
   if (!tflops || !macs_per_clock) return LYNX_ERR_NULL;
   if (iters < 1 || iters > (1 << 24)) return LYNX_ERR_SHAPE;

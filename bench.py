@@ -160,9 +160,14 @@ def max_over_ranks(x: float, world: int, device: str = "cuda") -> float:
 
 
 # ----------------------------------------------------------------------------- CPU oracle legs
-def oracle_rows_rate(t: dict, rows_per_call: int, budget_s: float, max_calls: int | None = None):
-    """Time the oracle on consecutive row samples; returns (TFLOP/s, rows, seconds, calls)."""
-    import oracle.lynx_oracle as O
+def oracle_rows_rate(t: dict, rows_per_call: int, budget_s: float, max_calls: int | None = None,
+                     threads: int | None = None):
+    """Time the plain C++ oracle on consecutive row samples with ``threads`` std::threads (default: every host
+    core); returns (TFLOP/s, rows, seconds, calls)."""
+    from oracle import cpp
+    O = cpp.CppOracle(cpp.build())
+    if threads:
+        O.threads = threads
     M, N, K = t["M"], t["N"], t["K"]
     done_rows, calls, t0 = 0, 0, time.perf_counter()
     while True:
@@ -177,41 +182,70 @@ def oracle_rows_rate(t: dict, rows_per_call: int, budget_s: float, max_calls: in
     return 2.0 * done_rows * N * K / el / 1e12, done_rows, el, calls
 
 
-def cpu_threads() -> int:
+def host_cores() -> int:
+    from oracle import cpp
+    return cpp.host_threads()
+
+
+def cpu_model() -> str:
     try:
-        from threadpoolctl import threadpool_info
-        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
-        if n and n[0]:
-            return int(n[0])
-    except Exception:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
         pass
-    return os.cpu_count() or 1
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.machine() or "unknown"
+
+
+def cpu_baseline_leg(t: dict) -> dict:
+    """The C++ oracle on bounded row samples of the bench workload: every host core (about 10 s), then one
+    thread (about 8 s)."""
+    cores = host_cores()
+    tf, rows, secs, _ = oracle_rows_rate(t, 8 * cores, 10.0, threads=cores)
+    tf1, rows1, secs1, _ = oracle_rows_rate(t, 8, 8.0, threads=1)
+    return {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{rows} rows of the QKV workload in {secs:.1f} s on {cores} std::threads "
+                      f"(plain C++ double oracle; W, LA, LB widened once per call)",
+            "cpu_model": cpu_model(),
+            "t1": {"value": tf1, "unit": "TFLOP/s", "threads": 1,
+                   "sample": f"{rows1} rows in {secs1:.1f} s on one thread"}}
 
 
 def run_reference(args) -> int:
-    """The oracle as it stands, on the host cores: each step is a bounded row sample."""
+    """The oracle as it stands, on the host cores: each step is one C++ oracle call on a bounded row sample."""
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
     import synth
     t = synth.layer_tensors(*WORKLOAD)
-    rows = 64
-    oracle_rows_rate(t, rows, 0, max_calls=max(1, args.warmup))  # warm-up
+    cores = host_cores()
+    rows = 4 * cores
+    oracle_rows_rate(t, rows, 0, max_calls=max(1, args.warmup), threads=cores)  # warm-up
     times = []
     for i in range(args.steps):
         t0 = time.perf_counter()
-        oracle_rows_rate(t, rows, 0, max_calls=1)
+        oracle_rows_rate(t, rows, 0, max_calls=1, threads=cores)
         times.append(time.perf_counter() - t0)
     step_s = sum(times) / len(times)
     value = 2.0 * rows * t["N"] * t["K"] / step_s / 1e12
-    cores = cpu_threads()
-    sample = f"{rows} of {t['M']} rows per step (QKV 4608x3072 -> 9216, rank 64), float64 numpy oracle"
+    sample = (f"{rows} of {t['M']} rows per step (QKV 4608x3072 -> 9216, rank 64), plain C++ double oracle on "
+              f"{cores} std::threads")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_dict(t, "reference"),
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample,
+                         "cpu_model": cpu_model()},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -475,22 +509,27 @@ def main() -> int:
     assert st == 0, asl.lynx_status_string(st)
     torch.cuda.empty_cache()
 
-    # The block stack: 8 blocks x (QKV sparse 3072->9216, out dense 3072->3072, up dense 3072->12288,
-    # down sparse 12288->3072), rank-64 LoRA on the sparse layers, independent seeded weights per block; the
+    # The block stack of the fifth workload: 8 blocks x (QKV sparse 3072->9216, out dense 3072->3072, up dense
+    # 3072->12288, down sparse 12288->3072), rank-64 LoRA on the sparse layers, the seeded weights of every
+    # block and the seeded activations of block 0 (the down layer's input is its GELU input) from synth; the
     # total time of the 32 linears at each M against the same 32 layers run dense through cuBLAS.
     stack = {}
-    wts = []
-    for b in range(8):
-        def w_(n, k):
-            return (torch.randn((n, k), generator=gen, device=dev) / k ** 0.5).to(torch.bfloat16)
 
-        def l_(a, c):
-            return (0.02 * torch.randn((a, c), generator=gen, device=dev)).to(torch.bfloat16)
-        wts.append({"qkv": w_(9216, 3072), "out": w_(3072, 3072), "up": w_(12288, 3072), "down": w_(3072, 12288),
-                    "la_qkv": l_(9216, R), "lb_qkv": l_(R, 3072), "la_down": l_(3072, R), "lb_down": l_(R, 12288)})
-    for Ms in (1024, 4608, 9216, 16384):
-        x3 = torch.randn((Ms, 3072), generator=gen, device=dev).to(torch.bfloat16)
-        x12 = torch.relu(torch.randn((Ms, 12288), generator=gen, device=dev)).to(torch.bfloat16)
+    def block_weights(b):
+        tq = synth.layer_tensors("stack", "qkv", block=b, with_x=False)
+        td = synth.layer_tensors("stack", "down", block=b, with_x=False)
+        return {"qkv": tq["W"], "la_qkv": tq["LA"], "lb_qkv": tq["LB"],
+                "out": synth.layer_tensors("stack", "out", block=b, with_x=False)["W"],
+                "up": synth.layer_tensors("stack", "up", block=b, with_x=False)["W"],
+                "down": td["W"], "la_down": td["LA"], "lb_down": td["LB"]}
+
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(8) as ex:
+        wts = [{k: to_dev(v) for k, v in w.items()} for w in ex.map(block_weights, range(8))]
+        xs = list(ex.map(lambda a: synth.layer_x("stack", a[1], M=a[0], block=0),
+                         [(Ms, l) for Ms in synth.STACK_M for l in ("qkv", "down")]))
+    for i, Ms in enumerate(synth.STACK_M):
+        x3, x12 = to_dev(xs[2 * i]), to_dev(xs[2 * i + 1])
         y = {n: torch.empty((Ms, n), dtype=torch.bfloat16, device=dev) for n in (3072, 9216, 12288)}
         ws_s = torch.empty(max(asl.lynx_workspace_bytes(Ms, 9216, 3072, R), asl.lynx_workspace_bytes(Ms, 3072, 12288, R)),
                            dtype=torch.uint8, device=dev)
@@ -547,7 +586,7 @@ def main() -> int:
                             "lynx_graph_ms": tt[2], "all_dense_cublas_graph_ms": tt[3],
                             "x_vs_dense_cublas_graph": tt[3] / tt[2]}
         del x3, x12, y, ws_s, layers, lgraph, dgraph
-    del wts
+    del wts, xs
     torch.cuda.empty_cache()
 
     # End to end through the C-ABI with host buffers, pipelined as a serving loop runs it: every step copies
@@ -606,8 +645,8 @@ def main() -> int:
             dist.destroy_process_group()
         return 0
 
-    # CPU baseline: the oracle on a bounded row sample, ~10 s
-    cpu_tf, cpu_rows, cpu_s, _ = oracle_rows_rate(t, 64, 10.0)
+    # CPU baseline: the C++ oracle on bounded row samples, every host core and one thread
+    cpu_base = cpu_baseline_leg(t)
     clocks = clk.summary()
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -619,8 +658,7 @@ def main() -> int:
                      "traffic": profiled_traffic("sparse_gemm_pair_qkv.md", "gemm_pair.cu"),
                      "kernel": "sparse GEMM + LoRA-up + s epilogue (tcgen05.mma.sp)",
                      "peak_source": f"2 x dense bf16 burst {dense_tf} TFLOP/s (nominal 2:4 ratio), {peaks['source']}"},
-        "cpu_baseline": {"value": cpu_tf, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
-                         "sample": f"{cpu_rows} rows of the QKV workload in {cpu_s:.1f} s (float64 numpy oracle)"},
+        "cpu_baseline": cpu_base,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": M * K * 2,
                 "d2h_bytes_per_step": M * N * 2, "ms_per_step": e2e_ms,
                 "note": "every step: pinned host X -> device, lynx_linear, Y -> pinned host; weights resident; "

@@ -142,12 +142,19 @@ LYNX_API int lynx_linear(const void* X, const void* W, const void* LA, const voi
  * allocating routine.
  *
  * Limits and rules:
- *   - a problem whose lynx_workspace_bytes(M, N, K, R) exceeds
- *     LYNX_NOALLOC_SCRATCH_BYTES is rejected with LYNX_ERR_TOO_LARGE before
- *     anything is enqueued;
+ *   - arguments are checked as lynx_linear checks them (NULL, shape, rank,
+ *     alignment statuses first); a valid problem whose
+ *     lynx_workspace_bytes(M, N, K, R) exceeds LYNX_NOALLOC_SCRATCH_BYTES is
+ *     then rejected with LYNX_ERR_TOO_LARGE, before anything is enqueued;
  *   - the first call on a device, with that device current, looks up the
  *     array's device address (cudaGetSymbolAddress); make that first call
  *     before any stream capture;
+ *   - the CUDA runtime loads the library's device code on a device lazily, at
+ *     the first lynx_* call that launches or looks up a symbol there, and the
+ *     array is reserved at that moment: that first call can allocate and
+ *     synchronise.  A caller that must never stall makes one warm-up call per
+ *     device (any lynx_* call that enqueues work, or this entry point on a
+ *     small problem) outside its request loop and before any capture;
  *   - every call on a device shares the one array and leaves its contents
  *     behind (nothing in it has to start at zero), so calls whose kernels
  *     overlap on the GPU -- on different streams, or from different threads --
@@ -268,16 +275,9 @@ LYNX_API void lynx_profile_next(void* const* events, int count);
  * four MMAs, mode 5 tcgen05.mma.sp with A in 64-byte rows (64-byte swizzle);
  * modes 6-8 run on CTA pairs (tcgen05 cta_group::2, M = 256 over two SMs):
  * 6 sparse with 128-byte-swizzled A, 7 sparse with 64-byte-swizzled A,
- * 8 dense, 9 as 7 with pseudo-random operands, 10 as 7 with varied
- * metadata, 11 both, 12 as 7 with a barrier wait, fence and multicast
- * commit per two MMAs, 13 the wait only, 14 the fence only, 15 the
- * multicast commit only, 16 a commit to the issuing CTA only, 17-19 the
- * sequence of mode 12 once every 4, 8 or 16 MMAs, 20 as 7 with the
- * selector alternating, 21 as 7 with the metadata column alternating, 22 as
- * 7 with the metadata address walking the GEMM's 32-column ring, 23 the
- * sequence of mode 12 with descriptors built once outside the loop.  Writes
- * the dense-equivalent rate (2*M*N*K per instruction, K = 16 dense or 32
- * logical sparse) in TFLOP/s and in MACs per SM clock.  Synchronises `stream`. */
+ * 8 dense.  Writes the dense-equivalent rate (2*M*N*K per instruction,
+ * K = 16 dense or 32 logical sparse) in TFLOP/s and in MACs per SM clock.
+ * Other modes return LYNX_ERR_UNSUPPORTED.  Synchronises `stream`. */
 LYNX_API int lynx_mma_rate(int mode, int iters, double* tflops, double* macs_per_clock, void* stream);
 
 /* Test hook.  inject = 1 makes the next GEMM launches never deliver their

@@ -14,10 +14,11 @@ a few strongly active channels per token (Key idea):
 
 * ``act``  -- N(0, 1) with a fixed random subset of channels (columns) scaled
   by a constant: the same outlier channels for every token;
-* ``gelu`` -- exact-erf GELU applied to N(0, v) with the same outlier-channel
-  structure; it stands in for GELU(up-projection output), a nonnegative-leaning
-  heavy-tailed input of the MLP down projection.  v = 1 + f*(a*a - 1) is the
-  variance that X·W_upᵀ has when W_up ~ N(0, 1/K) and X follows ``act``;
+* ``gelu`` -- exact-erf GELU applied to N(0, v): the element distribution of
+  GELU(up-projection output), the nonnegative-leaning input of the MLP down
+  projection.  v = 1 + f*(a*a - 1) is the variance that each entry of X·W_upᵀ
+  has when W_up ~ N(0, 1/K) and X follows ``act``; the weights mix every input
+  channel into every output, so the pre-activations carry no outlier channels;
 * weights ``W ~ N(0, 1/K)`` (variance 1/K), LoRA factors ``N(0, 0.02)`` (std
   0.02), seeded per tensor.
 """
@@ -30,7 +31,7 @@ import numpy as np
 
 __all__ = [
     "bf16_bits", "bf16_to_f32", "rng", "gaussian_bf16", "act_bf16", "gelu_bf16",
-    "Layer", "Workload", "WORKLOADS", "layer_tensors", "sample_rows",
+    "Layer", "Workload", "WORKLOADS", "layer_tensors", "layer_x", "sample_rows",
     "STACK_M", "structured_x",
 ]
 
@@ -40,9 +41,10 @@ def bf16_bits(a: np.ndarray) -> np.ndarray:
 
     Inputs are finite by construction, so no NaN handling is needed.
     """
-    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
-    return u.astype(np.uint16)
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
+    r = u + np.uint32(0x7FFF)  # finite values stay below 2^32 (the largest finite pattern is 0xFF7FFFFF)
+    r += (u >> np.uint32(16)) & np.uint32(1)
+    return (r >> np.uint32(16)).astype(np.uint16)
 
 
 def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
@@ -85,7 +87,7 @@ def _gelu(z: np.ndarray) -> np.ndarray:
 
 def gelu_bf16(key: tuple, M: int, K: int, pre_var: float, frac: float, scale: float,
               chan_key: tuple | None = None) -> np.ndarray:
-    """GELU(N(0, pre_var)) with outlier channels scaled before the GELU."""
+    """GELU(N(0, pre_var)), with round(frac*K) channels scaled by ``scale`` before the GELU (none for frac = 0)."""
     z = rng(*key).standard_normal((M, K), dtype=np.float32)
     z *= np.float32(math.sqrt(pre_var))
     ch = _outlier_channels(chan_key or key + (99,), K, frac)
@@ -164,7 +166,7 @@ def _x(wl: Workload, layer: Layer, M: int, block: int, batch: int = 0) -> np.nda
             parts.append(act_bf16(key, mh, layer.K, wl.frac, wl.scale, chan_key=chan))
         else:
             pre_var = 1.0 + wl.frac * (wl.scale * wl.scale - 1.0)
-            parts.append(gelu_bf16(key, mh, layer.K, pre_var, wl.frac, wl.scale, chan_key=chan))
+            parts.append(gelu_bf16(key, mh, layer.K, pre_var, 0.0, 1.0, chan_key=chan))
     return parts[0] if len(parts) == 1 else np.concatenate(parts, axis=0)
 
 
@@ -187,6 +189,12 @@ def layer_tensors(workload: str, layer: str, M: int | None = None, block: int = 
     if with_x:
         out["X"] = _x(wl, ly, M, block, batch)
     return out
+
+
+def layer_x(workload: str, layer: str, M: int | None = None, block: int = 0, batch: int = 0) -> np.ndarray:
+    """The seeded activation X (M x K bf16 bits) of one linear alone: the same bits as layer_tensors()["X"]."""
+    wl = WORKLOADS[workload]
+    return _x(wl, wl.layer(layer), wl.M if M is None else M, block, batch)
 
 
 def sample_rows(key: tuple, M: int, n: int = 512, edge: int = 64) -> np.ndarray:

@@ -105,6 +105,19 @@ def test_other_entry_points_reject_bad_arguments(asl):
         assert L.lynx_status_string(code)
 
 
+def test_noalloc_checks_arguments_before_the_scratch_size(asl):
+    """Bad pointers, ranks and shapes report their own status, not LYNX_ERR_TOO_LARGE (host checks only)."""
+    fn = asl.lib.lynx_linear_noalloc
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int64] * 4 + [ctypes.c_void_p]
+    assert fn(None, A, A, A, A, 16, 16, 16, 64, None) == -1                  # NULL X
+    assert fn(A, A, A, A, A, 16, 16, 16, 4096, None) == -7                   # rank other than 64
+    assert fn(A, A, A, A, A, 4608, 9216, 3072, 4096, None) == -7             # ... even when its bytes are large
+    assert fn(A, A, A, A, A, 16, 16, 24, 64, None) == -2                     # K % 16
+    assert fn(A + 8, A, A, A, A, 16, 16, 16, 64, None) == -3                 # misaligned X
+    assert fn(A, A, A, A, A, 16384, 3072, 12288, 64, None) == -8             # valid, beyond the scratch
+
+
 def test_force_split_range(asl):
     L = asl.lib
     try:

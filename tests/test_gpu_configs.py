@@ -8,7 +8,7 @@ host memory, and on the sampled rows otherwise."""
 import numpy as np
 import pytest
 
-import oracle.lynx_oracle as O
+from oracle import cpp as O
 import synth
 from helpers import S_RTOL, assert_y_close, to_bits, to_dev
 

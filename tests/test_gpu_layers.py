@@ -4,7 +4,7 @@ bit for bit, and the oracle accepts every layer given the same inputs."""
 import numpy as np
 import pytest
 
-import oracle.lynx_oracle as O
+from oracle import cpp as O
 import synth
 from helpers import assert_y_close, to_bits, to_dev
 

@@ -3,7 +3,7 @@
 import numpy as np
 import pytest
 
-import oracle.lynx_oracle as O
+from oracle import cpp as O
 import synth
 from helpers import S_RTOL, assert_y_close, pack_meta_reference, to_bits, to_dev
 

@@ -4,7 +4,7 @@ degenerate cases of the method."""
 import numpy as np
 import pytest
 
-import oracle.lynx_oracle as O
+from oracle import cpp as O
 import synth
 from helpers import REL_FRO, S_RTOL, assert_y_close, pack_meta_reference, to_bits, to_dev, widen
 
@@ -14,8 +14,8 @@ pytestmark = pytest.mark.gpu
 def _x(kind, M, K, seed=1):
     if kind == "act":
         return synth.act_bf16((M, K, seed), M, K, 0.05, 8.0)
-    if kind == "gelu":
-        return synth.gelu_bf16((M, K, seed), M, K, 3.97, 0.03, 10.0)
+    if kind == "gelu":  # GELU of the up projection's Gaussian pre-activations (variance 3.97)
+        return synth.gelu_bf16((M, K, seed), M, K, 3.97, 0.0, 1.0)
     return synth.structured_x(kind, M, K, seed)
 
 
@@ -165,8 +165,7 @@ def test_linear_structured_inputs(lynx, kind):
     X, W, LA, LB = _layer(160, 384, 256, 11, kind)
     Y = lynx.lynx_linear(to_dev(X), to_dev(W), to_dev(LA), to_dev(LB))
     assert lynx.lynx_sync_status() == 0
-    # 8 outlier channels x10 before the GELU make |y|max ~ 10 rms: bf16 output rounding floor applies
-    assert_y_close(to_bits(Y), O.linear(X, W, LA, LB), bf16_floor=(kind == "gelu"))
+    assert_y_close(to_bits(Y), O.linear(X, W, LA, LB))
 
 
 def test_linear_zero_rows_give_lora_only(lynx):

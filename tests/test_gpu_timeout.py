@@ -6,7 +6,7 @@ the next call with the switch off gives the right answer."""
 import numpy as np
 import pytest
 
-import oracle.lynx_oracle as O
+from oracle import cpp as O
 import synth
 from helpers import assert_y_close, to_bits, to_dev
 

@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 
 import synth
-from helpers import assert_y_close, to_bits, to_dev, widen
+from helpers import to_bits, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -35,22 +35,25 @@ def _layer(M, N, K, seed):
 
 
 def test_noalloc_matches_lynx_linear_on_consecutive_calls(lynx):
+    """Both entry points run the same kernels on the same inputs (only the workspace address differs), so
+    their outputs are identical bit for bit.  The larger problem runs first, so the smaller one finds the
+    earlier call's values, metadata, s and T' left in the shared array."""
     import torch
     fn = _fn(lynx)
     stream = torch.cuda.current_stream().cuda_stream
     outs = []
-    for seed, (M, N, K) in ((31, (300, 520, 528)), (32, (1024, 1536, 3072))):
+    for seed, (M, N, K) in ((32, (1024, 1536, 3072)), (31, (300, 520, 528))):
         X, W, LA, LB = _layer(M, N, K, seed)
         ref = lynx.lynx_linear(X, W, LA, LB)  # the existing entry point, with its own workspace
         Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
         st = fn(X.data_ptr(), W.data_ptr(), LA.data_ptr(), LB.data_ptr(), Y.data_ptr(), M, N, K, 64, stream)
         assert st == 0, lynx.lynx_status_string(st)
         assert lynx.lynx_sync_status() == 0
-        assert_y_close(to_bits(Y), widen(to_bits(ref)), "noalloc vs lynx_linear")
+        assert np.array_equal(to_bits(Y), to_bits(ref)), f"noalloc differs from lynx_linear at {(M, N, K)}"
         outs.append((Y, ref))
     # the second call reused the scratch array; the first call's result is untouched
     Y0, ref0 = outs[0]
-    assert_y_close(to_bits(Y0), widen(to_bits(ref0)), "first call after the second")
+    assert np.array_equal(to_bits(Y0), to_bits(ref0)), "first call's output changed by the second call"
 
 
 def test_noalloc_refuses_problems_beyond_its_scratch(lynx):
