@@ -22,19 +22,24 @@ __all__ = [
     "lynx_linear_dense", "lynx_prune_weight", "lynx_linear_wsparse",
     "lynx_sync_status", "lynx_status_string", "lynx_meta_to_canonical", "lynx_debug_set_fault",
     "lynx_debug_force_tile", "lynx_debug_force_split", "lynx_debug_prologue_split",
+    "lynx_debug_force_ksplit", "lynx_debug_linear_ksplit",
     "lynx_profile_next", "lynx_linear_kernel_count", "lynx_mma_rate",
     "LynxLayer", "lynx_layer", "lynx_layers_workspace_bytes", "lynx_run_layers", "LynxGraph",
+    "LYNX_LAYER_SPARSE", "LYNX_LAYER_GELU", "lynx_debug_pair_offsets",
 ]
 
 LYNX_OK = 0
 LYNX_ERR_TIMEOUT = -6
+LYNX_LAYER_SPARSE = 1
+LYNX_LAYER_GELU = 2
 
 _c_i64, _c_sz, _c_p = ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p
 
 
 class LynxLayer(ctypes.Structure):
-    """``lynx_layer`` of include/lynx.h: one sparse (lynx_linear) or dense (lynx_linear_dense) layer."""
-    _fields_ = [("sparse", ctypes.c_int32), ("X", _c_p), ("W", _c_p), ("LA", _c_p), ("LB", _c_p), ("Y", _c_p),
+    """``lynx_layer`` of include/lynx.h: one sparse (lynx_linear) or dense (lynx_linear_dense) layer; ``flags``
+    bit 0 = sparse, bit 1 = GELU of the output."""
+    _fields_ = [("flags", ctypes.c_int32), ("X", _c_p), ("W", _c_p), ("LA", _c_p), ("LB", _c_p), ("Y", _c_p),
                 ("M", _c_i64), ("N", _c_i64), ("K", _c_i64), ("R", _c_i64)]
 
 
@@ -65,6 +70,8 @@ def _load() -> ctypes.CDLL:
         "lynx_debug_force_tile": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
         "lynx_debug_force_split": (ctypes.c_int, [ctypes.c_int]),
         "lynx_debug_prologue_split": (ctypes.c_int, [_c_i64, _c_i64]),
+        "lynx_debug_force_ksplit": (ctypes.c_int, [ctypes.c_int]),
+        "lynx_debug_linear_ksplit": (ctypes.c_int, [_c_i64, _c_i64, _c_i64]),
         "lynx_profile_next": (None, [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]),
         "lynx_linear_kernel_count": (ctypes.c_int, [_c_i64, _c_i64, _c_i64, _c_i64]),
         "lynx_mma_rate": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_double),
@@ -74,6 +81,8 @@ def _load() -> ctypes.CDLL:
         "lynx_graph_create": (ctypes.c_int, [_c_layers, ctypes.c_int32, _c_p, _c_sz, ctypes.POINTER(_c_p), _c_i32p]),
         "lynx_graph_launch": (ctypes.c_int, [_c_p, _c_p]),
         "lynx_graph_destroy": (ctypes.c_int, [_c_p]),
+        "lynx_debug_pair_offsets": (ctypes.c_int, [_c_layers, ctypes.c_int32, ctypes.c_int32,
+                                                   ctypes.POINTER(ctypes.c_size_t)]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -284,7 +293,8 @@ def lynx_debug_set_fault(inject: int, wait_ns: int = 0) -> None:
 
 
 def lynx_debug_force_tile(tile_rows: int, tile_cols: int) -> None:
-    """Test hook: forces the 512x224, 512x192 or 256x256 sparse tile shape; (0, 0) restores the automatic choice."""
+    """Test hook: forces the 512x224, 512x192, 256x256 or 256x192 sparse tile shape; (0, 0) restores the automatic
+    choice."""
     _check(lib.lynx_debug_force_tile(tile_rows, tile_cols), "lynx_debug_force_tile")
 
 
@@ -293,15 +303,28 @@ def lynx_debug_force_split(split: int) -> None:
     _check(lib.lynx_debug_force_split(split), "lynx_debug_force_split")
 
 
+def lynx_debug_force_ksplit(splits: int) -> None:
+    """Test hook: the sparse GEMM splits the k-steps of each one-row-block tile (256 x 256, 256 x 192) over
+    ``splits`` units; 0 = automatic."""
+    _check(lib.lynx_debug_force_ksplit(splits), "lynx_debug_force_ksplit")
+
+
+def lynx_debug_linear_ksplit(M: int, N: int, K: int) -> int:
+    """The k-split count lynx_linear picks on this device for M x K -> N (1 = none)."""
+    return lib.lynx_debug_linear_ksplit(M, N, K)
+
+
 def lynx_debug_prologue_split(M: int, K: int) -> int:
     """Cluster size the sparsify pass picks on this device for an M x K activation."""
     return lib.lynx_debug_prologue_split(M, K)
 
 
 # ------------------------------------------------------------------ layer sequences and their CUDA graphs
-def lynx_layer(X, W, LA=None, LB=None, Y=None, sparse: bool = True) -> dict:
-    """One layer of a sequence: Y = lynx_linear(X, W, LA, LB) (sparse) or lynx_linear_dense(X, W, LA, LB).
-    Allocates Y (M x N bf16) when not given.  The dict keeps the tensors alive."""
+def lynx_layer(X, W, LA=None, LB=None, Y=None, sparse: bool = True, gelu: bool = False) -> dict:
+    """One layer of a sequence: Y = lynx_linear(X, W, LA, LB) (sparse) or lynx_linear_dense(X, W, LA, LB), passed
+    through the exact-erf GELU when ``gelu`` (the MLP up layer; a following sparse layer that reads this Y runs
+    fused with it, see include/lynx.h).  Allocates Y (M x N bf16) when not given.  The dict keeps the tensors
+    alive."""
     torch = _torch()
     _need(X, "X", torch.bfloat16)
     _need(W, "W", torch.bfloat16)
@@ -309,13 +332,15 @@ def lynx_layer(X, W, LA=None, LB=None, Y=None, sparse: bool = True) -> dict:
     N = W.shape[0]
     R = 64 if LB is None else LB.shape[0]
     Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device) if Y is None else Y
-    return {"sparse": bool(sparse), "X": X, "W": W, "LA": LA, "LB": LB, "Y": Y, "M": M, "N": N, "K": K, "R": R}
+    return {"sparse": bool(sparse), "gelu": bool(gelu), "X": X, "W": W, "LA": LA, "LB": LB, "Y": Y, "M": M, "N": N,
+            "K": K, "R": R}
 
 
 def _c_layer_array(layers):
     arr = (LynxLayer * max(len(layers), 1))()
     for i, l in enumerate(layers):
-        arr[i] = LynxLayer(int(l["sparse"]), _ptr(l["X"]), _ptr(l["W"]), _ptr(l["LA"]), _ptr(l["LB"]), _ptr(l["Y"]),
+        flags = (LYNX_LAYER_SPARSE if l["sparse"] else 0) | (LYNX_LAYER_GELU if l.get("gelu") else 0)
+        arr[i] = LynxLayer(flags, _ptr(l["X"]), _ptr(l["W"]), _ptr(l["LA"]), _ptr(l["LB"]), _ptr(l["Y"]),
                            l["M"], l["N"], l["K"], l["R"])
     return arr
 
@@ -340,6 +365,14 @@ def lynx_run_layers(layers, workspace=None, stream=None):
     _layer_error(lib.lynx_run_layers(_c_layer_array(layers), len(layers), _ptr(workspace), wbytes, _stream(stream),
                                      ctypes.byref(failed)), failed, "lynx_run_layers")
     return [l["Y"] for l in layers]
+
+
+def lynx_debug_pair_offsets(layers, i: int) -> dict:
+    """Workspace byte offsets of the fused MLP pair (i, i + 1): the sparse layer's vals, meta, s, T' and the
+    pair's total bytes."""
+    out = (ctypes.c_size_t * 5)()
+    _check(lib.lynx_debug_pair_offsets(_c_layer_array(layers), len(layers), i, out), "lynx_debug_pair_offsets")
+    return {"vals": out[0], "meta": out[1], "s": out[2], "T": out[3], "total": out[4]}
 
 
 class LynxGraph:

@@ -42,11 +42,31 @@
 #include <atomic>
 
 #include "kernels.h"
+#include "select.cuh"
 
 namespace lynx {
 namespace {
 
+__constant__ SelectTable c_pair_select_table = make_select_table();
+
+__device__ __forceinline__ float tanh_approx(float x) {
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(x));
+  return t;
+}
+// GELU of the up layer's output, x Phi(x), in the tanh form of Hendrycks and Gimpel ("Gaussian Error Linear
+// Units", 2016): 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))), with the hardware tanh approximation.  Its
+// distance from the error-function form is below 1e-3 |x| + 1e-3, under a tenth of a bf16 unit for the
+// values that matter, and it costs a handful of instructions instead of an erf evaluation.
+__device__ __forceinline__ float gelu_f(float x) {
+  const float u = x * fmaf(0.0356774081f, x * x, 0.7978845608f);  // sqrt(2/pi) (x + 0.044715 x^3)
+  const float hx = 0.5f * x;
+  return fmaf(hx, tanh_approx(u), hx);
+}
+
 constexpr int BLOCK = 128;         // rows per TMEM accumulator (one row per lane)
+constexpr int kPairMaxSplit = 4;   // k-splits per tile at most (the host's choice and test hook stay within it)
+constexpr int kDenseBK = 64;       // channels per stage of the dense path (64 or 128: one or two 64-channel boxes)
 constexpr int META_RING = 4;       // TMEM metadata stages
 constexpr int META_GROUP_COLS = 4;
 constexpr int TMEM_COLS = 512;
@@ -67,11 +87,13 @@ template <bool SPARSE, int MB, int TN>
 struct PairCfg {
   static constexpr int ROWS = MB * BLOCK;    // rows per CTA
   static constexpr int HALF_N = TN / 2;      // W rows staged per CTA
-  static constexpr int BK = SPARSE ? 128 : 64;
-  static constexpr int A_BLOCK = BLOCK * 128;
+  static constexpr int BK = SPARSE ? 128 : kDenseBK;
+  static constexpr int BOXES = SPARSE ? 1 : kDenseBK / 64;  // 64-channel (128-byte) A boxes per row block and stage
+  static constexpr int A_BOX = BLOCK * 128;
+  static constexpr int A_BLOCK = BOXES * A_BOX;
   static constexpr int A_SLOT = MB * A_BLOCK;
   static constexpr int SUB = HALF_N * 128;   // one 64-channel W sub-tile of this CTA
-  static constexpr int B_SLOT = SPARSE ? 2 * SUB : SUB;
+  static constexpr int B_SLOT = SPARSE ? 2 * SUB : BOXES * SUB;
   static constexpr int M_SLOT = SPARSE ? MB * kMetaChunkBytes : 0;
   static constexpr int STAGE = A_SLOT + B_SLOT + M_SLOT;
   // Output staging boxes per epilogue warp: two, so that a box is refilled while the other is stored; one
@@ -79,13 +101,21 @@ struct PairCfg {
   // (its few row tiles share each W tile between few CTA pairs, so its loads often come from DRAM).
   static constexpr int Y_BOXES = (SPARSE && MB == 1) ? 1 : 2;
   static constexpr int Y_STAGING = EPI_WARPS * Y_BOXES * Y_BUF;
-  static constexpr int NST = (SMEM_LIMIT - 1280 - Y_STAGING) / STAGE;
+  static constexpr int NST_FIT = (SMEM_LIMIT - 1280 - Y_STAGING) / STAGE;
+  static constexpr int NST = (SPARSE && NST_FIT > META_RING) ? META_RING : NST_FIT;
   static constexpr int SMEM = NST * STAGE + Y_STAGING + 256 + 1024;
-  static constexpr int META_COL = MB * TN;   // first metadata column (after the accumulators)
+  // Accumulator buffers: two where they fit in TMEM next to the metadata ring (the dense 256 x 256 tile, the sparse
+  // 256 x 192 tile), so that the MMAs of the next tile run into one while the epilogue drains the other.
+  static constexpr int META_COLS = SPARSE ? META_RING * MB * META_GROUP_COLS : 0;
+  static constexpr int ACC_BUFS = (2 * MB * TN + META_COLS <= TMEM_COLS) ? 2 : 1;
+  static constexpr int ACC_STRIDE = MB * TN;  // TMEM columns per accumulator buffer
+  static constexpr int META_COL = ACC_BUFS * ACC_STRIDE;  // first metadata column (after the accumulators)
   static_assert(STAGE % 1024 == 0, "stage slots keep 1 KiB alignment");
   static_assert(NST >= 2 && SMEM <= SMEM_LIMIT, "shared memory budget");
   static_assert(TN % 32 == 0 && TN <= 256 && HALF_N % 8 == 0, "MMA N");
-  static_assert(META_COL + (SPARSE ? META_RING * MB * META_GROUP_COLS : 0) <= TMEM_COLS, "TMEM budget");
+  static_assert(META_COL + META_COLS <= TMEM_COLS, "TMEM budget");
+  static_assert(ACC_BUFS * ACC_STRIDE <= TMEM_COLS, "TMEM budget of the accumulator buffers");
+  static_assert(8 * (2 * NST + 2 * ACC_BUFS + 3) + 32 <= 256, "barrier area");
   static_assert(!SPARSE || NST <= META_RING, "a metadata group must outlive the stages in flight");
 };
 
@@ -121,8 +151,12 @@ __device__ __forceinline__ void store_chunk_t(void* Y, int64_t ldy, int zrow, in
 }
 
 // TRANS: the accumulator tile is the transpose of the output (the weight-sparse variant multiplies the pruned
-// W, as the sparse operand, by X); the epilogue writes it transposed.
-template <bool SPARSE, bool LORA, int MB, int TN, bool TRANS>
+// W, as the sparse operand, by X); the epilogue writes it transposed.  SPLIT: the k-steps of every tile are split
+// over a.splits work units (few tiles for the GPU's CTA pairs); see the epilogue.  GELU: the output is
+// bf16(GELU(bf16(y))) and, with a.hvals, the epilogue also sparsifies it for the next layer (the MLP pair's
+// up layer feeding its down layer: "RT-Lynx" page, CUDA kernel optimisation, one execution path for the online
+// sparsification).
+template <bool SPARSE, bool LORA, int MB, int TN, bool TRANS, bool SPLIT, bool GELU>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ PairArgs a) {
   using C = PairCfg<SPARSE, MB, TN>;
@@ -130,18 +164,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   // does its per-stage bookkeeping, the other's queued MMAs keep the tensor pipe busy.
   constexpr int NISS = MB >= 2 ? 2 : 1;
   static_assert(MB % NISS == 0, "row blocks split evenly between the issuers");
+  static_assert(!(GELU && (SPLIT || TRANS)), "the GELU epilogue runs on whole, untransposed tiles");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ystage = smem + C::NST * C::STAGE;  // 1 KiB aligned
   uint64_t* full = reinterpret_cast<uint64_t*>(ystage + C::Y_STAGING);
   uint64_t* empty = full + C::NST;
-  uint64_t* acc_full = empty + C::NST;
-  uint64_t* acc_empty = acc_full + 1;
-  uint64_t* drain = acc_empty + 1;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* acc_full = empty + C::NST;        // [ACC_BUFS]
+  uint64_t* acc_empty = acc_full + C::ACC_BUFS;  // [ACC_BUFS]
+  uint64_t* drain = acc_empty + C::ACC_BUFS;
+  uint64_t* epi_bar = drain + 1;   // split-K: every epilogue warp of this CTA has written its partial
+  uint64_t* epi_bar2 = drain + 2;  // split-K: the unit's arrival order is known
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 3);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   volatile int* consumed_sh = abort_flag + 1;  // one count per MMA issuer
   volatile int* issued_sh = abort_flag + 3;
+  volatile int* last_flag = abort_flag + 4;   // split-K: this CTA reduces the unit's tile
+  uint32_t* sel_table = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(full) + 256);  // GELU: 64 entries
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -151,7 +190,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const int num_n = (a.N + TN - 1) / TN;
   const int ntiles = num_mp * num_n;
   const int nk = (a.K + C::BK - 1) / C::BK;
-  const int nstages = nk + (LORA ? 1 : 0);
+  // Work units: (tile, k-split) pairs, tile fastest; split ks covers k-steps [ks nk / S, (ks + 1) nk / S) and
+  // the last split also the LoRA stage.  With S > 1 each unit leaves an fp32 partial in global memory and the
+  // last unit of a tile to finish adds the S partials in split order (see the epilogue).
+  const int S = SPLIT ? a.splits : 1;
+  const int nunits = ntiles * S;
   const int64_t blocks_k = meta_blocks_k(a.K);
   const int meta_rowblocks = static_cast<int>(round_up(a.M, kMetaRowPad) / kMetaRows);
 
@@ -160,15 +203,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], NISS);  // one commit per MMA issuer
     }
-    mbar_init(acc_full, NISS);
-    mbar_init(acc_empty, 2 * EPI_WARPS);  // every epilogue warp of both CTAs of the pair
+    for (int b = 0; b < C::ACC_BUFS; ++b) {
+      mbar_init(&acc_full[b], NISS);
+      mbar_init(&acc_empty[b], 2 * EPI_WARPS);  // every epilogue warp of both CTAs of the pair
+    }
     mbar_init(drain, NISS);
+    mbar_init(epi_bar, EPI_WARPS);
+    mbar_init(epi_bar2, 1);
     *abort_flag = 0;
     consumed_sh[0] = 0;
     consumed_sh[1] = 0;
     *issued_sh = 0;
     fence_mbar_init();
   }
+  if (GELU && threadIdx.x < 64) sel_table[threadIdx.x] = c_pair_select_table.e[threadIdx.x];
   if (threadIdx.x == 32) {
     prefetch_tmap(&a.tmA);
     prefetch_tmap(&a.tmB);
@@ -191,17 +239,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   // The set-up above may overlap the previous kernel; nothing below touches global memory before it is done.
   pdl_launch_dependents();
   pdl_wait();
+  if (a.zero && blockIdx.x == 0)  // the next kernel's arrival counters start at zero
+    for (int i = threadIdx.x; i < a.nzero; i += THREADS) a.zero[i] = 0u;
 
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ TMA producer (both CTAs)
       constexpr uint32_t STAGE_BYTES = C::STAGE;
-      constexpr uint32_t LORA_BYTES = C::A_SLOT + C::SUB;
+      constexpr uint32_t LORA_BYTES = MB * C::A_BOX + C::SUB;  // T' (one box per row block) and this CTA's LA half
       const uint32_t full_leader0 = mapa_shared(&full[0], 0);  // the leader's full barriers, 8 B apart
       int g = 0, st = 0;
       uint32_t ph = 0;
       bool stop = false;
-      for (int tile = cluster; tile < ntiles && !stop; tile += nclusters) {
+      for (int unit = cluster; unit < nunits && !stop; unit += nclusters) {
+        const int tile = unit % ntiles, ks = unit / ntiles;
+        const int kbeg = ks * nk / S, kend = (ks + 1) * nk / S;
+        const int nst_u = kend - kbeg + ((LORA && ks == S - 1) ? 1 : 0);
         const int mp = tile % num_mp, nb = tile / num_mp;
         const int m0 = mp * 2 * C::ROWS + static_cast<int>(rank) * C::ROWS;
         const int n0 = nb * TN + static_cast<int>(rank) * C::HALF_N;
@@ -212,7 +265,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           if (rb >= meta_rowblocks) rb = meta_rowblocks - 1;  // rows past the padded M: never stored
           meta_row[h] = static_cast<int>(2 * (rb * blocks_k));
         }
-        for (int it = 0; it < nstages; ++it) {
+        for (int it = 0; it < nst_u; ++it) {
+          const int kk = kbeg + it;
           if (!mbar_wait(&empty[st], ph ^ 1, a.ctl, SITE_PRODUCER) || *abort_flag) {
             *abort_flag = 1;
             stop = true;
@@ -222,18 +276,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           uint8_t* sB = sA + C::A_SLOT;
           const uint32_t fb = full_leader0 + 8 * st;
           if (!(a.ctl.inject == 1 && g == 0)) {  // test hook: the first stage never arrives
-            if (it < nk) {
+            if (kk < kend) {
               if (leader) mbar_arrive_expect_tx(&full[st], 2 * STAGE_BYTES);
 #pragma unroll
-              for (int h = 0; h < MB; ++h) tma_load_2d_pair(sA + h * C::A_BLOCK, &a.tmA, fb, it * 64, m0 + h * BLOCK);
+              for (int h = 0; h < MB; ++h)
+#pragma unroll
+                for (int j = 0; j < C::BOXES; ++j)  // sparse: 64 kept values per row = 128 channels
+                  tma_load_2d_pair(sA + h * C::A_BLOCK + j * C::A_BOX, &a.tmA, fb, kk * (SPARSE ? 64 : C::BK) + 64 * j,
+                                   m0 + h * BLOCK);
               if constexpr (SPARSE) {
-                tma_load_2d_pair(sB, &a.tmB, fb, it * 128, n0);
-                tma_load_2d_pair(sB + C::SUB, &a.tmB, fb, it * 128 + 64, n0);
+                tma_load_2d_pair(sB, &a.tmB, fb, kk * 128, n0);
+                tma_load_2d_pair(sB + C::SUB, &a.tmB, fb, kk * 128 + 64, n0);
 #pragma unroll
                 for (int h = 0; h < MB; ++h)
-                  tma_load_2d_pair(sB + C::B_SLOT + h * kMetaChunkBytes, &a.tmMeta, fb, 0, meta_row[h] + 2 * it);
+                  tma_load_2d_pair(sB + C::B_SLOT + h * kMetaChunkBytes, &a.tmMeta, fb, 0, meta_row[h] + 2 * kk);
               } else {
-                tma_load_2d_pair(sB, &a.tmB, fb, it * 64, n0);
+#pragma unroll
+                for (int j = 0; j < C::BOXES; ++j) tma_load_2d_pair(sB + j * C::SUB, &a.tmB, fb, kk * C::BK + 64 * j, n0);
               }
             } else {
               if (leader) mbar_arrive_expect_tx(&full[st], 2 * LORA_BYTES);
@@ -261,6 +320,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       constexpr uint32_t IDESC_SP = idesc_bf16(2 * BLOCK, TN, true);
       constexpr uint64_t STEP = C::STAGE >> 4;    // descriptor start-address units per stage
       constexpr uint64_t ABLK = C::A_BLOCK >> 4;  // ... per row block of A
+      constexpr uint64_t ABOX = C::A_BOX >> 4;    // ... per 64-channel box of A
       constexpr uint64_t WSUB = C::SUB >> 4;      // ... per W sub-tile
       constexpr uint64_t MCHUNK = kMetaChunkBytes >> 4;
       const uint32_t s0 = smem_u32(smem);
@@ -268,16 +328,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const uint64_t b0 = sdesc(s0 + C::A_SLOT, 16, 1024, SWZ_128B);
       const uint64_t e0 = sdesc(s0 + C::A_SLOT + C::B_SLOT, 128, 128, SWZ_NONE);
       const uint32_t meta0 = tmem + C::META_COL;
-      int g = 0, st = 0, tcount = 0;
+      int g = 0, st = 0, tcount = 0, mring = 0;
       uint32_t ph = 0;
       bool stop = false;
-      for (int tile = cluster; tile < ntiles && !stop; tile += nclusters, ++tcount) {
-        if (!mbar_wait(acc_empty, (tcount & 1) ^ 1, a.ctl, SITE_MMA)) {
+      for (int unit = cluster; unit < nunits && !stop; unit += nclusters, ++tcount) {
+        const int ks = unit / ntiles;
+        const int kbeg = ks * nk / S, kend = (ks + 1) * nk / S;
+        const int nst_u = kend - kbeg + ((LORA && ks == S - 1) ? 1 : 0);
+        const int ab = tcount % C::ACC_BUFS;  // accumulator buffer of this unit
+        const uint32_t acc_base = tmem + ab * C::ACC_STRIDE;
+        if (!mbar_wait(&acc_empty[ab], ((tcount / C::ACC_BUFS) & 1) ^ 1, a.ctl, SITE_MMA)) {
           *abort_flag = 1;
           break;
         }
         tc_fence_after();
-        for (int it = 0; it < nstages; ++it) {
+        for (int it = 0; it < nst_u; ++it) {
           if (!mbar_wait(&full[st], ph, a.ctl, SITE_MMA)) {
             *abort_flag = 1;
             stop = true;
@@ -286,9 +351,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           tc_fence_after();
           const uint64_t ad = a0 + st * STEP, bd = b0 + st * STEP;
           const uint32_t acc0 = it != 0;
-          if (it < nk) {
+          if (kbeg + it < kend) {
             if constexpr (SPARSE) {
-              const uint32_t grp0 = meta0 + (it & (META_RING - 1)) * (MB * META_GROUP_COLS);
+              // metadata group of this stage: the ring rotates with every k-step this issuer runs
+              const uint32_t grp0 = meta0 + (mring++ & (META_RING - 1)) * (MB * META_GROUP_COLS);
 #pragma unroll
               for (int hh = 0; hh < MB / NISS; ++hh) {
                 const int h = k + hh * NISS;
@@ -299,7 +365,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 const int h = k + hh * NISS;
                 // MMA j: A bytes 32j of the 128-byte rows of row block h; W sub-tile j/2 at byte 64 (j%2);
                 // metadata column pair j/2 of row block h's group with selector j%2
-                const uint32_t d = tmem + h * TN, grp = grp0 + h * META_GROUP_COLS;
+                const uint32_t d = acc_base + h * TN, grp = grp0 + h * META_GROUP_COLS;
                 const uint64_t ah = ad + h * ABLK;
                 tc_mma_sp_pair(d, ah, bd, grp, IDESC_SP, acc0);
                 tc_mma_sp_pair(d, ah + 2, bd + 4, grp, IDESC_SP | 1u, 1);
@@ -310,19 +376,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 #pragma unroll
               for (int hh = 0; hh < MB / NISS; ++hh) {
                 const int h = k + hh * NISS;
-                const uint32_t d = tmem + h * TN;
+                const uint32_t d = acc_base + h * TN;
                 const uint64_t ah = ad + h * ABLK;
-                tc_mma_pair(d, ah, bd, IDESC, acc0);
-                tc_mma_pair(d, ah + 2, bd + 2, IDESC, 1);
-                tc_mma_pair(d, ah + 4, bd + 4, IDESC, 1);
-                tc_mma_pair(d, ah + 6, bd + 6, IDESC, 1);
+#pragma unroll
+                for (int j = 0; j < C::BOXES; ++j) {  // box j: A box j and W sub-tile j, four K = 16 steps
+                  tc_mma_pair(d, ah + j * ABOX, bd + j * WSUB, IDESC, acc0 | j);
+                  tc_mma_pair(d, ah + j * ABOX + 2, bd + j * WSUB + 2, IDESC, 1);
+                  tc_mma_pair(d, ah + j * ABOX + 4, bd + j * WSUB + 4, IDESC, 1);
+                  tc_mma_pair(d, ah + j * ABOX + 6, bd + j * WSUB + 6, IDESC, 1);
+                }
               }
             }
           } else {  // LoRA-up: T' (128 x 64 per row block) against this CTA's half of LA, four K = 16 steps
 #pragma unroll
             for (int hh = 0; hh < MB / NISS; ++hh) {
               const int h = k + hh * NISS;
-              const uint32_t d = tmem + h * TN;
+              const uint32_t d = acc_base + h * TN;
               const uint64_t ah = ad + h * ABLK;
               tc_mma_pair(d, ah, bd, IDESC, 1);
               tc_mma_pair(d, ah + 2, bd + 2, IDESC, 1);
@@ -337,7 +406,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             ph ^= 1;
           }
         }
-        if (!stop) tc_commit_pair(acc_full, 0x3);
+        if (!stop) tc_commit_pair(&acc_full[ab], 0x3);
       }
       consumed_sh[k] = g;
       tc_commit_pair(drain, 0x1);  // every MMA of both issuers has completed once this phase completes
@@ -360,16 +429,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const bool scaled = a.scale_mode == SCALE_MUL;
     const bool y_tma = a.y_tma != 0;
     uint8_t* ybuf = ystage + (warp - 2) * C::Y_BOXES * Y_BUF;
-    const uint32_t acc_empty_leader = mapa_shared(acc_empty, 0);
+    const uint32_t acc_empty_leader0 = mapa_shared(acc_empty, 0);  // the leader's acc_empty[0]; [1] is 8 B on
     const uint32_t taddr_warp = tmem + (static_cast<uint32_t>(q * 32) << 16) + h * TN + col_off;
-    int tcount = 0, ybox = 0;
-    for (int tile = cluster; tile < ntiles; tile += nclusters, ++tcount) {
+    const int m_pad = static_cast<int>(round_up(a.M, kMetaRowPad));  // GELU: metadata rows written
+    int tcount = 0, ybox = 0, nsplit = 0;
+    for (int unit = cluster; unit < nunits; unit += nclusters, ++tcount) {
+      const int tile = unit % ntiles, ks = unit / ntiles;
       const int mp = tile % num_mp, nb = tile / num_mp;
       const int row0 = mp * 2 * C::ROWS + static_cast<int>(rank) * C::ROWS + h * BLOCK + q * 32;
       const int row = row0 + lane;
       const int n0 = nb * TN + col_off;
       const float sc = (scaled && row < a.M) ? a.rowscale[row] : 1.f;  // issued before the wait
-      bool ok = mbar_wait(acc_full, tcount & 1, a.ctl, SITE_EPILOGUE);
+      const int ab = tcount % C::ACC_BUFS;
+      bool ok = mbar_wait(&acc_full[ab], (tcount / C::ACC_BUFS) & 1, a.ctl, SITE_EPILOGUE);
       ok = __all_sync(0xFFFFFFFFu, ok) && !*abort_flag;
       if (!ok) break;
       tc_fence_after();
@@ -425,36 +497,167 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           else store_chunk(yrow, col0, a.N, vec_ok, p);
         }
       };
+      // GELU epilogue: chunk c becomes h = bf16(GELU(y)) in place; with a.hvals its 8 groups of 4 columns are
+      // sparsified as the sparsify pass does (kept pairs to hvals, 16 bytes per row and chunk; the 32-bit
+      // metadata word of the row, whose 16-bit halves meet those of row r +- 8 -- lane ^ 8 -- in the tensor
+      // memory order of the chunk layout; squares of all and of the kept entries into the row's norm sums).
+      float hn_all = 0.f, hn_kept = 0.f;
+      auto finish_chunk = [&](int c) {
+        if constexpr (GELU) {
+          uint32_t* p = pk + c * 16;
 #pragma unroll
-      for (int c2 = 0; c2 < NC; c2 += 2) {
-        const bool two = c2 + 1 < NC;
-        uint32_t r0[32], r1[32];
-        tc_ld_32x32b_x32(taddr_warp + c2 * 32, r0);
-        if (two) tc_ld_32x32b_x32(taddr_warp + (c2 + 1) * 32, r1);
-        tc_wait_ld();
-        if (c2 + 2 >= NC) {
-          tc_fence_before();
-          __syncwarp();
-          // the pair's accumulators may be overwritten: this warp's TMEM reads have completed (wait::ld)
-          if (lane == 0) mbar_arrive_cluster_relaxed(acc_empty_leader);
-        }
+          for (int j = 0; j < 16; ++j) {
+            const float y0 = __uint_as_float(p[j] << 16), y1 = __uint_as_float(p[j] & 0xFFFF0000u);
+            __nv_bfloat162 hv = __floats2bfloat162_rn(gelu_f(y0), gelu_f(y1));
+            p[j] = *reinterpret_cast<uint32_t*>(&hv);
+          }
+          if (a.hvals) {
+            const int col0 = n0 + c * 32;
+            uint32_t kept[8], word = 0;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          __nv_bfloat162 v0 = __floats2bfloat162_rn(__uint_as_float(r0[2 * j]) * sc, __uint_as_float(r0[2 * j + 1]) * sc);
-          pk[c2 * 16 + j] = *reinterpret_cast<uint32_t*>(&v0);
-          if (two) {
-            __nv_bfloat162 v1 = __floats2bfloat162_rn(__uint_as_float(r1[2 * j]) * sc, __uint_as_float(r1[2 * j + 1]) * sc);
-            pk[(c2 + 1) * 16 + j] = *reinterpret_cast<uint32_t*>(&v1);
+            for (int g = 0; g < 8; ++g)
+              word |= select_group(p[2 * g], p[2 * g + 1], sel_table, kept[g], hn_all, hn_kept) << (4 * g);
+            if (live && col0 < a.N) {
+              uint4* dst = reinterpret_cast<uint4*>(a.hvals + static_cast<int64_t>(row) * (a.N / 2) + col0 / 2);
+              dst[0] = make_uint4(kept[0], kept[1], kept[2], kept[3]);
+              dst[1] = make_uint4(kept[4], kept[5], kept[6], kept[7]);
+            }
+            const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, word, 8);
+            const bool lowrow = (lane & 8) == 0;  // row % 16 < 8: the low halves' lane
+            const uint32_t mw = lowrow ? ((word & 0xFFFFu) | (other << 16)) : ((other >> 16) | (word & 0xFFFF0000u));
+            const int rr = row & (kMetaRows - 1);
+            const int tl = (rr >> 4) * 16 + (lowrow ? 0 : 8) + (rr & 7);
+            if (row < m_pad && col0 < a.N)
+              *reinterpret_cast<uint32_t*>(a.hmeta + (static_cast<int64_t>(row / kMetaRows) * (a.N / kMetaBlockCols) +
+                                                      col0 / kMetaBlockCols) * kMetaChunkBytes +
+                                           tl * 16 + ((col0 % kMetaBlockCols) / 32) * 4) = mw;
           }
         }
-        if (c2 < EARLY) write_chunk(c2);
-        if (c2 + 1 < EARLY) write_chunk(c2 + 1);
-      }
-      // Write-out of the rest, overlapping the next tile's main loop: one bulk group per chunk, the warp's
-      // staging boxes used in turn over the whole tile sequence.
+        write_chunk(c);
+      };
+      if constexpr (!SPLIT) {
 #pragma unroll
-      for (int c = EARLY; c < NC; ++c) write_chunk(c);
-      ybox += NC;
+        for (int c2 = 0; c2 < NC; c2 += 2) {
+          const bool two = c2 + 1 < NC;
+          uint32_t r0[32], r1[32];
+          tc_ld_32x32b_x32(taddr_warp + ab * C::ACC_STRIDE + c2 * 32, r0);
+          if (two) tc_ld_32x32b_x32(taddr_warp + ab * C::ACC_STRIDE + (c2 + 1) * 32, r1);
+          tc_wait_ld();
+          if (c2 + 2 >= NC) {
+            tc_fence_before();
+            __syncwarp();
+            // the pair's accumulators may be overwritten: this warp's TMEM reads have completed (wait::ld)
+            if (lane == 0) mbar_arrive_cluster_relaxed(acc_empty_leader0 + 8 * ab);
+          }
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            __nv_bfloat162 v0 = __floats2bfloat162_rn(__uint_as_float(r0[2 * j]) * sc, __uint_as_float(r0[2 * j + 1]) * sc);
+            pk[c2 * 16 + j] = *reinterpret_cast<uint32_t*>(&v0);
+            if (two) {
+              __nv_bfloat162 v1 = __floats2bfloat162_rn(__uint_as_float(r1[2 * j]) * sc, __uint_as_float(r1[2 * j + 1]) * sc);
+              pk[(c2 + 1) * 16 + j] = *reinterpret_cast<uint32_t*>(&v1);
+            }
+          }
+          if (c2 < EARLY) finish_chunk(c2);
+          if (c2 + 1 < EARLY) finish_chunk(c2 + 1);
+        }
+        // Write-out of the rest, overlapping the next tile's main loop: one bulk group per chunk, the warp's
+        // staging boxes used in turn over the whole tile sequence.
+#pragma unroll
+        for (int c = EARLY; c < NC; ++c) finish_chunk(c);
+        ybox += NC;
+        if constexpr (GELU) {
+          if (a.hvals && live) a.hnorm[static_cast<int64_t>(row) * a.hnorm_slots + n0 / COLS] = make_float2(hn_all, hn_kept);
+        }
+      } else {
+        // Split K: this unit's fp32 partial (this CTA's rows of the tile) goes to global memory, laid out as
+        // [tile][split][CTA of the pair][ROWS][TN].  Each lane writes its row's 32-column chunks (128 bytes).
+        const int64_t tile_elems = static_cast<int64_t>(C::ROWS) * TN;
+        const int64_t prow = static_cast<int64_t>(h * BLOCK + q * 32 + lane) * TN + col_off;
+        float* mine = a.partials + ((static_cast<int64_t>(tile) * S + ks) * 2 + rank) * tile_elems + prow;
+#pragma unroll
+        for (int c2 = 0; c2 < NC; c2 += 2) {
+          const bool two = c2 + 1 < NC;
+          uint32_t r0[32], r1[32];
+          tc_ld_32x32b_x32(taddr_warp + ab * C::ACC_STRIDE + c2 * 32, r0);
+          if (two) tc_ld_32x32b_x32(taddr_warp + ab * C::ACC_STRIDE + (c2 + 1) * 32, r1);
+          tc_wait_ld();
+          if (c2 + 2 >= NC) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster_relaxed(acc_empty_leader0 + 8 * ab);
+          }
+          float4* d0 = reinterpret_cast<float4*>(mine + c2 * 32);
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            d0[v] = make_float4(__uint_as_float(r0[4 * v]), __uint_as_float(r0[4 * v + 1]),
+                                __uint_as_float(r0[4 * v + 2]), __uint_as_float(r0[4 * v + 3]));
+          if (two) {
+            float4* d1 = reinterpret_cast<float4*>(mine + (c2 + 1) * 32);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              d1[v] = make_float4(__uint_as_float(r1[4 * v]), __uint_as_float(r1[4 * v + 1]),
+                                  __uint_as_float(r1[4 * v + 2]), __uint_as_float(r1[4 * v + 3]));
+          }
+        }
+        // Publish: every epilogue warp's partial is written (fence, then one arrival per warp); one thread
+        // takes the tile's arrival ticket.  The unit that draws the last ticket adds the S partials in split
+        // order -- the same order whichever unit finishes last, so the result does not depend on timing --
+        // and writes Y.  No unit waits for another: the others go on to their next unit.
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(epi_bar);
+        ok = mbar_wait(epi_bar, nsplit & 1, a.ctl, SITE_EPILOGUE);
+        if (ok && warp == 2 && lane == 0) {
+          unsigned int ticket;
+          asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                       : "=r"(ticket)
+                       : "l"(a.counters + 2 * tile + static_cast<int>(rank))
+                       : "memory");
+          *last_flag = ticket == static_cast<unsigned int>(S - 1);
+          mbar_arrive(epi_bar2);
+        }
+        ok = ok && mbar_wait(epi_bar2, nsplit & 1, a.ctl, SITE_EPILOGUE);
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        ++nsplit;
+        if (!ok) break;
+        if (*last_flag) {
+          __threadfence();
+          const float* base = a.partials + (static_cast<int64_t>(tile) * S * 2 + rank) * tile_elems + prow;
+#pragma unroll
+          for (int c = 0; c < NC; ++c) {
+            float acc[32];
+            // four columns at a time: every split's load is issued before the group is added in split order
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              float4 t[kPairMaxSplit];
+#pragma unroll
+              for (int s2 = 0; s2 < kPairMaxSplit; ++s2)
+                if (s2 < S) t[s2] = __ldcg(reinterpret_cast<const float4*>(base + s2 * 2 * tile_elems + c * 32) + v);
+              float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+              for (int s2 = 0; s2 < kPairMaxSplit; ++s2)
+                if (s2 < S) {
+                  sum.x += t[s2].x;
+                  sum.y += t[s2].y;
+                  sum.z += t[s2].z;
+                  sum.w += t[s2].w;
+                }
+              acc[4 * v] = sum.x;
+              acc[4 * v + 1] = sum.y;
+              acc[4 * v + 2] = sum.z;
+              acc[4 * v + 3] = sum.w;
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              __nv_bfloat162 v0 = __floats2bfloat162_rn(acc[2 * j] * sc, acc[2 * j + 1] * sc);
+              pk[c * 16 + j] = *reinterpret_cast<uint32_t*>(&v0);
+            }
+            write_chunk(c);
+          }
+          ybox += NC;
+        }
+      }
     }
     if (y_tma && lane == 0) bulk_wait_all();
   }
@@ -479,23 +682,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   }
 }
 
-template <bool SPARSE, bool LORA, int MB, int TN, bool TRANS = false>
+template <bool SPARSE, bool LORA, int MB, int TN, bool TRANS = false, bool SPLIT = false, bool GELU = false>
 cudaError_t launch(const PairArgs& a, cudaStream_t st) {
   using C = PairCfg<SPARSE, MB, TN>;
-  auto* k = gemm_pair_kernel<SPARSE, LORA, MB, TN, TRANS>;
+  auto* k = gemm_pair_kernel<SPARSE, LORA, MB, TN, TRANS, SPLIT, GELU>;
+  constexpr int smem = C::SMEM + (GELU ? 256 : 0);  // + the selection table
+  static_assert(smem <= SMEM_LIMIT, "shared memory budget");
   static std::atomic<bool> attr_set[64] = {};  // per device; setting it twice from racing threads is harmless
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   const int ntiles = ((a.M + 2 * C::ROWS - 1) / (2 * C::ROWS)) * ((a.N + TN - 1) / TN);
+  const int nunits = ntiles * (SPLIT ? a.splits : 1);
   int clusters = sm_count() / 2;
-  if (clusters > ntiles) clusters = ntiles;
+  if (clusters > nunits) clusters = nunits;
   if (clusters < 1) clusters = 1;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -503,7 +709,7 @@ cudaError_t launch(const PairArgs& a, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(2 * clusters);  // the cluster shape (2, 1, 1) is the kernel's own attribute
   cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
@@ -514,9 +720,10 @@ cudaError_t launch(const PairArgs& a, cudaStream_t st) {
 
 // Shared-memory traffic per thousand logical MACs of each sparse shape (TMA fill plus tensor-core operand
 // reads, the kernel's binding resource): 512 x 224 tiles 21.3 B, 512 x 192 tiles 22.9 B, 256 x 256 tiles
-// 23.8 B.  The shape with the smallest (tile waves x tile work x traffic) wins: 512 x 224 for the large DiT
-// QKV and MLP-up shapes, 512 x 192 where 224-wide column tiles would add a wave (N = 3072), 256 x 256 when few
-// row tiles would leave pairs idle (e.g. M = 1024).
+// 23.8 B, 256 x 192 tiles 26.7 B.  The shape with the smallest (tile waves x tile work x traffic) wins: 512 x 224
+// for the large DiT QKV and MLP-up shapes, 512 x 192 where 224-wide column tiles would add a wave (N = 3072),
+// 256 x 256 when few row tiles would leave pairs idle (e.g. M = 1024, N = 9216), 256 x 192 when narrower tiles
+// keep a short problem inside one wave (e.g. M = 1024, N = 3072: 64 tiles for 76 CTA pairs).
 PairShape pair_shape(bool sparse, int M, int N) {
   if (!sparse) return {1, 256};
   const int64_t clusters = sm_count() / 2 > 0 ? sm_count() / 2 : 1;
@@ -525,11 +732,11 @@ PairShape pair_shape(bool sparse, int M, int N) {
     const int64_t waves = (tiles + clusters - 1) / clusters;
     return static_cast<double>(waves) * 256.0 * rb * tn * bytes_per_kmac;
   };
-  const PairShape cand[3] = {{2, 224}, {2, 192}, {1, 256}};
-  const double bytes[3] = {21.3, 22.9, 23.8};
+  const PairShape cand[4] = {{2, 224}, {2, 192}, {1, 256}, {1, 192}};
+  const double bytes[4] = {21.3, 22.9, 23.8, 26.7};
   int best = 0;
   double best_cost = cost(cand[0].rb, cand[0].tn, bytes[0]);
-  for (int i = 1; i < 3; ++i) {
+  for (int i = 1; i < 4; ++i) {
     const double c = cost(cand[i].rb, cand[i].tn, bytes[i]);
     if (c < best_cost) {
       best = i;
@@ -541,16 +748,41 @@ PairShape pair_shape(bool sparse, int M, int N) {
 
 bool pair_shape_valid(bool sparse, PairShape shape) {
   if (!sparse) return shape.rb == 1 && shape.tn == 256;
-  return (shape.rb == 2 && (shape.tn == 224 || shape.tn == 192)) || (shape.rb == 1 && shape.tn == 256);
+  return (shape.rb == 2 && (shape.tn == 224 || shape.tn == 192)) || (shape.rb == 1 && (shape.tn == 256 || shape.tn == 192));
 }
 
-cudaError_t launch_gemm_pair(bool sparse, bool lora, PairShape shape, const PairArgs& a, cudaStream_t st) {
+int gelu_norm_slots(bool sparse, PairShape shape, int N) {
+  const int cols = shape.rb == 2 ? shape.tn : shape.tn / 2;  // columns of one epilogue warp
+  (void)sparse;
+  return ((N + shape.tn - 1) / shape.tn) * (shape.tn / cols);
+}
+
+cudaError_t launch_gemm_pair(bool sparse, bool lora, PairShape shape, const PairArgs& a, cudaStream_t st,
+                             bool gelu) {
   if (!pair_shape_valid(sparse, shape)) return cudaErrorInvalidValue;
+  if (gelu) {  // the MLP up layer: sparse with LoRA, or dense
+    if (!sparse)
+      return lora ? launch<false, true, 1, 256, false, false, true>(a, st)
+                  : launch<false, false, 1, 256, false, false, true>(a, st);
+    if (!lora) return cudaErrorInvalidValue;
+    if (shape.rb == 2 && shape.tn == 224) return launch<true, true, 2, 224, false, false, true>(a, st);
+    if (shape.rb == 2) return launch<true, true, 2, 192, false, false, true>(a, st);
+    if (shape.tn == 192) return launch<true, true, 1, 192, false, false, true>(a, st);
+    return launch<true, true, 1, 256, false, false, true>(a, st);
+  }
   if (!sparse) return lora ? launch<false, true, 1, 256>(a, st) : launch<false, false, 1, 256>(a, st);
   if (shape.rb == 2 && shape.tn == 224)
     return lora ? launch<true, true, 2, 224>(a, st) : launch<true, false, 2, 224>(a, st);
   if (shape.rb == 2)
     return lora ? launch<true, true, 2, 192>(a, st) : launch<true, false, 2, 192>(a, st);
+  // split K: the one-row-block tiles only (the shapes few-tile problems take)
+  if (shape.tn == 192) {
+    if (a.splits > 1)
+      return lora ? launch<true, true, 1, 192, false, true>(a, st) : launch<true, false, 1, 192, false, true>(a, st);
+    return lora ? launch<true, true, 1, 192>(a, st) : launch<true, false, 1, 192>(a, st);
+  }
+  if (a.splits > 1)
+    return lora ? launch<true, true, 1, 256, false, true>(a, st) : launch<true, false, 1, 256, false, true>(a, st);
   return lora ? launch<true, true, 1, 256>(a, st) : launch<true, false, 1, 256>(a, st);
 }
 
@@ -560,6 +792,7 @@ cudaError_t launch_gemm_pair_transposed(bool lora, PairShape shape, const PairAr
     return lora ? launch<true, true, 2, 224, true>(a, st) : launch<true, false, 2, 224, true>(a, st);
   if (shape.rb == 2)
     return lora ? launch<true, true, 2, 192, true>(a, st) : launch<true, false, 2, 192, true>(a, st);
+  if (shape.tn == 192) return lora ? launch<true, true, 1, 192, true>(a, st) : launch<true, false, 1, 192, true>(a, st);
   return lora ? launch<true, true, 1, 256, true>(a, st) : launch<true, false, 1, 256, true>(a, st);
 }
 

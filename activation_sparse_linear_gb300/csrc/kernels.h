@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include "ptx.cuh"
+#include "../../include/lynx.h"
 
 namespace lynx {
 
@@ -51,10 +52,12 @@ constexpr int kMaxPrologueSplit = 16;  // CTAs (one cluster) per row block; 16 i
 struct ProArgs {
   CUtensorMap tmX;   // X (M x K bf16), box 64 x 128, 128-byte swizzle
   CUtensorMap tmLB;  // LB (64 x K bf16), box 64 x 64, 128-byte swizzle (LoRA branch only)
-  CUtensorMap tmV;   // compressed values (M x K/2 bf16), box 64 x 128, 128-byte swizzle (TMA store)
+  uint16_t* vals;    // compressed values, M x K/2 bf16 (row-major)
   uint8_t* meta;     // metadata chunks (layout above)
   float* s;          // s = sqrt(sum x^2 / sum kept x^2) (1 for an all-zero row), M floats
   void* T;           // LoRA: T' = (X LB^T) / s, M x 64 bf16
+  unsigned int* zero;  // words set to 0 before anything else (the next GEMM's split-K counters), or NULL
+  int nzero;
   int M, K, M_pad, split, nkb;  // M_pad = round_up(M, 256); split = cluster size; nkb = 128-channel blocks
   DevCtl ctl;
 };
@@ -99,14 +102,50 @@ struct PairArgs {
   void* Y;
   int64_t ldy;
   int M, N, K;
+  int splits;              // k-splits per tile (1: none); > 1 needs partials and counters
+  float* partials;         // fp32 partial tiles, [tile][split][CTA][rows][TN] (splits > 1)
+  unsigned int* counters;  // one arrival counter per (tile, CTA), zero on entry (splits > 1)
+  // GELU epilogue (the MLP up layer): Y = bf16(GELU(bf16(y))); with hvals non-NULL the epilogue also writes the
+  // 2:4 sparsification of that output for the next layer: compressed values (M x N/2 bf16), metadata chunks
+  // (lynx_meta_bytes(M, N), N % 128 == 0) and, per row and per 32 x (columns of one epilogue warp) slot, the
+  // fp32 pair (sum h^2, sum kept h^2).
+  uint16_t* hvals;
+  uint8_t* hmeta;
+  float2* hnorm;
+  int hnorm_slots;         // slots per row
+  unsigned int* zero;      // words set to 0 once the previous kernel is done (the next kernel's counters), or NULL
+  int nzero;
   DevCtl ctl;
 };
 
-// The CTA-pair (cta_group::2) GEMM with the given tile shape (one of those pair_shape returns).
-cudaError_t launch_gemm_pair(bool sparse, bool lora, PairShape shape, const PairArgs& a, cudaStream_t st);
+// The CTA-pair (cta_group::2) GEMM with the given tile shape (one of those pair_shape returns); gelu selects the
+// GELU epilogue (sparse tiles with LoRA, and the dense tile).
+cudaError_t launch_gemm_pair(bool sparse, bool lora, PairShape shape, const PairArgs& a, cudaStream_t st,
+                             bool gelu = false);
+// Norm-partial slots per row of the GELU epilogue for an output of N columns with this tile shape.
+int gelu_norm_slots(bool sparse, PairShape shape, int N);
 // The sparse pair GEMM whose accumulator tile is the transpose of Y: a.M and a.N count the accumulator's rows
 // and columns (Y's columns and rows), tmY and ldy describe Y itself (rows of ldy elements).
 cudaError_t launch_gemm_pair_transposed(bool lora, PairShape shape, const PairArgs& a, cudaStream_t st);
+
+// LoRA down-projection and row scale of a sparse layer whose input H was sparsified by the previous layer's
+// GELU epilogue (lora_fin.cu): T' = bf16(H LB^T / s), s from the epilogue's norm partials.
+struct FinArgs {
+  CUtensorMap tmH;         // H (M x K bf16), box 64 x 128, 128-byte swizzle
+  CUtensorMap tmLB;        // LB (64 x K bf16), box 64 x 64, 128-byte swizzle
+  const float2* hnorm;     // (sum h^2, sum kept h^2) per row and slot, slots per row
+  int slots;
+  float* s;                // out: M fp32
+  void* T;                 // out: M x 64 bf16
+  float* partials;         // splits > 1: fp32 partials [tile][split][128][64]
+  unsigned int* counters;  // splits > 1: one arrival counter per 128-row tile, zero on entry
+  int M, K, splits;
+  DevCtl ctl;
+};
+int lora_fin_splits(int M, int K);
+size_t lora_fin_partial_bytes(int M, int splits);
+int lora_fin_counters(int M);
+cudaError_t launch_lora_fin(const FinArgs& a, cudaStream_t st);
 
 int sm_count();
 
@@ -118,5 +157,15 @@ int dense_arg_status(const void* X, const void* W, const void* LA, const void* L
                      int64_t N, int64_t K, int64_t R, const void* workspace, size_t workspace_bytes);
 // Drops this thread's pending stage-timing request (lynx_profile_next), so that a graph capture records none.
 void clear_stage_request();
+
+// Layer sequences (lynx_api.cu, used by layers.cu): the status the sequence would return before launching (the
+// failing index in *failed), its workspace bytes, and its launches.  A layer with the GELU flag followed by a
+// sparse layer that reads its output runs as one fused pair when the workspace holds the pair's plan.
+int seq_status(const lynx_layer* layers, int32_t n, const void* ws, size_t ws_bytes, int32_t* failed);
+size_t seq_workspace_bytes(const lynx_layer* layers, int32_t n);
+int seq_enqueue(const lynx_layer* layers, int32_t n, void* ws, size_t ws_bytes, cudaStream_t st);
+// Byte offsets in the workspace of the fused pair (i, i + 1): the down layer's values, metadata, s, T', and the
+// pair's total workspace bytes (out[0..4]); LYNX_ERR_UNSUPPORTED when the two layers do not fuse.
+int seq_pair_offsets(const lynx_layer* layers, int32_t n, int32_t i, size_t* out);
 
 }  // namespace lynx

@@ -27,6 +27,8 @@ __device__ int g_error_word;
 std::atomic<int> g_inject{0};
 std::atomic<int> g_force_tile{0};  // 0: tile shape by problem shape; else a forced shape, rb << 16 | tn
 std::atomic<int> g_force_split{0};  // 0: pre-pass cluster size by occupancy; else a forced size
+std::atomic<int> g_force_ksplit{0};  // 0: GEMM k-splits by tile count; else a forced count (one-row-block tiles)
+constexpr int kMaxKSplit = 4;
 thread_local void* const* t_prof_events = nullptr;
 thread_local int t_prof_count = 0;
 
@@ -152,6 +154,46 @@ Workspace carve(void* base, int64_t M, int64_t K, int64_t R) {
   return w;
 }
 
+// k-splits of the sparse GEMM: only the one-row-block tiles (the ones few-tile problems take) split, and only
+// when their tiles leave more than half of the CTA pairs idle; the split count (2-4, at least 8 k-steps per
+// unit) that fills the waves best wins.  A forced count (test hook) is clamped to the k-steps.
+int ksplit_for(PairShape shape, int64_t M, int64_t N, int64_t K) {
+  if (shape.rb != 1) return 1;
+  const int64_t nk = (K + 127) / 128;
+  const int forced = g_force_ksplit.load();
+  if (forced) return static_cast<int>(forced < nk ? forced : nk);
+  const int64_t clusters = sm_count() / 2;
+  if (clusters < 4) return 1;
+  const int64_t tiles = ((M + 255) / 256) * ((N + shape.tn - 1) / shape.tn);
+  if (2 * tiles > clusters) return 1;
+  int best = 1;
+  double best_eff = static_cast<double>(tiles) / static_cast<double>(clusters);
+  for (int sp = 2; sp <= kMaxKSplit && nk >= 8 * sp; ++sp) {
+    const int64_t units = tiles * sp, waves = (units + clusters - 1) / clusters;
+    const double eff = static_cast<double>(units) / static_cast<double>(waves * clusters);
+    if (eff > best_eff + 0.05) {
+      best = sp;
+      best_eff = eff;
+    }
+  }
+  return best;
+}
+
+// Bytes of the split-K region for `splits` (0 for 1): fp32 partial tiles [tile][split][CTA][128 rb][tn], then one
+// arrival counter per (tile, CTA), each part 256-byte aligned.
+size_t split_bytes(PairShape shape, int64_t M, int64_t N, int splits, size_t* counters_off = nullptr) {
+  if (splits <= 1) return 0;
+  const int64_t tiles = ((M + 256 * shape.rb - 1) / (256 * shape.rb)) * ((N + shape.tn - 1) / shape.tn);
+  const size_t partials = align256(static_cast<size_t>(tiles) * splits * 2 * 128 * shape.rb * shape.tn * 4);
+  if (counters_off) *counters_off = partials;
+  return partials + align256(static_cast<size_t>(tiles) * 2 * 4);
+}
+
+PairShape sparse_shape(int64_t M, int64_t N) {
+  const int forced = g_force_tile.load();
+  return forced ? PairShape{forced >> 16, forced & 0xFFFF} : pair_shape(true, static_cast<int>(M), static_cast<int>(N));
+}
+
 // T = X LB^T [/ s] on the 64-wide tcgen05 tile (standalone down-projection and the dense path).
 int run_lora_down(const void* X, const void* LB, const float* s, void* T, int64_t M, int64_t K, cudaStream_t st) {
   GemmArgs g;
@@ -174,9 +216,9 @@ int make_prologue(ProArgs* pa, const void* X, const void* LB, int64_t M, int64_t
                   void* T) {
   std::memset(pa, 0, sizeof(*pa));
   if (!make_map(&pa->tmX, X, K, M, K, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&pa->tmV, vals, K / 2, M, K / 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
       (LB && !make_map(&pa->tmLB, LB, K, kRank, K, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)))
     return LYNX_ERR_CUDA;
+  pa->vals = static_cast<uint16_t*>(vals);
   pa->meta = static_cast<uint8_t*>(meta);
   pa->s = s;
   pa->T = T;
@@ -186,6 +228,8 @@ int make_prologue(ProArgs* pa, const void* X, const void* LB, int64_t M, int64_t
   pa->nkb = static_cast<int>(meta_blocks_k(K));
   const int forced = g_force_split.load();
   pa->split = forced ? (forced < pa->nkb ? forced : pa->nkb) : prologue_split(pa->M, pa->K);
+  pa->zero = nullptr;
+  pa->nzero = 0;
   pa->ctl = make_ctl();
   return LYNX_OK;
 }
@@ -225,6 +269,296 @@ void clear_stage_request() {
   t_prof_count = 0;
 }
 
+namespace {
+
+// The GELU epilogue's sparsified output for the next layer (hvals NULL: none) and the words it zeroes.
+struct FuseOut {
+  uint16_t* hvals = nullptr;
+  uint8_t* hmeta = nullptr;
+  float2* hnorm = nullptr;
+  int slots = 0;
+  unsigned int* zero = nullptr;
+  int nzero = 0;
+};
+
+void set_fuse(PairArgs* g, const FuseOut* fo) {
+  if (!fo) return;
+  g->hvals = fo->hvals;
+  g->hmeta = fo->hmeta;
+  g->hnorm = fo->hnorm;
+  g->hnorm_slots = fo->slots;
+  g->zero = fo->zero;
+  g->nzero = fo->nzero;
+}
+
+// Arguments of the sparse pair GEMM over compressed values / metadata / s / T' of an M x K activation.
+int sparse_gemm_args(PairArgs* g, const void* vals, const void* meta, const float* s, const void* T, const void* W,
+                     const void* LA, void* Y, int64_t M, int64_t N, int64_t K, int64_t R, PairShape shape) {
+  std::memset(g, 0, sizeof(*g));
+  const uint64_t meta_rows = 2 * static_cast<uint64_t>(meta_bytes(M, K) / kMetaChunkBytes);  // 1 KiB rows
+  if (!make_map(&g->tmA, vals, K / 2, M, K / 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&g->tmB, W, K, N, K, 64, shape.tn / 2, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&g->tmMeta, meta, 256, meta_rows, 256, 256, 2, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_DATA_TYPE_UINT32) ||
+      !make_map(&g->tmT, T, R, M, R, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&g->tmLA, LA, R, N, R, 64, shape.tn / 2, CU_TENSOR_MAP_SWIZZLE_128B))
+    return LYNX_ERR_CUDA;
+  if (!set_y_map(g, Y, M, N)) return LYNX_ERR_CUDA;
+  g->rowscale = s;
+  g->scale_mode = SCALE_MUL;
+  g->Y = Y;
+  g->ldy = N;
+  g->M = static_cast<int>(M);
+  g->N = static_cast<int>(N);
+  g->K = static_cast<int>(K);
+  g->splits = 1;
+  g->ctl = make_ctl();
+  return LYNX_OK;
+}
+
+// lynx_linear after its argument checks; gelu: the GELU epilogue, with fo its sparsified output (no split K).
+int linear_impl(const void* X, const void* W, const void* LA, const void* LB, void* Y, int64_t M, int64_t N, int64_t K,
+                int64_t R, void* workspace, size_t workspace_bytes, cudaStream_t st, bool gelu, const FuseOut* fo,
+                const StageEvents& prof) {
+  Workspace ws = carve(workspace, M, K, R);
+  const PairShape shape = sparse_shape(M, N);
+  PairArgs g;
+  if (int e = sparse_gemm_args(&g, ws.vals, ws.meta, ws.s, ws.T, W, LA, Y, M, N, K, R, shape)) return e;
+  // split K when the workspace holds the partials (else the unsplit schedule, which needs only the base part)
+  int splits = gelu ? 1 : ksplit_for(shape, M, N, K);
+  size_t counters_off = 0;
+  if (splits > 1 && workspace_bytes < ws.bytes + split_bytes(shape, M, N, splits, &counters_off)) splits = 1;
+  g.splits = splits;
+  if (splits > 1) {
+    g.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + ws.bytes);
+    g.counters = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(workspace) + ws.bytes + counters_off);
+  }
+  set_fuse(&g, fo);
+
+  ProArgs pa;
+  if (int e = make_prologue(&pa, X, LB, M, K, ws.vals, ws.meta, ws.s, ws.T)) return e;
+  if (splits > 1) {  // the pre-pass zeroes the GEMM's arrival counters
+    pa.zero = g.counters;
+    pa.nzero = static_cast<int>(((M + 255) / 256) * ((N + shape.tn - 1) / shape.tn) * 2);
+  }
+  if (cudaError_t e = prof.mark(0, st)) return cuda_status(e);
+  if (cudaError_t e = launch_prologue(pa, true, st)) return cuda_status(e);
+  if (cudaError_t e = prof.mark(1, st)) return cuda_status(e);
+  if (cudaError_t e = launch_gemm_pair(true, true, shape, g, st, gelu)) return cuda_status(e);
+  return cuda_status(prof.mark(2, st));
+}
+
+// lynx_linear_dense after its argument checks (gelu, fo as for linear_impl).
+int dense_impl(const void* X, const void* W, const void* LA, const void* LB, void* Y, int64_t M, int64_t N, int64_t K,
+               int64_t R, void* workspace, cudaStream_t st, bool gelu, const FuseOut* fo, const StageEvents& prof) {
+  const bool lora = LA || LB;
+  PairArgs g;
+  std::memset(&g, 0, sizeof(g));
+  if (!make_map(&g.tmA, X, K, M, K, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&g.tmB, W, K, N, K, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+    return LYNX_ERR_CUDA;
+  if (lora) {
+    if (!make_map(&g.tmT, workspace, R, M, R, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&g.tmLA, LA, R, N, R, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+      return LYNX_ERR_CUDA;
+  }
+  if (!set_y_map(&g, Y, M, N)) return LYNX_ERR_CUDA;
+  g.rowscale = nullptr;
+  g.scale_mode = SCALE_NONE;
+  g.Y = Y;
+  g.ldy = N;
+  g.M = static_cast<int>(M);
+  g.N = static_cast<int>(N);
+  g.K = static_cast<int>(K);
+  g.splits = 1;
+  g.ctl = make_ctl();
+  set_fuse(&g, fo);
+  if (cudaError_t e = prof.mark(0, st)) return cuda_status(e);
+  if (lora) {
+    if (int e = run_lora_down(X, LB, nullptr, workspace, M, K, st)) return e;
+    if (cudaError_t e = prof.mark(1, st)) return cuda_status(e);
+    if (cudaError_t e = launch_gemm_pair(false, true, PairShape{1, 256}, g, st, gelu)) return cuda_status(e);
+    return cuda_status(prof.mark(2, st));
+  }
+  if (cudaError_t e = launch_gemm_pair(false, false, PairShape{1, 256}, g, st, gelu)) return cuda_status(e);
+  return cuda_status(prof.mark(1, st));
+}
+
+// ---------------------------------------------------------------- layer sequences and the fused MLP pair
+constexpr int32_t kKnownFlags = LYNX_LAYER_SPARSE | LYNX_LAYER_GELU;
+
+bool is_sparse(const lynx_layer& l) { return (l.flags & LYNX_LAYER_SPARSE) != 0; }
+bool is_gelu(const lynx_layer& l) { return (l.flags & LYNX_LAYER_GELU) != 0; }
+
+size_t single_workspace_bytes(const lynx_layer& l) {
+  if (is_sparse(l)) return is_gelu(l) ? carve(nullptr, l.M, l.K, l.R).bytes : lynx_workspace_bytes(l.M, l.N, l.K, l.R);
+  return (l.LA || l.LB) ? lynx_dense_workspace_bytes(l.M, l.R) : 0;
+}
+
+int single_status(const lynx_layer& l, const void* ws, size_t ws_bytes) {
+  if (l.flags & ~kKnownFlags) return LYNX_ERR_UNSUPPORTED;
+  return is_sparse(l) ? linear_arg_status(l.X, l.W, l.LA, l.LB, l.Y, l.M, l.N, l.K, l.R, ws, ws_bytes)
+                      : dense_arg_status(l.X, l.W, l.LA, l.LB, l.Y, l.M, l.N, l.K, l.R, ws, ws_bytes);
+}
+
+// Workspace plan of a fused pair (up = the GELU layer, dn = the sparse layer reading its output): the up layer's
+// own part first, then the down layer's values, metadata, s and T', the norm partials, the LoRA pass's partials,
+// one block of counters (the LoRA pass's, then the down GEMM's) that the up GEMM zeroes, and the down GEMM's
+// split-K partials.
+struct PairPlan {
+  PairShape up_shape{1, 256}, dn_shape{1, 256};
+  int slots = 0, fin_splits = 1, dn_splits = 1, fin_counters = 0, dn_counters = 0;
+  size_t up_bytes = 0, dn_off = 0, hnorm_off = 0, fin_off = 0, cnt_off = 0, dsplit_off = 0, total = 0;
+};
+
+bool fusable(const lynx_layer& up, const lynx_layer& dn) {
+  return is_gelu(up) && is_sparse(dn) && !is_gelu(dn) && dn.X == up.Y && dn.M == up.M && dn.K == up.N &&
+         up.N % kMetaBlockCols == 0 && !(up.flags & ~kKnownFlags) && !(dn.flags & ~kKnownFlags);
+}
+
+PairPlan plan_pair(const lynx_layer& up, const lynx_layer& dn) {
+  PairPlan p;
+  const int64_t M = up.M;
+  p.up_shape = is_sparse(up) ? sparse_shape(M, up.N) : PairShape{1, 256};
+  p.up_bytes = is_sparse(up) ? carve(nullptr, M, up.K, up.R).bytes
+                             : ((up.LA || up.LB) ? lynx_dense_workspace_bytes(M, up.R) : 0);
+  p.slots = gelu_norm_slots(is_sparse(up), p.up_shape, static_cast<int>(up.N));
+  p.fin_splits = lora_fin_splits(static_cast<int>(M), static_cast<int>(dn.K));
+  p.dn_shape = sparse_shape(M, dn.N);
+  p.dn_splits = ksplit_for(p.dn_shape, M, dn.N, dn.K);
+  p.fin_counters = p.fin_splits > 1 ? lora_fin_counters(static_cast<int>(M)) : 0;
+  size_t dn_cnt_off = 0;
+  const size_t dsplit = split_bytes(p.dn_shape, M, dn.N, p.dn_splits, &dn_cnt_off);
+  p.dn_counters = p.dn_splits > 1 ? static_cast<int>((dsplit - dn_cnt_off) / 4) : 0;
+  size_t off = align256(p.up_bytes);
+  p.dn_off = off;
+  off += carve(nullptr, M, dn.K, dn.R).bytes;
+  p.hnorm_off = off;
+  off += align256(static_cast<size_t>(M) * p.slots * sizeof(float2));
+  p.fin_off = off;
+  off += align256(lora_fin_partial_bytes(static_cast<int>(M), p.fin_splits));
+  p.cnt_off = off;
+  off += align256(static_cast<size_t>(p.fin_counters + p.dn_counters) * 4);
+  p.dsplit_off = off;
+  off += p.dn_splits > 1 ? dn_cnt_off : 0;  // the down GEMM's partials (its counters live in the block above)
+  p.total = off;
+  return p;
+}
+
+int run_pair(const lynx_layer& up, const lynx_layer& dn, const PairPlan& p, void* workspace, cudaStream_t st) {
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  const int64_t M = up.M;
+  Workspace dws = carve(base + p.dn_off, M, dn.K, dn.R);
+  unsigned int* counters = reinterpret_cast<unsigned int*>(base + p.cnt_off);
+  FuseOut fo;
+  fo.hvals = static_cast<uint16_t*>(dws.vals);
+  fo.hmeta = static_cast<uint8_t*>(dws.meta);
+  fo.hnorm = reinterpret_cast<float2*>(base + p.hnorm_off);
+  fo.slots = p.slots;
+  if (p.fin_counters + p.dn_counters > 0) {
+    fo.zero = counters;
+    fo.nzero = p.fin_counters + p.dn_counters;
+  }
+  const StageEvents none(-1);
+  const int e = is_sparse(up) ? linear_impl(up.X, up.W, up.LA, up.LB, up.Y, M, up.N, up.K, up.R, base, p.up_bytes, st,
+                                            true, &fo, none)
+                              : dense_impl(up.X, up.W, up.LA, up.LB, up.Y, M, up.N, up.K, up.R, base, st, true, &fo,
+                                           none);
+  if (e) return e;
+  // the down layer's LoRA down-projection over H = up.Y and its row scale, from the epilogue's norm partials
+  FinArgs f;
+  std::memset(&f, 0, sizeof(f));
+  if (!make_map(&f.tmH, dn.X, dn.K, M, dn.K, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&f.tmLB, dn.LB, dn.K, kRank, dn.K, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+    return LYNX_ERR_CUDA;
+  f.hnorm = fo.hnorm;
+  f.slots = p.slots;
+  f.s = dws.s;
+  f.T = dws.T;
+  f.partials = reinterpret_cast<float*>(base + p.fin_off);
+  f.counters = counters;
+  f.M = static_cast<int>(M);
+  f.K = static_cast<int>(dn.K);
+  f.splits = p.fin_splits;
+  f.ctl = make_ctl();
+  if (cudaError_t ce = launch_lora_fin(f, st)) return cuda_status(ce);
+  // the down layer's sparse GEMM on the values and metadata the up layer's epilogue wrote
+  PairArgs g;
+  if (int ge = sparse_gemm_args(&g, dws.vals, dws.meta, dws.s, dws.T, dn.W, dn.LA, dn.Y, M, dn.N, dn.K, dn.R,
+                                p.dn_shape))
+    return ge;
+  g.splits = p.dn_splits;
+  if (p.dn_splits > 1) {
+    g.partials = reinterpret_cast<float*>(base + p.dsplit_off);
+    g.counters = counters + p.fin_counters;
+  }
+  return cuda_status(launch_gemm_pair(true, true, p.dn_shape, g, st));
+}
+
+int run_single(const lynx_layer& l, void* ws, size_t ws_bytes, cudaStream_t st) {
+  const StageEvents none(-1);
+  if (is_sparse(l))
+    return linear_impl(l.X, l.W, l.LA, l.LB, l.Y, l.M, l.N, l.K, l.R, ws, ws_bytes, st, is_gelu(l), nullptr, none);
+  return dense_impl(l.X, l.W, l.LA, l.LB, l.Y, l.M, l.N, l.K, l.R, ws, st, is_gelu(l), nullptr, none);
+}
+
+}  // namespace
+
+int seq_status(const lynx_layer* layers, int32_t n, const void* ws, size_t ws_bytes, int32_t* failed) {
+  if (failed) *failed = -1;
+  if (n > 0 && !layers) return LYNX_ERR_NULL;
+  if (n < 0) return LYNX_ERR_SHAPE;
+  for (int32_t i = 0; i < n; ++i) {
+    if (int e = single_status(layers[i], ws, ws_bytes)) {
+      if (failed) *failed = i;
+      return e;
+    }
+  }
+  return LYNX_OK;
+}
+
+size_t seq_workspace_bytes(const lynx_layer* layers, int32_t n) {
+  if (!layers || n < 1) return 0;
+  size_t b = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    size_t w = single_workspace_bytes(layers[i]);
+    if (i + 1 < n && fusable(layers[i], layers[i + 1])) {
+      const size_t f = plan_pair(layers[i], layers[i + 1]).total;
+      if (f > w) w = f;
+    }
+    if (w > b) b = w;
+  }
+  return b;
+}
+
+int seq_pair_offsets(const lynx_layer* layers, int32_t n, int32_t i, size_t* out) {
+  if (!layers || !out) return LYNX_ERR_NULL;
+  if (i < 0 || i + 1 >= n || !fusable(layers[i], layers[i + 1])) return LYNX_ERR_UNSUPPORTED;
+  const PairPlan p = plan_pair(layers[i], layers[i + 1]);
+  const Workspace d = carve(nullptr, layers[i].M, layers[i + 1].K, layers[i + 1].R);
+  out[0] = p.dn_off + reinterpret_cast<uintptr_t>(d.vals);
+  out[1] = p.dn_off + reinterpret_cast<uintptr_t>(d.meta);
+  out[2] = p.dn_off + reinterpret_cast<uintptr_t>(d.s);
+  out[3] = p.dn_off + reinterpret_cast<uintptr_t>(d.T);
+  out[4] = p.total;
+  return LYNX_OK;
+}
+
+int seq_enqueue(const lynx_layer* layers, int32_t n, void* ws, size_t ws_bytes, cudaStream_t st) {
+  for (int32_t i = 0; i < n; ++i) {
+    if (i + 1 < n && fusable(layers[i], layers[i + 1])) {
+      const PairPlan p = plan_pair(layers[i], layers[i + 1]);
+      if (p.total <= ws_bytes) {
+        if (int e = run_pair(layers[i], layers[i + 1], p, ws, st)) return e;
+        ++i;
+        continue;
+      }
+    }
+    if (int e = run_single(layers[i], ws, ws_bytes, st)) return e;
+  }
+  return LYNX_OK;
+}
+
 }  // namespace lynx
 
 using namespace lynx;
@@ -237,9 +571,13 @@ size_t lynx_meta_bytes(int64_t M, int64_t K) {
 }
 
 size_t lynx_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t R) {
-  (void)N;
   if (M < 1 || K < 1 || R < 0) return 0;
-  return carve(nullptr, M, K, R).bytes;
+  size_t b = carve(nullptr, M, K, R).bytes;
+  if (N >= 1 && N <= (int64_t(1) << 24) && M <= 65535LL * 128) {
+    const PairShape shape = sparse_shape(M, N);
+    b += split_bytes(shape, M, N, ksplit_for(shape, M, N, K));
+  }
+  return b;
 }
 
 size_t lynx_dense_workspace_bytes(int64_t M, int64_t R) {
@@ -264,41 +602,9 @@ int lynx_lora_down(const void* X, const void* LB, const float* s, void* T, int64
 int lynx_linear(const void* X, const void* W, const void* LA, const void* LB, void* Y, int64_t M, int64_t N,
                 int64_t K, int64_t R, void* workspace, size_t workspace_bytes, void* stream) {
   if (int e = linear_arg_status(X, W, LA, LB, Y, M, N, K, R, workspace, workspace_bytes)) return e;
-  Workspace ws = carve(workspace, M, K, R);
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-
-  PairArgs g;
-  std::memset(&g, 0, sizeof(g));
-  const int forced = g_force_tile.load();
-  const PairShape shape = forced ? PairShape{forced >> 16, forced & 0xFFFF}
-                                 : pair_shape(true, static_cast<int>(M), static_cast<int>(N));
-  const uint64_t meta_rows = 2 * static_cast<uint64_t>(meta_bytes(M, K) / kMetaChunkBytes);  // 1 KiB rows
-  if (!make_map(&g.tmA, ws.vals, K / 2, M, K / 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&g.tmB, W, K, N, K, 64, shape.tn / 2, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&g.tmMeta, ws.meta, 256, meta_rows, 256, 256, 2, CU_TENSOR_MAP_SWIZZLE_NONE,
-                CU_TENSOR_MAP_DATA_TYPE_UINT32) ||
-      !make_map(&g.tmT, ws.T, R, M, R, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&g.tmLA, LA, R, N, R, 64, shape.tn / 2, CU_TENSOR_MAP_SWIZZLE_128B))
-    return LYNX_ERR_CUDA;
-  if (!set_y_map(&g, Y, M, N)) return LYNX_ERR_CUDA;
-  g.rowscale = ws.s;
-  g.scale_mode = SCALE_MUL;
-  g.Y = Y;
-  g.ldy = N;
-  g.M = static_cast<int>(M);
-  g.N = static_cast<int>(N);
-  g.K = static_cast<int>(K);
-  g.ctl = make_ctl();
-
-  ProArgs pa;
-  if (int e = make_prologue(&pa, X, LB, M, K, ws.vals, ws.meta, ws.s, ws.T)) return e;
-
   StageEvents prof(3);
-  if (cudaError_t e = prof.mark(0, st)) return cuda_status(e);
-  if (cudaError_t e = launch_prologue(pa, true, st)) return cuda_status(e);
-  if (cudaError_t e = prof.mark(1, st)) return cuda_status(e);
-  if (cudaError_t e = launch_gemm_pair(true, true, shape, g, st)) return cuda_status(e);
-  return cuda_status(prof.mark(2, st));
+  return linear_impl(X, W, LA, LB, Y, M, N, K, R, workspace, workspace_bytes, static_cast<cudaStream_t>(stream), false,
+                     nullptr, prof);
 }
 
 int lynx_sparsify_lora(const void* X, const void* LB, int64_t M, int64_t K, int64_t R, void* vals, void* meta,
@@ -318,38 +624,8 @@ int lynx_sparsify_lora(const void* X, const void* LB, int64_t M, int64_t K, int6
 int lynx_linear_dense(const void* X, const void* W, const void* LA, const void* LB, void* Y, int64_t M,
                       int64_t N, int64_t K, int64_t R, void* workspace, size_t workspace_bytes, void* stream) {
   if (int e = dense_arg_status(X, W, LA, LB, Y, M, N, K, R, workspace, workspace_bytes)) return e;
-  const bool lora = LA || LB;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-
-  PairArgs g;
-  std::memset(&g, 0, sizeof(g));
-  if (!make_map(&g.tmA, X, K, M, K, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&g.tmB, W, K, N, K, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
-    return LYNX_ERR_CUDA;
-  if (lora) {
-    if (!make_map(&g.tmT, workspace, R, M, R, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&g.tmLA, LA, R, N, R, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
-      return LYNX_ERR_CUDA;
-  }
-  if (!set_y_map(&g, Y, M, N)) return LYNX_ERR_CUDA;
-  g.rowscale = nullptr;
-  g.scale_mode = SCALE_NONE;
-  g.Y = Y;
-  g.ldy = N;
-  g.M = static_cast<int>(M);
-  g.N = static_cast<int>(N);
-  g.K = static_cast<int>(K);
-  g.ctl = make_ctl();
-  StageEvents prof(lora ? 3 : 2);
-  if (cudaError_t e = prof.mark(0, st)) return cuda_status(e);
-  if (lora) {
-    if (int e = run_lora_down(X, LB, nullptr, workspace, M, K, st)) return e;
-    if (cudaError_t e = prof.mark(1, st)) return cuda_status(e);
-    if (cudaError_t e = launch_gemm_pair(false, true, PairShape{1, 256}, g, st)) return cuda_status(e);
-    return cuda_status(prof.mark(2, st));
-  }
-  if (cudaError_t e = launch_gemm_pair(false, false, PairShape{1, 256}, g, st)) return cuda_status(e);
-  return cuda_status(prof.mark(1, st));
+  StageEvents prof((LA || LB) ? 3 : 2);
+  return dense_impl(X, W, LA, LB, Y, M, N, K, R, workspace, static_cast<cudaStream_t>(stream), false, nullptr, prof);
 }
 
 int lynx_linear_wsparse(const void* X, const void* Wvals, const void* Wmeta, const void* LA, const void* LB, void* Y,
@@ -480,6 +756,17 @@ int lynx_debug_force_split(int split) {
 int lynx_debug_prologue_split(int64_t M, int64_t K) {
   if (check_mk(M, K) != LYNX_OK) return 0;
   return prologue_split(static_cast<int>(M), static_cast<int>(K));
+}
+
+int lynx_debug_force_ksplit(int splits) {
+  if (splits < 0 || splits > kMaxKSplit) return LYNX_ERR_UNSUPPORTED;
+  g_force_ksplit.store(splits);
+  return LYNX_OK;
+}
+
+int lynx_debug_linear_ksplit(int64_t M, int64_t N, int64_t K) {
+  if (check_mk(M, K) != LYNX_OK || check_n(M, N) != LYNX_OK) return 0;
+  return ksplit_for(sparse_shape(M, N), M, N, K);
 }
 
 int lynx_debug_force_tile(int tile_rows, int tile_cols) {

@@ -12,10 +12,10 @@
 // ring of shared-memory stages.  One thread issues four tcgen05.mma
 // (M = 128, N = 64, K = 16) per stage into a 64-column TMEM accumulator, while
 // sixteen selection warps (four threads per row, 16 channels each) read the same
-// X tile, keep the top two of every four channels, and stage the kept values
-// (128-byte swizzled, the layout the sparse GEMM loads) and the metadata
-// chunk of every 128-channel block; a TMA store and a bulk copy write them
-// out.  Rows of X are therefore read from HBM once for both branches.
+// X tile, keep the top two of every four channels, and store the kept values
+// (16 bytes per thread and stage) and the metadata words (32 bits per thread
+// and 128-channel block) straight to global memory.  Rows of X are therefore
+// read from HBM once for both branches.
 //
 // The channel blocks of a row block are split over a cluster of `split` CTAs
 // so that the grid covers the GPU; each CTA keeps its fp32 shares (x^2,
@@ -35,53 +35,41 @@ namespace lynx {
 namespace {
 
 constexpr int P_ROWS = 128;                       // rows per CTA = TMEM lanes
-constexpr int P_NST = 6;                          // pipeline stages
+constexpr int P_NST = 8;                          // pipeline stages
 constexpr int P_WORKERS = 16;                     // selection warps: four threads per row
 constexpr int P_TPR = 32 * P_WORKERS / 128;       // threads per row (16 of each stage's 64 channels each)
-constexpr int P_PUB_WARP = 2 + P_WORKERS;         // lane 0 of the warp after the selection warps writes blocks out
-constexpr int P_THREADS = 96 + 32 * P_WORKERS;    // warp 0 TMA, warp 1 MMA, warps 2..17 selection, warp 18
+constexpr int P_THREADS = 64 + 32 * P_WORKERS;    // warp 0 TMA, warp 1 MMA, warps 2..17 selection
 static_assert(P_TPR == 4, "the selection code below assumes four threads per row");
 constexpr int P_XT = P_ROWS * 128;                // X tile: 128 rows x 64 channels (16 KiB)
 constexpr int P_LBT = kRankLB * 128;              // LB tile: 64 ranks x 64 channels (8 KiB)
 constexpr int P_STAGE = P_XT + P_LBT;
-constexpr int P_VBUF = P_ROWS * 128;              // kept values of one 128-channel block (16 KiB)
-constexpr int P_OBUF = P_VBUF + kMetaChunkBytes;  // + the block's metadata chunk
-constexpr int P_NOBUF = 3;                        // output staging buffers
 constexpr int P_SMALL = 2048;                     // barriers, s of the rows, norm shares of the rows
-constexpr int P_SMEM = P_NST * P_STAGE + P_NOBUF * P_OBUF + P_SMALL + 1024;  // + alignment
+constexpr int P_SMEM = P_NST * P_STAGE + P_SMALL + 1024;  // + alignment
 constexpr int P_TSTRIDE = 68;                     // floats per row of the T' share (272 B: conflict-free rows)
 static_assert(P_ROWS * P_TSTRIDE * 4 <= P_NST * P_STAGE, "the T' share fits in the drained stage ring");
 static_assert(P_SMEM <= 232448, "shared memory budget");
 
 __constant__ SelectTable c_select_table = make_select_table();
 
-enum Site : int { SITE_P_PRODUCER = 21, SITE_P_MMA = 22, SITE_P_WORKER = 23, SITE_P_ACC = 24, SITE_P_PUB = 25 };
+enum Site : int { SITE_P_PRODUCER = 21, SITE_P_MMA = 22, SITE_P_WORKER = 23, SITE_P_ACC = 24 };
 
 __device__ __forceinline__ void named_sync_workers() {
   asm volatile("bar.sync 1, %0;" ::"n"(32 * P_WORKERS) : "memory");
-}
-__device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_u32(ssrc)),
-               "r"(bytes)
-               : "memory");
 }
 
 template <bool LORA>
 __global__ void __launch_bounds__(P_THREADS, 1) prologue_kernel(const __grid_constant__ ProArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* obuf0 = smem + P_NST * P_STAGE;
-  uint64_t* full = reinterpret_cast<uint64_t*>(obuf0 + P_NOBUF * P_OBUF);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + P_NST * P_STAGE);
   uint64_t* empty = full + P_NST;
   uint64_t* acc_full = empty + P_NST;
-  uint64_t* done = acc_full + 1;        // [P_NOBUF] a block's staging buffer is written (one arrival per warp)
-  uint64_t* freed = done + P_NOBUF;     // [P_NOBUF] its store has read the buffer (publisher)
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(freed + P_NOBUF);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(acc_full + 1);
   float* s_sh = reinterpret_cast<float*>(tslot + 4);  // direct mode: s of the CTA's rows (128 floats)
   float2* npart = reinterpret_cast<float2*>(s_sh + P_ROWS);  // cluster mode: (sum x^2, sum kept x^2) per row
   uint32_t* sel_table = reinterpret_cast<uint32_t*>(npart + P_ROWS);  // the top-2-of-4 decision table
   float* tpart = reinterpret_cast<float*>(smem);            // cluster mode: T' share [128][P_TSTRIDE]
-  static_assert(8 * (3 * P_NST + 2 * P_NOBUF) + 16 + 12 * P_ROWS + 64 * 4 <= P_SMALL, "small-state area");
+  static_assert(8 * (2 * P_NST + 1) + 16 + 12 * P_ROWS + 64 * 4 <= P_SMALL, "small-state area");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rb = blockIdx.x / a.split, sp = blockIdx.x % a.split;
@@ -96,16 +84,11 @@ __global__ void __launch_bounds__(P_THREADS, 1) prologue_kernel(const __grid_con
       mbar_init(&empty[i], P_WORKERS + (LORA ? 1 : 0));
     }
     mbar_init(acc_full, 1);
-    for (int i = 0; i < P_NOBUF; ++i) {
-      mbar_init(&done[i], P_WORKERS);
-      mbar_init(&freed[i], 1);
-    }
     fence_mbar_init();
   }
   if (threadIdx.x < 64) sel_table[threadIdx.x] = c_select_table.e[threadIdx.x];
   if (threadIdx.x == 32) {
     prefetch_tmap(&a.tmX);
-    prefetch_tmap(&a.tmV);
     if (LORA) prefetch_tmap(&a.tmLB);
   }
   if (LORA && warp == 1) {
@@ -119,6 +102,8 @@ __global__ void __launch_bounds__(P_THREADS, 1) prologue_kernel(const __grid_con
   // The set-up above may overlap the previous kernel; nothing below touches global memory before it is done.
   pdl_launch_dependents();
   pdl_wait();
+  if (blockIdx.x == 0)  // the arrival counters of the split-K GEMM that follows start at zero
+    for (int i = threadIdx.x; i < a.nzero; i += P_THREADS) a.zero[i] = 0u;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -166,35 +151,24 @@ __global__ void __launch_bounds__(P_THREADS, 1) prologue_kernel(const __grid_con
       tc_commit(acc_full);  // fires once every MMA issued above has completed
       mbar_wait(acc_full, 0, a.ctl, SITE_P_ACC);  // no MMA may still run when TMEM is released
     }
-  } else if (warp == P_PUB_WARP) {
-    if (lane == 0) {
-      // -------------------------------------------------------------- publisher: finished blocks -> global
-      const int64_t blocks_k = meta_blocks_k(a.K);
-      const int nblocks = kb1 - kb0;
-      for (int kbl = 0; kbl < nblocks; ++kbl) {
-        const int b = kbl % P_NOBUF;
-        if (!mbar_wait(&done[b], (kbl / P_NOBUF) & 1, a.ctl, SITE_P_PUB)) break;
-        uint8_t* vb = obuf0 + b * P_OBUF;
-        const int kb = kb0 + kbl;
-        tma_store_2d(&a.tmV, vb, kb * 64, r0);
-        bulk_store(a.meta + (static_cast<int64_t>(rb) * blocks_k + kb) * kMetaChunkBytes, vb + P_VBUF,
-                   kMetaChunkBytes);
-        bulk_commit();
-        if (kbl > 0) {
-          bulk_wait_read_one();                          // block kbl - 1's copies have read their buffer
-          mbar_arrive(&freed[(kbl - 1) % P_NOBUF]);
-        }
-      }
-      bulk_wait_all();
-    }
   } else {
     // ---------------------------------------------------------------- selection warps
-    const int tw = threadIdx.x - 64;
-    const int r = tw >> 2, qq = tw & 3;  // row of the tile; which 16 of each stage's 64 channels
+    // Warp sw (0..15) takes rows base + i and base + 8 + i (i = 0..3, base = 16 (sw / 2) + 4 (sw % 2)), four
+    // neighbouring lanes per row (16 of each stage's 64 channels each).  Rows r and r + 8 of a 16-row group
+    // share the tensor-memory lanes of their metadata (low and high 16-bit halves of a word), so both halves
+    // of every word are computed inside one warp and one lane stores the whole word.
+    const int sw = warp - 2;
+    const int qq = lane & 3, hsel = lane >> 4;
+    const int r = 16 * (sw >> 1) + 4 * (sw & 1) + 8 * hsel + ((lane >> 2) & 3);
     const int row = r0 + r;
-    // this thread's 16-bit metadata half: groups 4 (qq & 1) .. +3 of a 32-channel word; rows r and r + 8 of a
-    // 16-row group share TMEM lanes (low halves in lanes 0-7 of the group, high halves in lanes 8-15)
-    const int mlane = (r / 16) * 16 + (qq & 1) * 8 + (r % 8), half_sel = (r % 16) / 8;
+    const bool row_live = row < a.M;
+    // this thread's 16-bit metadata half: groups 4 (qq & 1) .. +3 of a 32-channel word, in TMEM lane mlane;
+    // lane hsel of the pair (lane, lane ^ 16) stores word 2 hsel + qq / 2 of that lane (4 words of 16 bytes)
+    const int mlane = (r / 16) * 16 + (qq & 1) * 8 + (r % 8);
+    const int64_t blocks_k = meta_blocks_k(a.K);
+    uint8_t* mword = a.meta + static_cast<int64_t>(rb) * blocks_k * kMetaChunkBytes + mlane * 16 + hsel * 8 +
+                     (qq >> 1) * 4;
+    uint16_t* vrow = a.vals + static_cast<int64_t>(row_live ? row : 0) * (a.K / 2);
     float sx = 0.f, skept = 0.f;  // running sums of x^2 and kept x^2 (terms added in channel order)
     bool ok = true;
     // one 128-channel block (two stages) per iteration: eight groups per thread
@@ -223,24 +197,19 @@ __global__ void __launch_bounds__(P_THREADS, 1) prologue_kernel(const __grid_con
         const uint32_t n3 = select_group(u1.z, u1.w, sel_table, k[4 * sub + 3], sx, skept);
         half[sub] = n0 | (n1 << 4) | (n2 << 8) | (n3 << 12);
       }
-      uint8_t* vb = obuf0 + (kbl % P_NOBUF) * P_OBUF;
-      if (kbl >= P_NOBUF) {  // the buffer's previous block has been copied out
-        ok = mbar_wait(&freed[kbl % P_NOBUF], (kbl / P_NOBUF - 1) & 1, a.ctl, SITE_P_WORKER);
-        ok = __all_sync(0xFFFFFFFFu, ok);
-        if (!ok) break;
-      }
+      const int kb = kb0 + kbl;
+      if (row_live) {
 #pragma unroll
-      for (int sub = 0; sub < 2; ++sub) {
-        // 16-byte chunk 4 sub + qq of the row's 128 bytes of kept values, 128-byte swizzle
-        *reinterpret_cast<uint4*>(vb + r * 128 + (((4 * sub + qq) ^ (r & 7)) << 4)) =
-            make_uint4(k[4 * sub], k[4 * sub + 1], k[4 * sub + 2], k[4 * sub + 3]);
-        const int w = 2 * sub + (qq >> 1);  // 32-channel word of the chunk
-        *reinterpret_cast<uint16_t*>(vb + P_VBUF + mlane * 16 + w * 4 + half_sel * 2) =
-            static_cast<uint16_t>(half[sub]);
+        for (int sub = 0; sub < 2; ++sub) {  // the 8 kept values of this thread's 16 channels: 16 bytes
+          const int ch = kb * kMetaBlockCols + sub * 64 + 16 * qq;
+          if (ch < a.K)
+            *reinterpret_cast<uint4*>(vrow + ch / 2) = make_uint4(k[4 * sub], k[4 * sub + 1], k[4 * sub + 2], k[4 * sub + 3]);
+        }
       }
-      fence_proxy_async();  // block complete: hand the buffer to the publisher
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&done[kbl % P_NOBUF]);
+      const uint32_t p0 = __shfl_xor_sync(0xFFFFFFFFu, half[0], 16);  // the partner row's halves
+      const uint32_t p1 = __shfl_xor_sync(0xFFFFFFFFu, half[1], 16);
+      const uint32_t word = hsel == 0 ? (half[0] | (p0 << 16)) : (p1 | (half[1] << 16));
+      *reinterpret_cast<uint32_t*>(mword + static_cast<int64_t>(kb) * kMetaChunkBytes) = word;
     }
     // row sums: the four threads of a row are neighbouring lanes
     sx += __shfl_xor_sync(0xFFFFFFFFu, sx, 1);
@@ -274,7 +243,7 @@ __global__ void __launch_bounds__(P_THREADS, 1) prologue_kernel(const __grid_con
           const int trow = q * 32 + lane, grow = r0 + trow;
           if (a.split == 1) {
             if (grow < a.M) {
-              const float sv = s_sh[trow];
+              const float inv = 1.f / s_sh[trow];  // T' = T * (1 / s): one division per row
               uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.T) + static_cast<int64_t>(grow) * kRankLB);
 #pragma unroll
               for (int v8 = 0; v8 < 8; ++v8) {
@@ -282,8 +251,8 @@ __global__ void __launch_bounds__(P_THREADS, 1) prologue_kernel(const __grid_con
                 uint32_t pk[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                  __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(src[2 * j]) / sv,
-                                                            __uint_as_float(src[2 * j + 1]) / sv);
+                  __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(src[2 * j]) * inv,
+                                                            __uint_as_float(src[2 * j + 1]) * inv);
                   pk[j] = *reinterpret_cast<uint32_t*>(&b2);
                 }
                 dst[v8] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -309,40 +278,51 @@ __global__ void __launch_bounds__(P_THREADS, 1) prologue_kernel(const __grid_con
     // CTA j of the cluster finishes rows [j * 128 / split, (j + 1) * 128 / split): it adds the split CTAs' shares in rank order
     // (deterministic), reading them from the peers' shared memory, and writes s and T'.
     cluster_sync();  // every CTA's shares are in its shared memory
-    const int row_lo = sp * P_ROWS / a.split, rows = (sp + 1) * P_ROWS / a.split - row_lo, per_row = LORA ? 8 : 1;
-    for (int i = threadIdx.x; i < rows * per_row; i += P_THREADS) {
-      const int rr = row_lo + i / per_row, g = i % per_row, grow = r0 + rr;
-      float sxs = 0.f, sks = 0.f;
-      float acc[8] = {};
-      for (int p = 0; p < a.split; ++p) {
-        const float2 n2 = ld_cluster_f32x2(mapa_shared(&npart[rr], p));
-        sxs += n2.x;
-        sks += n2.y;
-        if (LORA) {
-          const uint32_t t = mapa_shared(tpart + rr * P_TSTRIDE + 8 * g, p);
-          const float4 u = ld_cluster_f32x4(t), w = ld_cluster_f32x4(t + 16);
-          acc[0] += u.x;
-          acc[1] += u.y;
-          acc[2] += u.z;
-          acc[3] += u.w;
-          acc[4] += w.x;
-          acc[5] += w.y;
-          acc[6] += w.z;
-          acc[7] += w.w;
-        }
-      }
-      const float sv = sks > 0.f ? sqrtf(sxs / sks) : 1.f;
-      if (grow < a.M) {
-        if (g == 0) a.s[grow] = sv;
-        if (LORA) {
-          uint32_t pk[4];
+    const int row_lo = sp * P_ROWS / a.split, rows = (sp + 1) * P_ROWS / a.split - row_lo;
+    // Each thread first issues all its peer loads (up to kMaxPrologueSplit), then adds them in rank order, so
+    // the distributed-shared-memory round trips overlap instead of following one another.
+    if (threadIdx.x < rows) {  // s of the row
+      const int rr = row_lo + threadIdx.x, grow = r0 + rr;
+      float2 n2[kMaxPrologueSplit];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * j] / sv, acc[2 * j + 1] / sv);
-            pk[j] = *reinterpret_cast<uint32_t*>(&b2);
+      for (int p = 0; p < kMaxPrologueSplit; ++p)
+        if (p < a.split) n2[p] = ld_cluster_f32x2(mapa_shared(&npart[rr], p));
+      float sxs = 0.f, sks = 0.f;
+#pragma unroll
+      for (int p = 0; p < kMaxPrologueSplit; ++p)
+        if (p < a.split) {
+          sxs += n2[p].x;
+          sks += n2[p].y;
+        }
+      const float sv = sks > 0.f ? sqrtf(sxs / sks) : 1.f;
+      s_sh[rr] = sv;
+      if (grow < a.M) a.s[grow] = sv;
+    }
+    if (LORA) {
+      __syncthreads();  // s of the CTA's rows in s_sh
+      // T' in items of 4 ranks: 16 per row
+      for (int i = threadIdx.x; i < rows * 16; i += P_THREADS) {
+        const int rr = row_lo + i / 16, g = i % 16, grow = r0 + rr;
+        float4 t4[kMaxPrologueSplit];
+        const uint32_t t = smem_u32(tpart + rr * P_TSTRIDE + 4 * g);
+#pragma unroll
+        for (int p = 0; p < kMaxPrologueSplit; ++p)
+          if (p < a.split) t4[p] = ld_cluster_f32x4(mapa_shared_u32(t, p));
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int p = 0; p < kMaxPrologueSplit; ++p)
+          if (p < a.split) {
+            acc.x += t4[p].x;
+            acc.y += t4[p].y;
+            acc.z += t4[p].z;
+            acc.w += t4[p].w;
           }
-          reinterpret_cast<uint4*>(a.T)[static_cast<int64_t>(grow) * (kRankLB / 8) + g] =
-              make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        if (grow < a.M) {
+          const float inv = 1.f / s_sh[rr];  // T' = T * (1 / s): one division per row
+          __nv_bfloat162 b0 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+          __nv_bfloat162 b1 = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+          reinterpret_cast<uint2*>(a.T)[static_cast<int64_t>(grow) * (kRankLB / 4) + g] =
+              make_uint2(*reinterpret_cast<uint32_t*>(&b0), *reinterpret_cast<uint32_t*>(&b1));
         }
       }
     }

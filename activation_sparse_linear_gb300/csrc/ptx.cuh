@@ -253,6 +253,12 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// shared::cluster address in CTA `rank` of the cluster of a shared::cta address (32-bit) of this CTA.
+__device__ __forceinline__ uint32_t mapa_shared_u32(uint32_t saddr, uint32_t rank) {
+  uint32_t d;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(saddr), "r"(rank));
+  return d;
+}
 // Loads from a cluster-mapped shared-memory address (a peer CTA's shared memory).
 __device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t addr) {
   float4 v;

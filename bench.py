@@ -434,7 +434,8 @@ def main() -> int:
     for name, (Ms, Ns, Ks) in (("mlp_up 4608x3072->12288", (4608, 12288, 3072)),
                                ("mlp_down 4608x12288->3072", (4608, 3072, 12288)),
                                ("cfg2_qkv 9216x3072->9216", (9216, 9216, 3072)),
-                               ("stack_qkv 16384x3072->9216", (16384, 9216, 3072))):
+                               ("stack_qkv 16384x3072->9216", (16384, 9216, 3072)),
+                               ("stack_down 1024x12288->3072", (1024, 3072, 12288))):
         cs = []
         for _ in range(2):
             cs.append({"X": torch.randn((Ms, Ks), generator=gen, device=dev).to(torch.bfloat16),
@@ -510,9 +511,12 @@ def main() -> int:
     torch.cuda.empty_cache()
 
     # The block stack of the fifth workload: 8 blocks x (QKV sparse 3072->9216, out dense 3072->3072, up dense
-    # 3072->12288, down sparse 12288->3072), rank-64 LoRA on the sparse layers, the seeded weights of every
-    # block and the seeded activations of block 0 (the down layer's input is its GELU input) from synth; the
-    # total time of the 32 linears at each M against the same 32 layers run dense through cuBLAS.
+    # 3072->12288 followed by the MLP's GELU, down sparse 12288->3072 on that GELU output), rank-64 LoRA on the
+    # sparse layers, the seeded weights of every block and the seeded block input from synth.  The up and down
+    # layers form the MLP pair, which this library runs fused (the up layer's epilogue applies GELU and
+    # sparsifies its output for the down layer).  Against it: the same 32 linears dense through cuBLAS with the
+    # same GELU (torch) between up and down.  Both sides run eagerly and as one CUDA graph each.
+    import torch.nn.functional as F
     stack = {}
 
     def block_weights(b):
@@ -526,41 +530,30 @@ def main() -> int:
     from concurrent.futures import ThreadPoolExecutor
     with ThreadPoolExecutor(8) as ex:
         wts = [{k: to_dev(v) for k, v in w.items()} for w in ex.map(block_weights, range(8))]
-        xs = list(ex.map(lambda a: synth.layer_x("stack", a[1], M=a[0], block=0),
-                         [(Ms, l) for Ms in synth.STACK_M for l in ("qkv", "down")]))
+        xs = list(ex.map(lambda Ms: synth.layer_x("stack", "qkv", M=Ms, block=0), synth.STACK_M))
     for i, Ms in enumerate(synth.STACK_M):
-        x3, x12 = to_dev(xs[2 * i]), to_dev(xs[2 * i + 1])
-        y = {n: torch.empty((Ms, n), dtype=torch.bfloat16, device=dev) for n in (3072, 9216, 12288)}
-        ws_s = torch.empty(max(asl.lynx_workspace_bytes(Ms, 9216, 3072, R), asl.lynx_workspace_bytes(Ms, 3072, 12288, R)),
-                           dtype=torch.uint8, device=dev)
+        x3 = to_dev(xs[i])
+        y = {n: torch.empty((Ms, n), dtype=torch.bfloat16, device=dev) for n in (3072, 9216)}
+        h = torch.empty((Ms, 12288), dtype=torch.bfloat16, device=dev)
+        y_dn = torch.empty((Ms, 3072), dtype=torch.bfloat16, device=dev)
+        layers = []
+        for w in wts:
+            layers += [asl.lynx_layer(x3, w["qkv"], w["la_qkv"], w["lb_qkv"], y[9216], sparse=True),
+                       asl.lynx_layer(x3, w["out"], None, None, y[3072], sparse=False),
+                       asl.lynx_layer(x3, w["up"], None, None, h, sparse=False, gelu=True),
+                       asl.lynx_layer(h, w["down"], w["la_down"], w["lb_down"], y_dn, sparse=True)]
+        ws_s = torch.empty(asl.lynx_layers_workspace_bytes(layers), dtype=torch.uint8, device=dev)
 
         def lynx_stack():
-            for w in wts:
-                for xin, wt, la, lb, yo, kk in ((x3, w["qkv"], w["la_qkv"], w["lb_qkv"], y[9216], 3072),
-                                               (x12, w["down"], w["la_down"], w["lb_down"], y[3072], 12288)):
-                    if L.lynx_linear(xin.data_ptr(), wt.data_ptr(), la.data_ptr(), lb.data_ptr(), yo.data_ptr(), Ms,
-                                     wt.shape[0], kk, R, ws_s.data_ptr(), ws_s.numel(), sp) != 0:
-                        raise RuntimeError("lynx_linear failed")
-                for wt, yo in ((w["out"], y[3072]), (w["up"], y[12288])):
-                    if L.lynx_linear_dense(x3.data_ptr(), wt.data_ptr(), None, None, yo.data_ptr(), Ms, wt.shape[0],
-                                           3072, R, None, 0, sp) != 0:
-                        raise RuntimeError("lynx_linear_dense failed")
+            asl.lynx_run_layers(layers, ws_s, stream=stream)
 
         def dense_stack():
             for w in wts:
                 torch.matmul(x3, w["qkv"].t(), out=y[9216])
                 torch.matmul(x3, w["out"].t(), out=y[3072])
-                torch.matmul(x3, w["up"].t(), out=y[12288])
-                torch.matmul(x12, w["down"].t(), out=y[3072])
+                hd = F.gelu(torch.matmul(x3, w["up"].t()))
+                torch.matmul(hd, w["down"].t(), out=y_dn)
 
-        # The same 32 linears as one CUDA graph each: the library's layer-sequence graph and a captured
-        # torch/cuBLAS graph of the dense stack, so that neither side pays a host call per layer.
-        layers = []
-        for w in wts:
-            layers += [asl.lynx_layer(x3, w["qkv"], w["la_qkv"], w["lb_qkv"], y[9216], sparse=True),
-                       asl.lynx_layer(x12, w["down"], w["la_down"], w["lb_down"], y[3072], sparse=True),
-                       asl.lynx_layer(x3, w["out"], None, None, y[3072], sparse=False),
-                       asl.lynx_layer(x3, w["up"], None, None, y[12288], sparse=False)]
         lgraph = asl.LynxGraph(layers, ws_s)
         dense_stack()  # cuBLAS workspace and kernels chosen before capture
         torch.cuda.synchronize()
@@ -585,8 +578,42 @@ def main() -> int:
         stack[f"M={Ms}"] = {"lynx_ms": tt[0], "all_dense_cublas_ms": tt[1], "x_vs_dense_cublas": tt[1] / tt[0],
                             "lynx_graph_ms": tt[2], "all_dense_cublas_graph_ms": tt[3],
                             "x_vs_dense_cublas_graph": tt[3] / tt[2]}
-        del x3, x12, y, ws_s, layers, lgraph, dgraph
+        del x3, y, h, y_dn, ws_s, layers, lgraph, dgraph
     del wts, xs
+    torch.cuda.empty_cache()
+
+    # The MLP pair of the third workload (4608 tokens: up 3072->12288 sparse with LoRA, GELU, down 12288->3072
+    # sparse with LoRA), fused through the layer sequence, against cuBLAS up, GELU (torch) and cuBLAS down.
+    tu = synth.layer_tensors("mlp", "up")
+    td = synth.layer_tensors("mlp", "down", with_x=False)
+    Mm = tu["M"]
+    xu = to_dev(tu["X"])
+    hu = torch.empty((Mm, 12288), dtype=torch.bfloat16, device=dev)
+    yd = torch.empty((Mm, 3072), dtype=torch.bfloat16, device=dev)
+    wu, wd = to_dev(tu["W"]), to_dev(td["W"])
+    pair = [asl.lynx_layer(xu, wu, to_dev(tu["LA"]), to_dev(tu["LB"]), hu, sparse=True, gelu=True),
+            asl.lynx_layer(hu, wd, to_dev(td["LA"]), to_dev(td["LB"]), yd, sparse=True)]
+    ws_p = torch.empty(asl.lynx_layers_workspace_bytes(pair), dtype=torch.uint8, device=dev)
+    tt = []
+    for fn in (lambda: asl.lynx_run_layers(pair, ws_p, stream=stream),
+               lambda: torch.matmul(F.gelu(torch.matmul(xu, wu.t())), wd.t(), out=yd)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(20):
+            fn()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        tt.append(a0.elapsed_time(a1) / 20)
+    st = asl.lynx_sync_status()
+    assert st == 0, asl.lynx_status_string(st)
+    fl = 2.0 * Mm * 12288 * 3072 * 2
+    mlp_pair = {"lynx_ms": tt[0], "tflops": fl / (tt[0] * 1e-3) / 1e12, "cublas_gelu_ms": tt[1],
+                "x_vs_dense_cublas": tt[1] / tt[0],
+                "note": "up 4608x3072->12288 sparse+LoRA, GELU, down 12288->3072 sparse+LoRA (fused pair)"}
+    del xu, hu, yd, wu, wd, pair, ws_p
     torch.cuda.empty_cache()
 
     # End to end through the C-ABI with host buffers, pipelined as a serving loop runs it: every step copies
@@ -681,6 +708,7 @@ def main() -> int:
             "other_shapes": shapes,
             "sparsify_alone": sparsify_alone,
             "block_stack_32_linears": stack,
+            "mlp_pair_fused": mlp_pair,
             "mma_microbench": {"dense_tflops": mma_dense_tf, "sparse_tflops_effective": mma_sparse_tf,
                                "dense_macs_per_clk": mma_dense_mpc, "sparse_macs_per_clk_effective": mma_sparse_mpc,
                                "sparse_over_dense": mma_sparse_tf / mma_dense_tf,

@@ -73,9 +73,14 @@ typedef enum {
  * group (0x4). */
 LYNX_API size_t lynx_meta_bytes(int64_t M, int64_t K);
 
-/* Workspace bytes needed by lynx_linear: compressed values (M x K/2 bf16),
- * metadata (lynx_meta_bytes), s (M fp32) and the M x R LoRA intermediate T'
- * (bf16), each 256-byte aligned.  Independent of N. */
+/* Workspace bytes needed by lynx_linear on the current device: compressed
+ * values (M x K/2 bf16), metadata (lynx_meta_bytes), s (M fp32) and the M x R
+ * LoRA intermediate T' (bf16), each 256-byte aligned -- the base part --
+ * and, for problems whose output tiles would leave a large share of the GPU
+ * idle, the split-K region of the sparse GEMM: fp32 partial tiles and one
+ * arrival counter per tile and CTA (this part depends on N).  lynx_linear
+ * accepts any workspace that holds the base part; it runs the split-K
+ * schedule only when the whole amount is there. */
 LYNX_API size_t lynx_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t R);
 
 /* Workspace bytes needed by lynx_linear_dense when a LoRA branch is given
@@ -176,12 +181,28 @@ LYNX_API int lynx_linear_dense(const void* X, const void* W, const void* LA, con
  * into a CUDA graph that replays every kernel of it with one host call.
  * (The graph is a deployment convenience, not part of the paper.) */
 
-/* One layer.  sparse = 1: Y = lynx_linear(X, W, LA, LB) (LA and LB required,
- * R = 64); sparse = 0: Y = lynx_linear_dense(X, W, LA, LB) (LA and LB both
- * NULL, or both given with R = 64).  Device pointers and layouts as for those
- * calls.  A layer may read the Y of an earlier layer of the same sequence. */
+/* One layer.  flags & LYNX_LAYER_SPARSE: Y = lynx_linear(X, W, LA, LB) (LA
+ * and LB required, R = 64); otherwise Y = lynx_linear_dense(X, W, LA, LB) (LA
+ * and LB both NULL, or both given with R = 64).  flags & LYNX_LAYER_GELU: the
+ * layer's bf16 result y is passed through the exact-erf GELU, Y = bf16(GELU(y))
+ * (the activation between a DiT MLP's up and down projections).  Device
+ * pointers and layouts as for those calls.  A layer may read the Y of an
+ * earlier layer of the same sequence.
+ *
+ * The MLP pair: when a GELU layer is followed by a sparse layer whose X is
+ * that Y (same pointer and M, its K equal to the GELU layer's N, N % 128 == 0),
+ * the sequence runs the pair fused ("RT-Lynx" page, CUDA kernel optimisation:
+ * one execution path for the online sparsification): the GELU layer's
+ * epilogue also writes the 2:4 values, metadata and partial row norms of its
+ * output, and the sparse layer's sparsify pass is replaced by a LoRA
+ * down-projection that finishes s and T'.  Y of the GELU layer is still
+ * written; the results equal those of the two layers run one by one, up to the
+ * fp32 summation order of the row norms.  The fused pair needs more workspace
+ * (lynx_layers_workspace_bytes counts it); with less, the pair runs unfused. */
+#define LYNX_LAYER_SPARSE 1
+#define LYNX_LAYER_GELU 2
 typedef struct {
-  int32_t sparse;
+  int32_t flags;
   const void* X;
   const void* W;
   const void* LA;
@@ -190,14 +211,16 @@ typedef struct {
   int64_t M, N, K, R;
 } lynx_layer;
 
-/* Workspace for a sequence: the largest any one layer needs (the layers run
- * one after another and reuse it).  0 if layers is NULL or n < 1. */
+/* Workspace for a sequence: the largest any one layer, or fused MLP pair,
+ * needs (they run one after another and reuse it).  0 if layers is NULL or
+ * n < 1. */
 LYNX_API size_t lynx_layers_workspace_bytes(const lynx_layer* layers, int32_t n);
 
 /* Enqueues the n layers in order on `stream` (asynchronous).  Every layer is
  * checked on the host first: if one fails, nothing is enqueued, its status is
  * returned and its index is stored in *failed_layer (when failed_layer is not
- * NULL; -1 otherwise).  n = 0 enqueues nothing and returns LYNX_OK. */
+ * NULL; -1 otherwise).  Flags other than the two above give
+ * LYNX_ERR_UNSUPPORTED.  n = 0 enqueues nothing and returns LYNX_OK. */
 LYNX_API int lynx_run_layers(const lynx_layer* layers, int32_t n, void* workspace, size_t workspace_bytes,
                              void* stream, int32_t* failed_layer);
 
@@ -280,6 +303,12 @@ LYNX_API void lynx_profile_next(void* const* events, int count);
  * Other modes return LYNX_ERR_UNSUPPORTED.  Synchronises `stream`. */
 LYNX_API int lynx_mma_rate(int mode, int iters, double* tflops, double* macs_per_clock, void* stream);
 
+/* Test hook.  For layers i and i + 1 of a sequence that run as a fused MLP pair, writes the byte offsets in the
+ * sequence's workspace of the sparse layer's compressed values, metadata, s and T' (written by the pair's first
+ * two kernels) to offsets[0..3] and the pair's workspace bytes to offsets[4].  LYNX_ERR_UNSUPPORTED when the two
+ * layers do not fuse, LYNX_ERR_NULL for NULL arguments. */
+LYNX_API int lynx_debug_pair_offsets(const lynx_layer* layers, int32_t n, int32_t i, size_t* offsets);
+
 /* Test hook.  inject = 1 makes the next GEMM launches never deliver their
  * first pipeline stage, so their bounded waits run out after wait_ns
  * nanoseconds and lynx_sync_status reports LYNX_ERR_TIMEOUT.  inject = 0
@@ -296,9 +325,20 @@ LYNX_API int lynx_debug_force_split(int split);
  * each CTA owns whole rows); 0 for sizes out of range. */
 LYNX_API int lynx_debug_prologue_split(int64_t M, int64_t K);
 
+/* Test hook.  splits = 1 .. 4 makes the sparse GEMM of every later lynx_linear call whose tile shape has one row
+ * block per CTA (256 x 256 or 256 x 192) split each tile's k-steps over that many work units (clamped to the tile's 128-channel steps; 1 =
+ * never split); 0 restores the automatic choice.  lynx_workspace_bytes follows the setting.  Returns LYNX_OK, or
+ * LYNX_ERR_UNSUPPORTED (setting unchanged) for other values. */
+LYNX_API int lynx_debug_force_ksplit(int splits);
+
+/* The k-split count lynx_linear picks on the current device for these sizes (1 = no split); 0 for sizes out of
+ * range. */
+LYNX_API int lynx_debug_linear_ksplit(int64_t M, int64_t N, int64_t K);
+
 /* Test hook.  Makes lynx_linear (and lynx_linear_wsparse, whose tile rows are output columns) use sparse
  * pair tiles of tile_rows x tile_cols for every shape: 512 x 224,
- * 512 x 192 or 256 x 256 (all must give the same result); 0 x 0 restores the automatic choice by shape.
+ * 512 x 192, 256 x 256 or 256 x 192 (all must give the same result); 0 x 0 restores the automatic choice by
+ * shape.
  * Returns LYNX_OK, or LYNX_ERR_UNSUPPORTED (setting unchanged) for any other shape. */
 LYNX_API int lynx_debug_force_tile(int tile_rows, int tile_cols);
 

@@ -25,7 +25,8 @@ SOURCE = os.path.join(HERE, "lynx_oracle.cpp")
 LIB = os.path.join(HERE, "liblynx_oracle.so")
 
 __all__ = ["build", "CppOracle", "default", "widen", "select_2of4", "keep_mask", "norm_scale", "canonical_meta",
-           "sparsify", "linear", "lora_down", "linear_dense", "linear_wsparse", "NIBBLE_OF_PAIR", "host_threads"]
+           "sparsify", "linear", "lora_down", "linear_dense", "linear_wsparse", "round_bf16", "gelu", "gelu_bf16",
+           "mlp_input", "NIBBLE_OF_PAIR", "host_threads"]
 
 #: 4-bit metadata of a kept index pair (i0 < i1): i0 in bits 0-1, i1 in bits 2-3.
 NIBBLE_OF_PAIR = {(i0, i1): i0 | (i1 << 2) for i0 in range(4) for i1 in range(i0 + 1, 4)}
@@ -90,6 +91,9 @@ class CppOracle:
                                                _f64p, ctypes.c_int]),
             "lo_linear_wsparse": (ctypes.c_int, [_u16p, _u16p, _u16p, _u16p, _i64, _i64, _i64, _i64, _i64p, _i64,
                                                  _f64p, ctypes.c_int]),
+            "lo_round_bf16": (None, [_f64p, _i64, _u16p]),
+            "lo_gelu": (None, [_f64p, _i64, _f64p]),
+            "lo_gelu_bf16": (None, [_u16p, _i64, _u16p]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -203,6 +207,33 @@ class CppOracle:
                     _p(Y, _f64p), self.threads), "linear")
         return Y
 
+    def round_bf16(self, x) -> np.ndarray:
+        """Nearest bf16 (ties to even) of float64 values, as uint16 bit patterns."""
+        xd = np.ascontiguousarray(x, dtype=np.float64)
+        out = np.empty(xd.shape, dtype=np.uint16)
+        self.lib.lo_round_bf16(_p(xd, _f64p), xd.size, _p(out, _u16p))
+        return out
+
+    def gelu(self, x) -> np.ndarray:
+        """Exact-erf GELU in float64."""
+        xd = np.ascontiguousarray(x, dtype=np.float64)
+        out = np.empty(xd.shape, dtype=np.float64)
+        self.lib.lo_gelu(_p(xd, _f64p), xd.size, _p(out, _f64p))
+        return out
+
+    def gelu_bf16(self, Y) -> np.ndarray:
+        """H = bf16(GELU(Y)) of a bf16 tensor Y (bit patterns in and out)."""
+        Yb = _bits(Y)
+        out = np.empty(Yb.shape, dtype=np.uint16)
+        self.lib.lo_gelu_bf16(_p(Yb, _u16p), Yb.size, _p(out, _u16p))
+        return out
+
+    def mlp_input(self, X, W, LA=None, LB=None, sparse=True, rows=None) -> np.ndarray:
+        """The MLP down layer's input for the given rows: H = bf16(GELU(bf16(Y_up))), Y_up the up layer
+        (sparse: linear, else linear_dense) in double, rounded to the up layer's bf16 output first."""
+        y = self.linear(X, W, LA, LB, rows) if sparse else self.linear_dense(X, W, LA, LB, rows)
+        return self.gelu_bf16(self.round_bf16(y))
+
     def linear_dense(self, X, W, LA=None, LB=None, rows=None) -> np.ndarray:
         return self._dense_like(self.lib.lo_linear_dense, X, W, LA, LB, rows)
 
@@ -255,6 +286,22 @@ def lora_down(X, LB, s=None):
 
 def linear_dense(X, W, LA=None, LB=None, rows=None):
     return default().linear_dense(X, W, LA, LB, rows)
+
+
+def round_bf16(x):
+    return default().round_bf16(x)
+
+
+def gelu(x):
+    return default().gelu(x)
+
+
+def gelu_bf16(Y):
+    return default().gelu_bf16(Y)
+
+
+def mlp_input(X, W, LA=None, LB=None, sparse=True, rows=None):
+    return default().mlp_input(X, W, LA, LB, sparse, rows)
 
 
 def linear_wsparse(X, W, LA=None, LB=None, rows=None):

@@ -304,4 +304,48 @@ int lo_linear_wsparse(const uint16_t* X, const uint16_t* W, const uint16_t* LA, 
   return 0;
 }
 
+// Round to the nearest bf16 value, ties to even (8 significant bits), returned as its bit pattern.  Values too
+// large for bf16 become infinity; NaN becomes the canonical quiet NaN.
+uint16_t lo_round_bf16_one(double v) {
+  if (std::isnan(v)) return 0x7FC0;
+  const bool neg = std::signbit(v);
+  const double a = std::fabs(v);
+  float f = 0.0f;
+  if (a != 0.0) {
+    int e = 0;
+    const double m = std::frexp(a, &e);              // a = m 2^e, m in [0.5, 1)
+    int emin = -125;                                 // bf16 shares float32's exponent range
+    double r;
+    if (e >= emin) {
+      r = std::nearbyint(std::ldexp(m, 8));          // 8 significant bits, ties to even
+      f = static_cast<float>(std::ldexp(r, e - 8));  // exact: r has at most 9 bits
+    } else {                                         // subnormal: a fixed quantum of 2^-133
+      r = std::nearbyint(std::ldexp(a, 133));
+      f = static_cast<float>(std::ldexp(r, -133));
+    }
+    if (std::isinf(f) || std::fabs(static_cast<double>(f)) > 3.3895313892515355e38) f = INFINITY;
+  }
+  if (neg) f = -f;
+  uint32_t u;
+  std::memcpy(&u, &f, sizeof(u));
+  return static_cast<uint16_t>(u >> 16);
+}
+
+void lo_round_bf16(const double* x, int64_t n, uint16_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = lo_round_bf16_one(x[i]);
+}
+
+// GELU with the exact error function: 0.5 x (1 + erf(x / sqrt(2))).
+void lo_gelu(const double* x, int64_t n, double* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = 0.5 * x[i] * (1.0 + std::erf(x[i] / std::sqrt(2.0)));
+}
+
+// The MLP activation applied to a bf16 tensor (the up layer's bf16 output): H = bf16(GELU(Y)).
+void lo_gelu_bf16(const uint16_t* Y, int64_t n, uint16_t* H) {
+  for (int64_t i = 0; i < n; ++i) {
+    const double y = widen_one(Y[i]);
+    H[i] = lo_round_bf16_one(0.5 * y * (1.0 + std::erf(y / std::sqrt(2.0))));
+  }
+}
+
 }  // extern "C"

@@ -36,7 +36,8 @@ import numpy as np
 
 __all__ = [
     "widen", "select_2of4", "keep_mask", "norm_scale", "sparsify", "canonical_meta",
-    "linear", "linear_dense", "linear_wsparse", "lora_down", "NIBBLE_OF_PAIR",
+    "linear", "linear_dense", "linear_wsparse", "lora_down", "round_bf16", "gelu", "gelu_bf16", "mlp_input",
+    "NIBBLE_OF_PAIR",
 ]
 
 #: 4-bit metadata of a kept index pair (i0 < i1): i0 in bits 0-1, i1 in bits 2-3.
@@ -185,3 +186,39 @@ def linear_wsparse(X, W, LA=None, LB=None, rows=None) -> np.ndarray:
     if LA is not None and LB is not None:
         y = y + (x @ widen(LB).T) @ widen(LA).T
     return y
+
+
+def round_bf16(x) -> np.ndarray:
+    """Nearest bf16 value (8 significant bits, ties to even) of float64 values, as uint16 bit patterns.
+
+    Magnitudes below 2^-126 round on the subnormal grid of 2^-133; values beyond the largest bf16 become
+    infinity.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    m, e = np.frexp(a)                                   # a = m 2^e, m in [0.5, 1)
+    normal = e >= -125
+    r = np.where(normal, np.rint(np.ldexp(m, 8)), np.rint(np.ldexp(a, 133)))  # rint: ties to even
+    v = np.where(normal, np.ldexp(r, e - 8), np.ldexp(r, -133))
+    v = np.where(v > 3.3895313892515355e38, np.inf, v)
+    f = np.copysign(v, x).astype(np.float32)
+    return (f.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+
+def gelu(x) -> np.ndarray:
+    """GELU with the exact error function, 0.5 x (1 + erf(x / sqrt 2)), in float64 (scipy's erf)."""
+    from scipy.special import erf
+    x = np.asarray(x, dtype=np.float64)
+    return 0.5 * x * (1.0 + erf(x / np.sqrt(2.0)))
+
+
+def gelu_bf16(Y) -> np.ndarray:
+    """H = bf16(GELU(Y)) of a bf16 tensor Y (the MLP activation applied to the up layer's bf16 output)."""
+    return round_bf16(gelu(widen(Y)))
+
+
+def mlp_input(X, W, LA=None, LB=None, sparse=True, rows=None) -> np.ndarray:
+    """The MLP down layer's input for the given rows: H = bf16(GELU(bf16(Y_up))), with Y_up the up layer
+    (sparse: ``linear``, else ``linear_dense``) in float64, rounded to the up layer's bf16 output first."""
+    y = linear(X, W, LA, LB, rows) if sparse else linear_dense(X, W, LA, LB, rows)
+    return gelu_bf16(round_bf16(y))

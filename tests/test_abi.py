@@ -130,12 +130,24 @@ def test_force_split_range(asl):
     assert L.lynx_debug_prologue_split(0, 3072) == 0 and L.lynx_debug_prologue_split(64, 24) == 0  # host checks
 
 
+def test_force_ksplit_range(asl):
+    L = asl.lib
+    try:
+        for bad in (-1, 5, 64):
+            assert L.lynx_debug_force_ksplit(bad) == -7
+        for ok in (1, 2, 3, 4):
+            assert L.lynx_debug_force_ksplit(ok) == 0
+    finally:
+        assert L.lynx_debug_force_ksplit(0) == 0
+    assert L.lynx_debug_linear_ksplit(0, 16, 16) == 0 and L.lynx_debug_linear_ksplit(16, 16, 24) == 0
+
+
 def test_force_tile_accepts_only_built_shapes(asl):
     L = asl.lib
     try:
-        for rows, cols in [(512, 256), (256, 192), (384, 224), (1, 1), (0, 224)]:
+        for rows, cols in [(512, 256), (256, 224), (384, 224), (1, 1), (0, 224)]:
             assert L.lynx_debug_force_tile(rows, cols) == -7
-        for rows, cols in [(512, 224), (512, 192), (256, 256)]:
+        for rows, cols in [(512, 224), (512, 192), (256, 256), (256, 192)]:
             assert L.lynx_debug_force_tile(rows, cols) == 0
     finally:
         assert L.lynx_debug_force_tile(0, 0) == 0

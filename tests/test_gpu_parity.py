@@ -114,7 +114,7 @@ def _layer(M, N, K, seed=7, xkind="act"):
     return X, W, LA, LB
 
 
-@pytest.mark.parametrize("tile", [(512, 224), (512, 192), (256, 256)])  # sparse pair tile shapes
+@pytest.mark.parametrize("tile", [(512, 224), (512, 192), (256, 256), (256, 192)])  # sparse pair tile shapes
 @pytest.mark.parametrize("M,N,K", LINEAR_CASES)
 def test_linear_full_comparison(lynx, M, N, K, tile):
     X, W, LA, LB = _layer(M, N, K)
@@ -242,7 +242,7 @@ def test_mma_rate_microbenchmark_runs(lynx):
 WSPARSE_CASES = [(256, 512, 512), (300, 520, 528), (1, 8, 16), (200, 1003, 256), (600, 1160, 384), (129, 136, 3072)]
 
 
-@pytest.mark.parametrize("tile", [(512, 224), (512, 192), (256, 256)])
+@pytest.mark.parametrize("tile", [(512, 224), (512, 192), (256, 256), (256, 192)])
 @pytest.mark.parametrize("M,N,K", WSPARSE_CASES)
 def test_weight_sparse_linear(lynx, M, N, K, tile):
     """Y = X W~^T + X (LA LB)^T with W pruned and compressed by the sparsify pass: the GEMM runs W~ as the
@@ -273,3 +273,65 @@ def test_weight_sparse_on_24_weights_matches_dense_layer(lynx):
     assert_y_close(to_bits(Y), O.linear_dense(X, W))
     assert float((Y.float() - Yd.float()).abs().max()) <= float(Yd.float().abs().max()) * 2 ** -7
     torch.cuda.synchronize()
+
+
+# ------------------------------------------------------------------ split K (few output tiles)
+@pytest.mark.parametrize("tile", [(256, 256), (256, 192)])
+@pytest.mark.parametrize("splits", [2, 3])
+@pytest.mark.parametrize("M,N,K", LINEAR_CASES)
+def test_linear_split_k(lynx, M, N, K, splits, tile):
+    """The one-row-block sparse tiles with each tile's k-steps split over work units: every unit writes an fp32
+    partial, the last one to finish adds them in split order; the LoRA stage runs in the last split."""
+    X, W, LA, LB = _layer(M, N, K, seed=27)
+    lynx.lynx_debug_force_tile(*tile)
+    lynx.lynx_debug_force_ksplit(splits)
+    try:
+        Y = lynx.lynx_linear(to_dev(X), to_dev(W), to_dev(LA), to_dev(LB))
+        assert lynx.lynx_sync_status() == 0
+    finally:
+        lynx.lynx_debug_force_ksplit(0)
+        lynx.lynx_debug_force_tile(0, 0)
+    assert_y_close(to_bits(Y), O.linear(X, W, LA, LB))
+
+
+def test_split_k_is_deterministic_and_reuses_its_workspace(lynx):
+    """Arrival order varies between runs, the split order of the sum does not: repeated calls on one workspace
+    (whose counters the pre-pass zeroes every call) give the same bits."""
+    import torch
+    M, N, K = 1024, 768, 3072
+    X, W, LA, LB = (to_dev(a) for a in _layer(M, N, K, seed=29))
+    lynx.lynx_debug_force_tile(256, 256)
+    lynx.lynx_debug_force_ksplit(3)
+    try:
+        assert lynx.lynx_debug_linear_ksplit(M, N, K) == 3
+        ws = torch.empty(lynx.lynx_workspace_bytes(M, N, K), dtype=torch.uint8, device="cuda")
+        outs = [to_bits(lynx.lynx_linear(X, W, LA, LB, workspace=ws)) for _ in range(3)]
+        assert lynx.lynx_sync_status() == 0
+    finally:
+        lynx.lynx_debug_force_ksplit(0)
+        lynx.lynx_debug_force_tile(0, 0)
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+    assert_y_close(outs[0], O.linear(to_bits(X), to_bits(W), to_bits(LA), to_bits(LB)))
+
+
+def test_split_k_choice_and_workspace_fallback(lynx):
+    """On this GPU a short, wide-K problem (256 tokens through the MLP down shape: 16 tiles of 256 x 192) splits;
+    the DiT shapes do not (the MLP down shape at 1024 tokens fills one wave with 64 tiles of 256 x 192).  A
+    workspace holding only the base part runs the unsplit schedule and gives the oracle's answer too."""
+    import torch
+    assert lynx.lynx_debug_linear_ksplit(256, 3072, 12288) > 1
+    for M, N, K in [(4608, 9216, 3072), (4608, 3072, 12288), (16384, 9216, 3072), (1024, 9216, 3072),
+                    (1024, 3072, 12288)]:
+        assert lynx.lynx_debug_linear_ksplit(M, N, K) == 1, (M, N, K)
+    M, N, K = 256, 1536, 3072
+    X, W, LA, LB = _layer(M, N, K, seed=31)
+    lynx.lynx_debug_force_ksplit(0)
+    full = lynx.lynx_workspace_bytes(M, N, K)
+    lynx.lynx_debug_force_ksplit(1)
+    base = lynx.lynx_workspace_bytes(M, N, K)
+    lynx.lynx_debug_force_ksplit(0)
+    assert lynx.lynx_debug_linear_ksplit(M, N, K) > 1 and full > base
+    ws = torch.empty(base, dtype=torch.uint8, device="cuda")
+    Y = lynx.lynx_linear(to_dev(X), to_dev(W), to_dev(LA), to_dev(LB), workspace=ws)
+    assert lynx.lynx_sync_status() == 0
+    assert_y_close(to_bits(Y), O.linear(X, W, LA, LB))

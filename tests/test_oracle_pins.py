@@ -336,6 +336,57 @@ def test_lora_down_recombination(O):
     assert np.allclose(s[:, None] * acc, O.linear(X, W, LA, LB), rtol=1e-14, atol=0)
 
 
+# ----------------------------------------------------------------------------- the MLP activation (GELU of the up output)
+def pin_gelu(O):
+    """Closed forms: GELU(x) = x Phi(x); Phi(1) = 0.8413447460685429, Phi(-1) = 1 - Phi(1); GELU(0) = 0;
+    GELU(x) - GELU(-x) = x (Phi(x) + Phi(-x) = 1); GELU(x) -> x and GELU(-x) -> 0 for large x."""
+    g = O.gelu(np.array([1.0, -1.0, 0.0, 10.0, -10.0, 2.5, -2.5]))
+    assert abs(g[0] - 0.8413447460685429) < 1e-15
+    assert abs(g[1] + 0.15865525393145707) < 1e-15
+    assert g[2] == 0.0
+    assert abs(g[3] - 10.0) < 1e-14 and abs(g[4]) < 1e-14
+    assert abs((g[5] - g[6]) - 2.5) < 1e-14
+
+
+def pin_round_bf16(O):
+    """Ties go to even on the 2^-7 grid of [1, 2); exactly representable values are kept; the grid of [2^k, 2^k+1)
+    scales; every float32 rounds as torch rounds float32 to bf16."""
+    ulp = 2.0 ** -7
+    cases = [(1.0, 0x3F80), (1.0 + ulp / 2, 0x3F80), (1.0 + 1.5 * ulp, 0x3F82), (1.0 + ulp / 2 + 1e-12, 0x3F81),
+             (-1.0 - ulp / 2, 0xBF80), (3.0, 0x4040), (0.0, 0x0000), (-0.0, 0x8000), (1e39, 0x7F80)]
+    got = O.round_bf16(np.array([c[0] for c in cases]))
+    assert got.tolist() == [c[1] for c in cases], [hex(v) for v in got]
+    import torch
+    f = np.random.default_rng(3).standard_normal(20000).astype(np.float32) * np.float32(7.0)
+    want = torch.from_numpy(f).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(O.round_bf16(f.astype(np.float64)), want)
+
+
+def test_gelu_closed_forms(O):
+    pin_gelu(O)
+
+
+def test_round_bf16(O):
+    pin_round_bf16(O)
+
+
+def test_gelu_bf16_is_round_of_gelu(O):
+    Y = synth.gaussian_bf16((4, 5), (16, 64), 2.0)
+    assert np.array_equal(O.gelu_bf16(Y), O.round_bf16(O.gelu(exact_widen(Y))))
+
+
+def test_mlp_input_chains_the_up_layer(O):
+    """H = bf16(GELU(bf16(Y_up))) row by row, with Y_up the up layer (sparse or dense)."""
+    g = np.random.default_rng(17)
+    M, N, K, R = 6, 16, 24, 2
+    X, W, LA, LB = (bits(g.standard_normal(sh)) for sh in [(M, K), (N, K), (N, R), (R, K)])
+    for sparse in (True, False):
+        y = O.linear(X, W, LA, LB) if sparse else O.linear_dense(X, W, LA, LB)
+        want = O.gelu_bf16(O.round_bf16(y))
+        assert np.array_equal(O.mlp_input(X, W, LA, LB, sparse=sparse), want)
+        assert np.array_equal(O.mlp_input(X, W, LA, LB, sparse=sparse, rows=[4, 1]), want[[4, 1]])
+
+
 # ----------------------------------------------------------------------------- the two oracles agree
 @pytest.mark.parametrize("M,K,kind", [(33, 64, "act"), (40, 256, "mixed"), (16, 512, "ties"), (64, 3072, "gelu")])
 def test_cpp_and_numpy_oracles_agree(M, K, kind):
@@ -449,6 +500,8 @@ PINS = {
     "wsparse_loops": lambda O: pin_wsparse_loops(O, 0),
     "dense_loops": pin_dense_loops,
     "meta_decode": pin_meta_decodes_to_mask,
+    "gelu": pin_gelu,
+    "round_bf16": pin_round_bf16,
 }
 
 
@@ -494,6 +547,10 @@ CPP_MUTATIONS = [
      ["hand_lora_down"]),
     ("weight pruning skipped", "if (!keep[static_cast<size_t>(k)]) wt[static_cast<size_t>(n * K + k)] = 0.0;",
      "(void)keep;", ["wsparse_loops"]),
+    ("GELU with tanh argument", "0.5 * x[i] * (1.0 + std::erf(x[i] / std::sqrt(2.0)))",
+     "0.5 * x[i] * (1.0 + std::tanh(x[i] / std::sqrt(2.0)))", ["gelu"]),
+    ("bf16 rounding truncates", "r = std::nearbyint(std::ldexp(m, 8));", "r = std::trunc(std::ldexp(m, 8));",
+     ["round_bf16"]),
     ("dense layer drops its LoRA", "if (LA) lora_row(x.data(), la.data(), lb.data(), N, K, R, yr.data());\n"
      "    for (int64_t n = 0; n < N; ++n) Y[i * N + n] = y[static_cast<size_t>(n)] + yr[static_cast<size_t>(n)];\n"
      "  });\n  return 0;\n}\n\n// The weight-2:4",
