@@ -25,13 +25,14 @@ __all__ = [
     "lynx_debug_force_ksplit", "lynx_debug_linear_ksplit",
     "lynx_profile_next", "lynx_linear_kernel_count", "lynx_mma_rate",
     "LynxLayer", "lynx_layer", "lynx_layers_workspace_bytes", "lynx_run_layers", "LynxGraph",
-    "LYNX_LAYER_SPARSE", "LYNX_LAYER_GELU", "lynx_debug_pair_offsets",
+    "LYNX_LAYER_SPARSE", "LYNX_LAYER_GELU", "LYNX_LAYER_FUSE_SPARSIFY", "lynx_debug_pair_offsets",
 ]
 
 LYNX_OK = 0
 LYNX_ERR_TIMEOUT = -6
 LYNX_LAYER_SPARSE = 1
 LYNX_LAYER_GELU = 2
+LYNX_LAYER_FUSE_SPARSIFY = 4
 
 _c_i64, _c_sz, _c_p = ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p
 
@@ -320,11 +321,11 @@ def lynx_debug_prologue_split(M: int, K: int) -> int:
 
 
 # ------------------------------------------------------------------ layer sequences and their CUDA graphs
-def lynx_layer(X, W, LA=None, LB=None, Y=None, sparse: bool = True, gelu: bool = False) -> dict:
+def lynx_layer(X, W, LA=None, LB=None, Y=None, sparse: bool = True, gelu: bool = False, fuse: bool = False) -> dict:
     """One layer of a sequence: Y = lynx_linear(X, W, LA, LB) (sparse) or lynx_linear_dense(X, W, LA, LB), passed
-    through the exact-erf GELU when ``gelu`` (the MLP up layer; a following sparse layer that reads this Y runs
-    fused with it, see include/lynx.h).  Allocates Y (M x N bf16) when not given.  The dict keeps the tensors
-    alive."""
+    through GELU when ``gelu`` (the MLP up layer).  ``fuse`` (with ``gelu``): a following sparse layer that reads
+    this Y runs fused with it (include/lynx.h, LYNX_LAYER_FUSE_SPARSIFY).  Allocates Y (M x N bf16) when not given.
+    The dict keeps the tensors alive."""
     torch = _torch()
     _need(X, "X", torch.bfloat16)
     _need(W, "W", torch.bfloat16)
@@ -332,14 +333,15 @@ def lynx_layer(X, W, LA=None, LB=None, Y=None, sparse: bool = True, gelu: bool =
     N = W.shape[0]
     R = 64 if LB is None else LB.shape[0]
     Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device) if Y is None else Y
-    return {"sparse": bool(sparse), "gelu": bool(gelu), "X": X, "W": W, "LA": LA, "LB": LB, "Y": Y, "M": M, "N": N,
-            "K": K, "R": R}
+    return {"sparse": bool(sparse), "gelu": bool(gelu), "fuse": bool(fuse), "X": X, "W": W, "LA": LA, "LB": LB, "Y": Y,
+            "M": M, "N": N, "K": K, "R": R}
 
 
 def _c_layer_array(layers):
     arr = (LynxLayer * max(len(layers), 1))()
     for i, l in enumerate(layers):
-        flags = (LYNX_LAYER_SPARSE if l["sparse"] else 0) | (LYNX_LAYER_GELU if l.get("gelu") else 0)
+        flags = ((LYNX_LAYER_SPARSE if l["sparse"] else 0) | (LYNX_LAYER_GELU if l.get("gelu") else 0) |
+                 (LYNX_LAYER_FUSE_SPARSIFY if l.get("fuse") else 0))
         arr[i] = LynxLayer(flags, _ptr(l["X"]), _ptr(l["W"]), _ptr(l["LA"]), _ptr(l["LB"]), _ptr(l["Y"]),
                            l["M"], l["N"], l["K"], l["R"])
     return arr

@@ -385,7 +385,7 @@ int dense_impl(const void* X, const void* W, const void* LA, const void* LB, voi
 }
 
 // ---------------------------------------------------------------- layer sequences and the fused MLP pair
-constexpr int32_t kKnownFlags = LYNX_LAYER_SPARSE | LYNX_LAYER_GELU;
+constexpr int32_t kKnownFlags = LYNX_LAYER_SPARSE | LYNX_LAYER_GELU | LYNX_LAYER_FUSE_SPARSIFY;
 
 bool is_sparse(const lynx_layer& l) { return (l.flags & LYNX_LAYER_SPARSE) != 0; }
 bool is_gelu(const lynx_layer& l) { return (l.flags & LYNX_LAYER_GELU) != 0; }
@@ -412,7 +412,8 @@ struct PairPlan {
 };
 
 bool fusable(const lynx_layer& up, const lynx_layer& dn) {
-  return is_gelu(up) && is_sparse(dn) && !is_gelu(dn) && dn.X == up.Y && dn.M == up.M && dn.K == up.N &&
+  return is_gelu(up) && (up.flags & LYNX_LAYER_FUSE_SPARSIFY) && is_sparse(dn) && !is_gelu(dn) && dn.X == up.Y &&
+         dn.M == up.M && dn.K == up.N &&
          up.N % kMetaBlockCols == 0 && !(up.flags & ~kKnownFlags) && !(dn.flags & ~kKnownFlags);
 }
 

@@ -512,10 +512,9 @@ def main() -> int:
 
     # The block stack of the fifth workload: 8 blocks x (QKV sparse 3072->9216, out dense 3072->3072, up dense
     # 3072->12288 followed by the MLP's GELU, down sparse 12288->3072 on that GELU output), rank-64 LoRA on the
-    # sparse layers, the seeded weights of every block and the seeded block input from synth.  The up and down
-    # layers form the MLP pair, which this library runs fused (the up layer's epilogue applies GELU and
-    # sparsifies its output for the down layer).  Against it: the same 32 linears dense through cuBLAS with the
-    # same GELU (torch) between up and down.  Both sides run eagerly and as one CUDA graph each.
+    # sparse layers, the seeded weights of every block and the seeded block input from synth.  The up layer's
+    # epilogue applies the GELU.  Against it: the same 32 linears dense through cuBLAS with the same GELU (torch)
+    # between up and down.  Both sides run eagerly and as one CUDA graph each.
     import torch.nn.functional as F
     stack = {}
 
@@ -583,7 +582,7 @@ def main() -> int:
     torch.cuda.empty_cache()
 
     # The MLP pair of the third workload (4608 tokens: up 3072->12288 sparse with LoRA, GELU, down 12288->3072
-    # sparse with LoRA), fused through the layer sequence, against cuBLAS up, GELU (torch) and cuBLAS down.
+    # sparse with LoRA) through the layer sequence, unfused and fused, against cuBLAS up, GELU (torch), cuBLAS down.
     tu = synth.layer_tensors("mlp", "up")
     td = synth.layer_tensors("mlp", "down", with_x=False)
     Mm = tu["M"]
@@ -591,12 +590,16 @@ def main() -> int:
     hu = torch.empty((Mm, 12288), dtype=torch.bfloat16, device=dev)
     yd = torch.empty((Mm, 3072), dtype=torch.bfloat16, device=dev)
     wu, wd = to_dev(tu["W"]), to_dev(td["W"])
-    pair = [asl.lynx_layer(xu, wu, to_dev(tu["LA"]), to_dev(tu["LB"]), hu, sparse=True, gelu=True),
-            asl.lynx_layer(hu, wd, to_dev(td["LA"]), to_dev(td["LB"]), yd, sparse=True)]
-    ws_p = torch.empty(asl.lynx_layers_workspace_bytes(pair), dtype=torch.uint8, device=dev)
+    lau, lbu, lad, lbd = to_dev(tu["LA"]), to_dev(tu["LB"]), to_dev(td["LA"]), to_dev(td["LB"])
+    pair = [asl.lynx_layer(xu, wu, lau, lbu, hu, sparse=True, gelu=True),
+            asl.lynx_layer(hu, wd, lad, lbd, yd, sparse=True)]
+    fused = [asl.lynx_layer(xu, wu, lau, lbu, hu, sparse=True, gelu=True, fuse=True),
+             asl.lynx_layer(hu, wd, lad, lbd, yd, sparse=True)]
+    ws_p = torch.empty(asl.lynx_layers_workspace_bytes(fused), dtype=torch.uint8, device=dev)
     tt = []
     for fn in (lambda: asl.lynx_run_layers(pair, ws_p, stream=stream),
-               lambda: torch.matmul(F.gelu(torch.matmul(xu, wu.t())), wd.t(), out=yd)):
+               lambda: torch.matmul(F.gelu(torch.matmul(xu, wu.t())), wd.t(), out=yd),
+               lambda: asl.lynx_run_layers(fused, ws_p, stream=stream)):
         for _ in range(3):
             fn()
         torch.cuda.synchronize()
@@ -611,9 +614,11 @@ def main() -> int:
     assert st == 0, asl.lynx_status_string(st)
     fl = 2.0 * Mm * 12288 * 3072 * 2
     mlp_pair = {"lynx_ms": tt[0], "tflops": fl / (tt[0] * 1e-3) / 1e12, "cublas_gelu_ms": tt[1],
-                "x_vs_dense_cublas": tt[1] / tt[0],
-                "note": "up 4608x3072->12288 sparse+LoRA, GELU, down 12288->3072 sparse+LoRA (fused pair)"}
-    del xu, hu, yd, wu, wd, pair, ws_p
+                "x_vs_dense_cublas": tt[1] / tt[0], "lynx_fused_sparsify_ms": tt[2],
+                "note": "up 4608x3072->12288 sparse+LoRA, GELU in its epilogue, down 12288->3072 sparse+LoRA with "
+                        "its own sparsify pass; lynx_fused_sparsify_ms: the down layer's sparsification written by "
+                        "the up layer's epilogue instead (LYNX_LAYER_FUSE_SPARSIFY)"}
+    del xu, hu, yd, wu, wd, pair, fused, ws_p, lau, lbu, lad, lbd
     torch.cuda.empty_cache()
 
     # End to end through the C-ABI with host buffers, pipelined as a serving loop runs it: every step copies
@@ -708,7 +713,7 @@ def main() -> int:
             "other_shapes": shapes,
             "sparsify_alone": sparsify_alone,
             "block_stack_32_linears": stack,
-            "mlp_pair_fused": mlp_pair,
+            "mlp_pair": mlp_pair,
             "mma_microbench": {"dense_tflops": mma_dense_tf, "sparse_tflops_effective": mma_sparse_tf,
                                "dense_macs_per_clk": mma_dense_mpc, "sparse_macs_per_clk_effective": mma_sparse_mpc,
                                "sparse_over_dense": mma_sparse_tf / mma_dense_tf,

@@ -189,18 +189,21 @@ LYNX_API int lynx_linear_dense(const void* X, const void* W, const void* LA, con
  * pointers and layouts as for those calls.  A layer may read the Y of an
  * earlier layer of the same sequence.
  *
- * The MLP pair: when a GELU layer is followed by a sparse layer whose X is
- * that Y (same pointer and M, its K equal to the GELU layer's N, N % 128 == 0),
- * the sequence runs the pair fused ("RT-Lynx" page, CUDA kernel optimisation:
- * one execution path for the online sparsification): the GELU layer's
- * epilogue also writes the 2:4 values, metadata and partial row norms of its
- * output, and the sparse layer's sparsify pass is replaced by a LoRA
- * down-projection that finishes s and T'.  Y of the GELU layer is still
- * written; the results equal those of the two layers run one by one, up to the
- * fp32 summation order of the row norms.  The fused pair needs more workspace
- * (lynx_layers_workspace_bytes counts it); with less, the pair runs unfused. */
+ * The fused MLP pair: a GELU layer with LYNX_LAYER_FUSE_SPARSIFY, followed by
+ * a sparse layer whose X is that Y (same pointer and M, its K equal to the
+ * GELU layer's N, N % 128 == 0), runs as one pair ("RT-Lynx" page, CUDA
+ * kernel optimisation: one execution path for the online sparsification):
+ * the GELU layer's epilogue also writes the 2:4 values, metadata and partial
+ * row norms of its output, and the sparse layer's sparsify pass is replaced
+ * by a LoRA down-projection that finishes s and T'.  Y of the GELU layer is
+ * still written; the results equal those of the two layers run one by one, up
+ * to the fp32 summation order of the row norms.  The fused pair needs more
+ * workspace (lynx_layers_workspace_bytes counts it); with less, or without the
+ * flag, the pair runs as two layers (the GELU epilogue, then the sparse
+ * layer's own sparsify pass), which measures faster on GB300. */
 #define LYNX_LAYER_SPARSE 1
 #define LYNX_LAYER_GELU 2
+#define LYNX_LAYER_FUSE_SPARSIFY 4
 typedef struct {
   int32_t flags;
   const void* X;
@@ -219,7 +222,7 @@ LYNX_API size_t lynx_layers_workspace_bytes(const lynx_layer* layers, int32_t n)
 /* Enqueues the n layers in order on `stream` (asynchronous).  Every layer is
  * checked on the host first: if one fails, nothing is enqueued, its status is
  * returned and its index is stored in *failed_layer (when failed_layer is not
- * NULL; -1 otherwise).  Flags other than the two above give
+ * NULL; -1 otherwise).  Flags other than the three above give
  * LYNX_ERR_UNSUPPORTED.  n = 0 enqueues nothing and returns LYNX_OK. */
 LYNX_API int lynx_run_layers(const lynx_layer* layers, int32_t n, void* workspace, size_t workspace_bytes,
                              void* stream, int32_t* failed_layer);

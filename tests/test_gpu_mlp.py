@@ -57,11 +57,11 @@ def _mlp_tensors(M, K, Nup, Nd, seed, up_sparse=True):
     return X, Wu, LAu, LBu, Wd, LAd, LBd
 
 
-def _run_pair(lynx, X, Wu, LAu, LBu, Wd, LAd, LBd, up_sparse, workspace_bytes=None):
+def _run_pair(lynx, X, Wu, LAu, LBu, Wd, LAd, LBd, up_sparse, workspace_bytes=None, fuse=True):
     import torch
     Xd = to_dev(X)
     up = lynx.lynx_layer(Xd, to_dev(Wu), None if LAu is None else to_dev(LAu), None if LBu is None else to_dev(LBu),
-                         sparse=up_sparse, gelu=True)
+                         sparse=up_sparse, gelu=True, fuse=fuse)
     dn = lynx.lynx_layer(up["Y"], to_dev(Wd), to_dev(LAd), to_dev(LBd), sparse=True)
     layers = [up, dn]
     need = lynx.lynx_layers_workspace_bytes(layers)
@@ -126,19 +126,29 @@ def test_fused_pair_dense_up(lynx, M, K, Nup, Nd):
     _check_pair(lynx, layers, ws, *t, up_sparse=False)
 
 
-def test_fused_pair_equals_unfused_selection_and_y(lynx):
-    """With a workspace too small for the fused plan the pair runs unfused (the down layer's own sparsify pass):
-    the same H, the same Y within tolerance (only the fp32 summation order of the row norms differs)."""
+@pytest.mark.parametrize("how", ["small workspace", "no fuse flag"])
+def test_fused_pair_equals_unfused_selection_and_y(lynx, how):
+    """Without the fuse flag, or with a workspace too small for the fused plan, the pair runs unfused (the GELU
+    epilogue, then the down layer's own sparsify pass): the same H, the same Y within tolerance (only the fp32
+    summation order of the row norms differs)."""
     M, K, Nup, Nd = 384, 512, 1024, 256
     t = _mlp_tensors(M, K, Nup, Nd, seed=41)
     fused, ws = _run_pair(lynx, *t, up_sparse=True)
     small = max(lynx.lynx_workspace_bytes(M, Nup, K), lynx.lynx_workspace_bytes(M, Nd, Nup))
     assert small < lynx.lynx_debug_pair_offsets(fused, 0)["total"]
-    unfused, _ = _run_pair(lynx, *t, up_sparse=True, workspace_bytes=small)
+    if how == "small workspace":
+        unfused, _ = _run_pair(lynx, *t, up_sparse=True, workspace_bytes=small)
+    else:
+        unfused, _ = _run_pair(lynx, *t, up_sparse=True, fuse=False)
+        with pytest.raises(lynx.LynxError):
+            lynx.lynx_debug_pair_offsets(unfused, 0)
+        assert lynx.lynx_layers_workspace_bytes(unfused) == small
     assert np.array_equal(to_bits(fused[0]["Y"]), to_bits(unfused[0]["Y"]))
     yf, yu = to_bits(fused[1]["Y"]), to_bits(unfused[1]["Y"])
     assert_y_close(yf, widen(yu), "fused vs unfused")
     assert np.mean(yf == yu) > 0.98
+    rows = np.arange(0, M, 7)
+    assert_y_close(yu[rows], O.linear(to_bits(unfused[0]["Y"])[rows], t[4], t[5], t[6]), "unfused Y on the GPU's H")
 
 
 def test_gelu_layer_alone(lynx):
