@@ -19,7 +19,7 @@ __all__ = [
     "LynxError", "lib", "LYNX_OK", "LYNX_ERR_TIMEOUT",
     "lynx_meta_bytes", "lynx_workspace_bytes", "lynx_dense_workspace_bytes",
     "lynx_sparsify", "lynx_sparsify_lora", "lynx_lora_down", "lynx_linear",
-    "lynx_linear_dense", "lynx_prune_weight", "lynx_linear_wsparse",
+    "lynx_linear_dense", "lynx_linear_fused", "lynx_prune_weight", "lynx_linear_wsparse",
     "lynx_sync_status", "lynx_status_string", "lynx_meta_to_canonical", "lynx_debug_set_fault",
     "lynx_debug_force_tile", "lynx_debug_force_split", "lynx_debug_prologue_split",
     "lynx_debug_force_ksplit", "lynx_debug_linear_ksplit",
@@ -61,6 +61,8 @@ def _load() -> ctypes.CDLL:
         "lynx_sparsify_lora": (ctypes.c_int, [_c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_p, _c_p, _c_p, _c_p, _c_p]),
         "lynx_linear": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_i64, _c_p, _c_sz, _c_p]),
         "lynx_linear_dense": (ctypes.c_int,
+                              [_c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_i64, _c_p, _c_sz, _c_p]),
+        "lynx_linear_fused": (ctypes.c_int,
                               [_c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_i64, _c_p, _c_sz, _c_p]),
         "lynx_linear_wsparse": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_i64,
                                                 _c_p, _c_sz, _c_p]),
@@ -216,6 +218,23 @@ def lynx_linear_dense(X, W, LA=None, LB=None, Y=None, workspace=None, stream=Non
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib.lynx_linear_dense(_ptr(X), _ptr(W), _ptr(LA), _ptr(LB), _ptr(Y), M, N, K, R, _ptr(workspace), wbytes,
                                  _stream(stream)), "lynx_linear_dense")
+    return Y
+
+
+def lynx_linear_fused(X, W, LA, LB, Y=None, workspace=None, stream=None):
+    """Y = S(X) W^T + X (LA LB)^T with the 2:4 selection inside the GEMM (no sparsify pass; see include/lynx.h)."""
+    torch = _torch()
+    for t, n in ((X, "X"), (W, "W"), (LA, "LA"), (LB, "LB")):
+        _need(t, n, torch.bfloat16)
+    M, K = X.shape
+    N = W.shape[0]
+    R = LB.shape[0]
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device) if Y is None else Y
+    if workspace is None:
+        workspace = torch.empty(lynx_dense_workspace_bytes(M, R), dtype=torch.uint8, device=X.device)
+    wbytes = workspace.numel() * workspace.element_size()
+    _check(lib.lynx_linear_fused(_ptr(X), _ptr(W), _ptr(LA), _ptr(LB), _ptr(Y), M, N, K, R, _ptr(workspace), wbytes,
+                                 _stream(stream)), "lynx_linear_fused")
     return Y
 
 

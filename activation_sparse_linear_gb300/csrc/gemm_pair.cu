@@ -83,12 +83,15 @@ enum Site : int { SITE_PRODUCER = 11, SITE_MMA = 12, SITE_EPILOGUE = 13, SITE_DR
 // 64-channel sub-tiles; one metadata chunk per row block) feeding four tcgen05.mma.sp per row block;
 // dense = 64 channels feeding four tcgen05.mma per row block.  Several MMAs per barrier round keep the
 // single issuing thread ahead of the tensor pipe.
-template <bool SPARSE, int MB, int TN>
+// F1 (sparse, one row block): the stage carries the dense X tile (two 64-channel boxes per row block) instead of
+// compressed values; the epilogue warps select in registers and write the compressed values over box 0 and the
+// metadata chunk into the stage before the MMAs read them.
+template <bool SPARSE, int MB, int TN, bool F1 = false>
 struct PairCfg {
   static constexpr int ROWS = MB * BLOCK;    // rows per CTA
   static constexpr int HALF_N = TN / 2;      // W rows staged per CTA
   static constexpr int BK = SPARSE ? 128 : kDenseBK;
-  static constexpr int BOXES = SPARSE ? 1 : kDenseBK / 64;  // 64-channel (128-byte) A boxes per row block and stage
+  static constexpr int BOXES = SPARSE ? (F1 ? 2 : 1) : kDenseBK / 64;  // 64-channel (128-byte) A boxes per row block and stage
   static constexpr int A_BOX = BLOCK * 128;
   static constexpr int A_BLOCK = BOXES * A_BOX;
   static constexpr int A_SLOT = MB * A_BLOCK;
@@ -96,6 +99,7 @@ struct PairCfg {
   static constexpr int B_SLOT = SPARSE ? 2 * SUB : BOXES * SUB;
   static constexpr int M_SLOT = SPARSE ? MB * kMetaChunkBytes : 0;
   static constexpr int STAGE = A_SLOT + B_SLOT + M_SLOT;
+  static constexpr int LOAD_BYTES = F1 ? A_SLOT + B_SLOT : STAGE;  // TMA bytes of a k-step per CTA
   // Output staging boxes per epilogue warp: two, so that a box is refilled while the other is stored; one
   // for the sparse 256 x 256 tile, whose short 128-channel steps need a fourth operand stage in its place
   // (its few row tiles share each W tile between few CTA pairs, so its loads often come from DRAM).
@@ -115,7 +119,8 @@ struct PairCfg {
   static_assert(TN % 32 == 0 && TN <= 256 && HALF_N % 8 == 0, "MMA N");
   static_assert(META_COL + META_COLS <= TMEM_COLS, "TMEM budget");
   static_assert(ACC_BUFS * ACC_STRIDE <= TMEM_COLS, "TMEM budget of the accumulator buffers");
-  static_assert(8 * (2 * NST + 2 * ACC_BUFS + 3) + 32 <= 256, "barrier area");
+  static_assert(8 * (2 * NST + 2 * ACC_BUFS + 3 + (F1 ? 2 * NST + 1 : 0)) + 32 <= 256, "barrier area");
+  static_assert(!F1 || (SPARSE && MB == 1), "in-GEMM selection: sparse, one row block");
   static_assert(!SPARSE || NST <= META_RING, "a metadata group must outlive the stages in flight");
 };
 
@@ -156,10 +161,16 @@ __device__ __forceinline__ void store_chunk_t(void* Y, int64_t ldy, int zrow, in
 // bf16(GELU(bf16(y))) and, with a.hvals, the epilogue also sparsifies it for the next layer (the MLP pair's
 // up layer feeding its down layer: "RT-Lynx" page, CUDA kernel optimisation, one execution path for the online
 // sparsification).
-template <bool SPARSE, bool LORA, int MB, int TN, bool TRANS, bool SPLIT, bool GELU>
+// F1: the GEMM selects the 2:4 pattern itself ("RT-Lynx" page, CUDA kernel optimisation: 2:4 activations built
+// directly in registers): the producer loads dense X tiles; the epilogue warps, before draining a tile, take each
+// stage's X rows (two threads per row, 64 channels each), keep the top two of every four in registers, write the
+// compressed values and the metadata into the stage, add x^2 and kept x^2 over the tile's whole K, and at the
+// LoRA stage write T' = bf16(T / s) of their rows (T = X LB^T, unscaled, from a.lora_t) in place of a loaded T'.
+template <bool SPARSE, bool LORA, int MB, int TN, bool TRANS, bool SPLIT, bool GELU, bool F1 = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ PairArgs a) {
-  using C = PairCfg<SPARSE, MB, TN>;
+  using C = PairCfg<SPARSE, MB, TN, F1>;
+  static_assert(!F1 || (LORA && !TRANS && !SPLIT && !GELU), "in-GEMM selection variant");
   // With two row blocks, two threads issue the MMAs (one row block each): while one waits on a barrier or
   // does its per-stage bookkeeping, the other's queued MMAs keep the tensor pipe busy.
   constexpr int NISS = MB >= 2 ? 2 : 1;
@@ -175,12 +186,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   uint64_t* drain = acc_empty + C::ACC_BUFS;
   uint64_t* epi_bar = drain + 1;   // split-K: every epilogue warp of this CTA has written its partial
   uint64_t* epi_bar2 = drain + 2;  // split-K: the unit's arrival order is known
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 3);
+  uint64_t* conv_full = drain + 3;          // F1 [NST] (leader): both CTAs' selection of the stage is in place
+  uint64_t* xfull = conv_full + C::NST;     // F1 [NST]: this CTA's X tile of the stage has landed
+  uint64_t* s_bar = xfull + C::NST;         // F1: every epilogue warp of this CTA has written its rows' s
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 3 + (F1 ? 2 * C::NST + 1 : 0));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   volatile int* consumed_sh = abort_flag + 1;  // one count per MMA issuer
   volatile int* issued_sh = abort_flag + 3;
   volatile int* last_flag = abort_flag + 4;   // split-K: this CTA reduces the unit's tile
-  uint32_t* sel_table = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(full) + 256);  // GELU: 64 entries
+  uint32_t* sel_table = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(full) + 256);  // GELU, F1: 64 entries
+  float* s_sh = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 512);  // F1: s of the CTA's rows
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -210,19 +225,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     mbar_init(drain, NISS);
     mbar_init(epi_bar, EPI_WARPS);
     mbar_init(epi_bar2, 1);
+    if constexpr (F1)
+      for (int i = 0; i < C::NST; ++i) {
+        mbar_init(&conv_full[i], 2 * EPI_WARPS);  // every epilogue warp of both CTAs
+        mbar_init(&xfull[i], 1);                  // this CTA's producer (expect_tx)
+      }
+    if constexpr (F1) mbar_init(s_bar, EPI_WARPS);
     *abort_flag = 0;
     consumed_sh[0] = 0;
     consumed_sh[1] = 0;
     *issued_sh = 0;
     fence_mbar_init();
   }
-  if (GELU && threadIdx.x < 64) sel_table[threadIdx.x] = c_pair_select_table.e[threadIdx.x];
+  if ((GELU || F1) && threadIdx.x < 64) sel_table[threadIdx.x] = c_pair_select_table.e[threadIdx.x];
   if (threadIdx.x == 32) {
     prefetch_tmap(&a.tmA);
     prefetch_tmap(&a.tmB);
-    if (SPARSE) prefetch_tmap(&a.tmMeta);
+    if (SPARSE && !F1) prefetch_tmap(&a.tmMeta);
     if (LORA) {
-      prefetch_tmap(&a.tmT);
+      if (!F1) prefetch_tmap(&a.tmT);
       prefetch_tmap(&a.tmLA);
     }
     if (a.y_tma) prefetch_tmap(&a.tmY);
@@ -245,7 +266,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ TMA producer (both CTAs)
-      constexpr uint32_t STAGE_BYTES = C::STAGE;
+      constexpr uint32_t STAGE_BYTES = C::LOAD_BYTES;
       constexpr uint32_t LORA_BYTES = MB * C::A_BOX + C::SUB;  // T' (one box per row block) and this CTA's LA half
       const uint32_t full_leader0 = mapa_shared(&full[0], 0);  // the leader's full barriers, 8 B apart
       int g = 0, st = 0;
@@ -277,27 +298,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           const uint32_t fb = full_leader0 + 8 * st;
           if (!(a.ctl.inject == 1 && g == 0)) {  // test hook: the first stage never arrives
             if (kk < kend) {
-              if (leader) mbar_arrive_expect_tx(&full[st], 2 * STAGE_BYTES);
+              if constexpr (F1) {  // X (dense, two boxes per row block) lands on this CTA's own barrier
+                if (leader) mbar_arrive_expect_tx(&full[st], 2 * C::B_SLOT);
+                mbar_arrive_expect_tx(&xfull[st], C::A_SLOT);
 #pragma unroll
-              for (int h = 0; h < MB; ++h)
+                for (int h = 0; h < MB; ++h)
 #pragma unroll
-                for (int j = 0; j < C::BOXES; ++j)  // sparse: 64 kept values per row = 128 channels
-                  tma_load_2d_pair(sA + h * C::A_BLOCK + j * C::A_BOX, &a.tmA, fb, kk * (SPARSE ? 64 : C::BK) + 64 * j,
-                                   m0 + h * BLOCK);
+                  for (int j = 0; j < C::BOXES; ++j)
+                    tma_load_2d(sA + h * C::A_BLOCK + j * C::A_BOX, &a.tmA, &xfull[st], kk * 128 + 64 * j, m0 + h * BLOCK);
+              } else {
+                if (leader) mbar_arrive_expect_tx(&full[st], 2 * STAGE_BYTES);
+#pragma unroll
+                for (int h = 0; h < MB; ++h)
+#pragma unroll
+                  for (int j = 0; j < C::BOXES; ++j)  // sparse: 64 kept values per row = 128 channels
+                    tma_load_2d_pair(sA + h * C::A_BLOCK + j * C::A_BOX, &a.tmA, fb,
+                                     kk * (SPARSE ? 64 : C::BK) + 64 * j, m0 + h * BLOCK);
+              }
               if constexpr (SPARSE) {
                 tma_load_2d_pair(sB, &a.tmB, fb, kk * 128, n0);
                 tma_load_2d_pair(sB + C::SUB, &a.tmB, fb, kk * 128 + 64, n0);
+                if constexpr (!F1)
 #pragma unroll
-                for (int h = 0; h < MB; ++h)
-                  tma_load_2d_pair(sB + C::B_SLOT + h * kMetaChunkBytes, &a.tmMeta, fb, 0, meta_row[h] + 2 * kk);
+                  for (int h = 0; h < MB; ++h)
+                    tma_load_2d_pair(sB + C::B_SLOT + h * kMetaChunkBytes, &a.tmMeta, fb, 0, meta_row[h] + 2 * kk);
               } else {
 #pragma unroll
                 for (int j = 0; j < C::BOXES; ++j) tma_load_2d_pair(sB + j * C::SUB, &a.tmB, fb, kk * C::BK + 64 * j, n0);
               }
             } else {
-              if (leader) mbar_arrive_expect_tx(&full[st], 2 * LORA_BYTES);
+              if constexpr (F1) {  // T' comes from the epilogue warps; the stage is free for them to write
+                if (leader) mbar_arrive_expect_tx(&full[st], 2 * C::SUB);
+                mbar_arrive(&xfull[st]);
+              } else {
+                if (leader) mbar_arrive_expect_tx(&full[st], 2 * LORA_BYTES);
 #pragma unroll
-              for (int h = 0; h < MB; ++h) tma_load_2d_pair(sA + h * C::A_BLOCK, &a.tmT, fb, 0, m0 + h * BLOCK);
+                for (int h = 0; h < MB; ++h) tma_load_2d_pair(sA + h * C::A_BLOCK, &a.tmT, fb, 0, m0 + h * BLOCK);
+              }
               tma_load_2d_pair(sB, &a.tmLA, fb, 0, n0);
             }
           }
@@ -343,7 +380,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
         tc_fence_after();
         for (int it = 0; it < nst_u; ++it) {
-          if (!mbar_wait(&full[st], ph, a.ctl, SITE_MMA)) {
+          if (!mbar_wait(&full[st], ph, a.ctl, SITE_MMA) || (F1 && !mbar_wait(&conv_full[st], ph, a.ctl, SITE_MMA))) {
             *abort_flag = 1;
             stop = true;
             break;
@@ -433,13 +470,89 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const uint32_t taddr_warp = tmem + (static_cast<uint32_t>(q * 32) << 16) + h * TN + col_off;
     const int m_pad = static_cast<int>(round_up(a.M, kMetaRowPad));  // GELU: metadata rows written
     int tcount = 0, ybox = 0, nsplit = 0;
+    // F1: the selection of one unit's stages (two threads per row, 64 channels each; both in one warp), then s
+    // of the rows for the epilogue.  cg counts the stages in the producer's order.
+    int cg = 0;
+    const uint32_t conv_full_leader0 = mapa_shared(&conv_full[0], 0);
+    auto convert_unit = [&](int mp) -> bool {
+      const int hf = lane >> 4;
+      const int rr = 16 * (warp - 2) + (lane & 15);  // row of this CTA's row block
+      const int grow = mp * 2 * C::ROWS + static_cast<int>(rank) * C::ROWS + rr;
+      const int tl0 = (rr / 16) * 16 + (rr % 8), hh = (rr % 16) / 8;  // metadata lane base and 16-bit half
+      float sx = 0.f, sk = 0.f;  // x^2 and kept x^2 of this thread's channels, over the whole K
+      for (int it = 0; it <= nk; ++it, ++cg) {
+        const int cst = cg % C::NST;
+        bool okc = mbar_wait(&xfull[cst], (cg / C::NST) & 1, a.ctl, SITE_EPILOGUE);
+        okc = __all_sync(0xFFFFFFFFu, okc) && !*abort_flag;
+        if (!okc) return false;
+        uint8_t* stage = smem + cst * C::STAGE;
+        uint8_t* arow = stage + rr * 128;  // row rr of box 0: the compressed values, or T'
+        if (it < nk) {
+          const uint8_t* xr = stage + hf * C::A_BOX + rr * 128;  // channels 64 hf .. 64 hf + 63 of the step
+          uint4 v[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) v[j] = *reinterpret_cast<const uint4*>(xr + ((j ^ (rr & 7)) << 4));
+          uint32_t kept[16], w0 = 0, w1 = 0;  // metadata words of 32-channel chunks 2 hf and 2 hf + 1
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t n0g = select_group(v[j].x, v[j].y, sel_table, kept[2 * j], sx, sk);
+            const uint32_t n1g = select_group(v[j].z, v[j].w, sel_table, kept[2 * j + 1], sx, sk);
+            if (j < 4) w0 |= (n0g | (n1g << 4)) << (8 * j);
+            else w1 |= (n0g | (n1g << 4)) << (8 * (j - 4));
+          }
+          __syncwarp();  // both threads of every row have read box 0
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4*>(arow + (((4 * hf + j) ^ (rr & 7)) << 4)) =
+                make_uint4(kept[4 * j], kept[4 * j + 1], kept[4 * j + 2], kept[4 * j + 3]);
+          uint8_t* mchunk = stage + C::A_SLOT + C::B_SLOT;  // the stage's metadata chunk, tensor-memory order
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+            for (int qh = 0; qh < 2; ++qh)
+              *reinterpret_cast<uint16_t*>(mchunk + (tl0 + 8 * qh) * 16 + (2 * hf + cc) * 4 + hh * 2) =
+                  static_cast<uint16_t>((cc ? w1 : w0) >> (16 * qh));
+        } else {
+          // the LoRA stage: s of the row from both threads' sums, then T' = bf16(T * (1 / s)) over box 0
+          const float tx = sx + __shfl_xor_sync(0xFFFFFFFFu, sx, 16);
+          const float tk = sk + __shfl_xor_sync(0xFFFFFFFFu, sk, 16);
+          const float sv = tk > 0.f ? sqrtf(tx / tk) : 1.f;
+          const float inv = 1.f / sv;
+          const uint4* tsrc = reinterpret_cast<const uint4*>(a.lora_t + static_cast<int64_t>(grow < a.M ? grow : 0) *
+                                                                            kRankLB + 32 * hf);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint4 t4 = grow < a.M ? tsrc[j] : make_uint4(0u, 0u, 0u, 0u);
+            uint32_t w[4] = {t4.x, t4.y, t4.z, t4.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(w[u] << 16) * inv,
+                                                        __uint_as_float(w[u] & 0xFFFF0000u) * inv);
+              w[u] = *reinterpret_cast<uint32_t*>(&b2);
+            }
+            *reinterpret_cast<uint4*>(arow + (((4 * hf + j) ^ (rr & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          if (hf == 0) s_sh[rr] = sv;
+        }
+        fence_proxy_async();  // the generic-proxy writes above, before the tensor core reads them
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(conv_full_leader0 + 8 * cst);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_bar);  // this warp's rows' s are in s_sh
+      bool oks = mbar_wait(s_bar, tcount & 1, a.ctl, SITE_EPILOGUE);
+      return __all_sync(0xFFFFFFFFu, oks) && !*abort_flag;
+    };
     for (int unit = cluster; unit < nunits; unit += nclusters, ++tcount) {
       const int tile = unit % ntiles, ks = unit / ntiles;
       const int mp = tile % num_mp, nb = tile / num_mp;
       const int row0 = mp * 2 * C::ROWS + static_cast<int>(rank) * C::ROWS + h * BLOCK + q * 32;
       const int row = row0 + lane;
       const int n0 = nb * TN + col_off;
-      const float sc = (scaled && row < a.M) ? a.rowscale[row] : 1.f;  // issued before the wait
+      if constexpr (F1)
+        if (!convert_unit(mp)) break;
+      const float sc = F1 ? s_sh[h * BLOCK + q * 32 + lane]
+                          : ((scaled && row < a.M) ? a.rowscale[row] : 1.f);  // issued before the wait
       const int ab = tcount % C::ACC_BUFS;
       bool ok = mbar_wait(&acc_full[ab], (tcount / C::ACC_BUFS) & 1, a.ctl, SITE_EPILOGUE);
       ok = __all_sync(0xFFFFFFFFu, ok) && !*abort_flag;
@@ -673,6 +786,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       if (!mbar_wait(&full[g % C::NST], (g / C::NST) & 1, a.ctl, SITE_DRAIN)) break;
     }
   }
+  if (F1 && *abort_flag && warp == 0 && lane == 0) {
+    // this CTA's X loads of the last stages issued land before it leaves
+    const int issued = *issued_sh;
+    for (int g = issued > C::NST ? issued - C::NST : 0; g < issued; ++g)
+      if (!mbar_wait(&xfull[g % C::NST], (g / C::NST) & 1, a.ctl, SITE_DRAIN)) break;
+  }
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // no CTA leaves while its peer may still read its shared memory or TMEM
@@ -682,11 +801,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   }
 }
 
-template <bool SPARSE, bool LORA, int MB, int TN, bool TRANS = false, bool SPLIT = false, bool GELU = false>
+template <bool SPARSE, bool LORA, int MB, int TN, bool TRANS = false, bool SPLIT = false, bool GELU = false,
+          bool F1 = false>
 cudaError_t launch(const PairArgs& a, cudaStream_t st) {
-  using C = PairCfg<SPARSE, MB, TN>;
-  auto* k = gemm_pair_kernel<SPARSE, LORA, MB, TN, TRANS, SPLIT, GELU>;
-  constexpr int smem = C::SMEM + (GELU ? 256 : 0);  // + the selection table
+  using C = PairCfg<SPARSE, MB, TN, F1>;
+  auto* k = gemm_pair_kernel<SPARSE, LORA, MB, TN, TRANS, SPLIT, GELU, F1>;
+  constexpr int smem = C::SMEM + ((GELU || F1) ? 256 : 0) + (F1 ? 512 : 0);  // + the selection table, s
   static_assert(smem <= SMEM_LIMIT, "shared memory budget");
   static std::atomic<bool> attr_set[64] = {};  // per device; setting it twice from racing threads is harmless
   int dev = 0;
@@ -784,6 +904,11 @@ cudaError_t launch_gemm_pair(bool sparse, bool lora, PairShape shape, const Pair
   if (a.splits > 1)
     return lora ? launch<true, true, 1, 256, false, true>(a, st) : launch<true, false, 1, 256, false, true>(a, st);
   return lora ? launch<true, true, 1, 256>(a, st) : launch<true, false, 1, 256>(a, st);
+}
+
+cudaError_t launch_gemm_pair_f1(const PairArgs& a, cudaStream_t st) {
+  if (!a.lora_t || a.splits != 1) return cudaErrorInvalidValue;
+  return launch<true, true, 1, 256, false, false, false, true>(a, st);
 }
 
 cudaError_t launch_gemm_pair_transposed(bool lora, PairShape shape, const PairArgs& a, cudaStream_t st) {

@@ -115,6 +115,7 @@ struct PairArgs {
   int hnorm_slots;         // slots per row
   unsigned int* zero;      // words set to 0 once the previous kernel is done (the next kernel's counters), or NULL
   int nzero;
+  const uint16_t* lora_t;  // in-GEMM selection: T = X LB^T (M x 64 bf16, not divided by s)
   DevCtl ctl;
 };
 
@@ -124,6 +125,9 @@ cudaError_t launch_gemm_pair(bool sparse, bool lora, PairShape shape, const Pair
                              bool gelu = false);
 // Norm-partial slots per row of the GELU epilogue for an output of N columns with this tile shape.
 int gelu_norm_slots(bool sparse, PairShape shape, int N);
+// The sparse pair GEMM that selects the 2:4 pattern itself (256 x 256 tiles): a.tmA maps the dense X (box 64 x
+// 128, 128-byte swizzle), a.lora_t holds T = X LB^T; s comes from the GEMM's own row sums (a.rowscale unused).
+cudaError_t launch_gemm_pair_f1(const PairArgs& a, cudaStream_t st);
 // The sparse pair GEMM whose accumulator tile is the transpose of Y: a.M and a.N count the accumulator's rows
 // and columns (Y's columns and rows), tmY and ldy describe Y itself (rows of ldy elements).
 cudaError_t launch_gemm_pair_transposed(bool lora, PairShape shape, const PairArgs& a, cudaStream_t st);

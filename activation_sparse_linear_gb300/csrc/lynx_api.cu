@@ -629,6 +629,35 @@ int lynx_linear_dense(const void* X, const void* W, const void* LA, const void* 
   return dense_impl(X, W, LA, LB, Y, M, N, K, R, workspace, static_cast<cudaStream_t>(stream), false, nullptr, prof);
 }
 
+int lynx_linear_fused(const void* X, const void* W, const void* LA, const void* LB, void* Y, int64_t M, int64_t N,
+                      int64_t K, int64_t R, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!LA || !LB || !workspace) return LYNX_ERR_NULL;
+  if (int e = dense_arg_status(X, W, LA, LB, Y, M, N, K, R, workspace, workspace_bytes)) return e;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  StageEvents prof(3);
+  PairArgs g;
+  std::memset(&g, 0, sizeof(g));
+  if (!make_map(&g.tmA, X, K, M, K, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&g.tmB, W, K, N, K, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&g.tmLA, LA, R, N, R, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+    return LYNX_ERR_CUDA;
+  if (!set_y_map(&g, Y, M, N)) return LYNX_ERR_CUDA;
+  g.scale_mode = SCALE_NONE;  // s comes from the GEMM's own row sums
+  g.Y = Y;
+  g.ldy = N;
+  g.M = static_cast<int>(M);
+  g.N = static_cast<int>(N);
+  g.K = static_cast<int>(K);
+  g.splits = 1;
+  g.lora_t = static_cast<const uint16_t*>(workspace);
+  g.ctl = make_ctl();
+  if (cudaError_t e = prof.mark(0, st)) return cuda_status(e);
+  if (int e = run_lora_down(X, LB, nullptr, workspace, M, K, st)) return e;  // T = X LB^T, not divided by s
+  if (cudaError_t e = prof.mark(1, st)) return cuda_status(e);
+  if (cudaError_t e = launch_gemm_pair_f1(g, st)) return cuda_status(e);
+  return cuda_status(prof.mark(2, st));
+}
+
 int lynx_linear_wsparse(const void* X, const void* Wvals, const void* Wmeta, const void* LA, const void* LB, void* Y,
                         int64_t M, int64_t N, int64_t K, int64_t R, void* workspace, size_t workspace_bytes,
                         void* stream) {

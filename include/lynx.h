@@ -130,6 +130,19 @@ LYNX_API int lynx_sparsify_lora(const void* X, const void* LB, int64_t M, int64_
 LYNX_API int lynx_linear(const void* X, const void* W, const void* LA, const void* LB, void* Y, int64_t M, int64_t N,
                 int64_t K, int64_t R, void* workspace, size_t workspace_bytes, void* stream);
 
+/* The same Y = S(X) W^T + X (LA LB)^T with the 2:4 selection inside the GEMM (the page's own design, "RT-Lynx"
+ * page, CUDA kernel optimisation: 2:4 activations built directly in registers): no compressed copy of X goes
+ * through global memory.  Enqueues the LoRA down-projection T = X LB^T (into workspace) and one GEMM on
+ * 256 x 256 tiles whose epilogue warps, while a tile's k-steps stream in, select the top two of every four
+ * channels of the dense X tile, write the compressed values and metadata into shared memory for the sparse
+ * MMAs, and sum x^2 and kept x^2 over the row; at the tile's last step they form s and T' = bf16(T / s).
+ *   Arguments as for lynx_linear (LA, LB, workspace required; R = 64); workspace: >= lynx_dense_workspace_bytes(M,
+ *   R) bytes (T).  Results agree with lynx_linear within the stated tolerance: s is summed in another order and
+ *   T is rounded to bf16 before the division by s.  Every column tile repeats its rows' selection, so this
+ *   path trades the sparsify pass's global-memory round trip for N / 256 selections per row. */
+LYNX_API int lynx_linear_fused(const void* X, const void* W, const void* LA, const void* LB, void* Y, int64_t M,
+                               int64_t N, int64_t K, int64_t R, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Size of the fixed scratch array behind lynx_linear_noalloc, per GPU. */
 #define LYNX_NOALLOC_SCRATCH_BYTES (64u << 20)
 
