@@ -18,11 +18,12 @@
 // read from HBM once for both branches.
 //
 // The channel blocks of a row block are split over a cluster of `split` CTAs
-// so that the grid covers the GPU; each CTA keeps its fp32 shares (x^2,
-// kept x^2, and its 128 x 64 share of X LB^T) in shared memory, and CTA j of
-// the cluster adds the split shares of its rows in rank order, reading them
-// through distributed shared memory, and writes s and T'.  With split = 1 the
-// CTA writes s and T' itself.
+// so that the grid covers the GPU.  Each row has an owner CTA in the cluster;
+// every CTA stores its fp32 shares of a row (x^2, kept x^2, and its share of
+// X LB^T) straight into the owner's shared memory (distributed shared memory,
+// one slot per sending CTA), and after one cluster barrier the owner adds the
+// slots of its rows in rank order and writes s and T'.  With split = 1 the CTA
+// writes s and T' itself.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -35,7 +36,7 @@ namespace lynx {
 namespace {
 
 constexpr int P_ROWS = 128;                       // rows per CTA = TMEM lanes
-constexpr int P_NST = 8;                          // pipeline stages
+constexpr int P_NST = 7;                          // pipeline stages
 constexpr int P_WORKERS = 16;                     // selection warps: four threads per row
 constexpr int P_TPR = 32 * P_WORKERS / 128;       // threads per row (16 of each stage's 64 channels each)
 constexpr int P_THREADS = 64 + 32 * P_WORKERS;    // warp 0 TMA, warp 1 MMA, warps 2..17 selection
@@ -44,9 +45,13 @@ constexpr int P_XT = P_ROWS * 128;                // X tile: 128 rows x 64 chann
 constexpr int P_LBT = kRankLB * 128;              // LB tile: 64 ranks x 64 channels (8 KiB)
 constexpr int P_STAGE = P_XT + P_LBT;
 constexpr int P_SMALL = 2048;                     // barriers, s of the rows, norm shares of the rows
-constexpr int P_SMEM = P_NST * P_STAGE + P_SMALL + 1024;  // + alignment
-constexpr int P_TSTRIDE = 68;                     // floats per row of the T' share (272 B: conflict-free rows)
-static_assert(P_ROWS * P_TSTRIDE * 4 <= P_NST * P_STAGE, "the T' share fits in the drained stage ring");
+constexpr int P_TSTRIDE = 68;                     // floats per row of a T' share (272 B: conflict-free rows)
+// Receive slots of the cluster reduction: split x ceil(128 / split) rows (at most 143 for split <= 16), each an
+// X LB^T share row and a (x^2, kept x^2) pair.
+constexpr int P_RECV_ROWS = 144;
+constexpr int P_RECV = P_RECV_ROWS * (P_TSTRIDE * 4 + 8);
+constexpr int P_SMEM = P_NST * P_STAGE + P_SMALL + P_RECV + 1024;  // + alignment
+static_assert(P_RECV_ROWS >= P_ROWS + kMaxPrologueSplit - 1, "receive slots for every cluster size");
 static_assert(P_SMEM <= 232448, "shared memory budget");
 
 __constant__ SelectTable c_select_table = make_select_table();
@@ -66,9 +71,9 @@ __global__ void __launch_bounds__(P_THREADS, 1) prologue_kernel(const __grid_con
   uint64_t* acc_full = empty + P_NST;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(acc_full + 1);
   float* s_sh = reinterpret_cast<float*>(tslot + 4);  // direct mode: s of the CTA's rows (128 floats)
-  float2* npart = reinterpret_cast<float2*>(s_sh + P_ROWS);  // cluster mode: (sum x^2, sum kept x^2) per row
-  uint32_t* sel_table = reinterpret_cast<uint32_t*>(npart + P_ROWS);  // the top-2-of-4 decision table
-  float* tpart = reinterpret_cast<float*>(smem);            // cluster mode: T' share [128][P_TSTRIDE]
+  uint32_t* sel_table = reinterpret_cast<uint32_t*>(s_sh + 3 * P_ROWS);  // the top-2-of-4 decision table
+  float* recv_t = reinterpret_cast<float*>(smem + P_NST * P_STAGE + P_SMALL);  // cluster mode: T shares received
+  float2* recv_n = reinterpret_cast<float2*>(recv_t + P_RECV_ROWS * P_TSTRIDE);  // ... and norm shares
   static_assert(8 * (2 * P_NST + 1) + 16 + 12 * P_ROWS + 64 * 4 <= P_SMALL, "small-state area");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -99,6 +104,15 @@ __global__ void __launch_bounds__(P_THREADS, 1) prologue_kernel(const __grid_con
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = LORA ? *tslot : 0u;
+  // Cluster mode: each row has an owner CTA, rows [ceil(128 j / split), ceil(128 (j + 1) / split)) for rank j; a
+  // share sent by rank p lands in the owner's slot p * rmax + (row - first row of the owner).  The barrier phase
+  // opened here tells every thread, before its first store into a peer, that all CTAs of the cluster have started.
+  const int rmax = (P_ROWS + a.split - 1) / a.split;
+  auto owner_slot = [&](int r, int& o) {
+    o = r * a.split / P_ROWS;
+    return sp * rmax + r - (P_ROWS * o + a.split - 1) / a.split;
+  };
+  if (a.split > 1) cluster_arrive_relaxed();
   // The set-up above may overlap the previous kernel; nothing below touches global memory before it is done.
   pdl_launch_dependents();
   pdl_wait();
@@ -216,18 +230,20 @@ __global__ void __launch_bounds__(P_THREADS, 1) prologue_kernel(const __grid_con
     skept += __shfl_xor_sync(0xFFFFFFFFu, skept, 1);
     sx += __shfl_xor_sync(0xFFFFFFFFu, sx, 2);
     skept += __shfl_xor_sync(0xFFFFFFFFu, skept, 2);
+    if (a.split > 1) cluster_wait();  // every CTA of the cluster has started
     if (qq == 0) {
       if (a.split == 1) {
         const float sv = skept > 0.f ? sqrtf(sx / skept) : 1.f;
         s_sh[r] = sv;
         if (row < a.M) a.s[row] = sv;
-      } else {
-        npart[r] = make_float2(sx, skept);
+      } else {  // this CTA's norm shares of row r, into the owner's slot
+        int o;
+        const int slot = owner_slot(r, o);
+        st_cluster_f32x2(mapa_shared(&recv_n[slot], o), make_float2(sx, skept));
       }
     }
     if (LORA) {
-      // s_sh complete; every worker is past the stage ring, which then holds the T' share (the MMAs are done
-      // with it once acc_full has fired)
+      // s_sh complete (direct mode)
       named_sync_workers();
       if (warp < 6) {
         // TMEM lane quarter q = warp % 4 holds rows 32 q .. 32 q + 31
@@ -258,42 +274,40 @@ __global__ void __launch_bounds__(P_THREADS, 1) prologue_kernel(const __grid_con
                 dst[v8] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
               }
             }
-          } else {
-            float4* dst = reinterpret_cast<float4*>(tpart + trow * P_TSTRIDE);  // 272-byte rows: no bank conflicts
+          } else {  // this CTA's share of row trow of X LB^T, into the owner's slot (272-byte rows)
+            int o;
+            const int slot = owner_slot(trow, o);
+            const uint32_t dst = mapa_shared(recv_t + slot * P_TSTRIDE, o);
 #pragma unroll
             for (int v4 = 0; v4 < 16; ++v4) {
               const uint32_t* src = v4 < 8 ? t0 + 4 * v4 : t1 + 4 * (v4 - 8);
-              dst[v4] = make_float4(__uint_as_float(src[0]), __uint_as_float(src[1]), __uint_as_float(src[2]),
-                                    __uint_as_float(src[3]));
+              st_cluster_f32x4(dst + 16 * v4, make_float4(__uint_as_float(src[0]), __uint_as_float(src[1]),
+                                                          __uint_as_float(src[2]), __uint_as_float(src[3])));
             }
           }
         }
       }
     }
   }
+  if (a.split > 1 && warp < 2) cluster_wait();  // the producer and MMA warps' half of the start-up phase
   tc_fence_before();
   __syncthreads();
   if (a.split > 1) {
     // ---------------------------------------------------------------- cluster reduction of the shares
-    // CTA j of the cluster finishes rows [j * 128 / split, (j + 1) * 128 / split): it adds the split CTAs' shares in rank order
-    // (deterministic), reading them from the peers' shared memory, and writes s and T'.
-    cluster_sync();  // every CTA's shares are in its shared memory
-    const int row_lo = sp * P_ROWS / a.split, rows = (sp + 1) * P_ROWS / a.split - row_lo;
-    // Each thread first issues all its peer loads (up to kMaxPrologueSplit), then adds them in rank order, so
-    // the distributed-shared-memory round trips overlap instead of following one another.
+    // The owner of rows [row_lo, row_hi) adds the slots of the split CTAs in rank order (deterministic) and
+    // writes s and T'.  Only local shared memory is read: after the barrier no CTA touches a peer, so no CTA
+    // has to wait for the others before it leaves.
+    cluster_sync();  // every share is in its owner's shared memory
+    const int row_lo = (P_ROWS * sp + a.split - 1) / a.split;
+    const int rows = (P_ROWS * (sp + 1) + a.split - 1) / a.split - row_lo;
     if (threadIdx.x < rows) {  // s of the row
       const int rr = row_lo + threadIdx.x, grow = r0 + rr;
-      float2 n2[kMaxPrologueSplit];
-#pragma unroll
-      for (int p = 0; p < kMaxPrologueSplit; ++p)
-        if (p < a.split) n2[p] = ld_cluster_f32x2(mapa_shared(&npart[rr], p));
       float sxs = 0.f, sks = 0.f;
-#pragma unroll
-      for (int p = 0; p < kMaxPrologueSplit; ++p)
-        if (p < a.split) {
-          sxs += n2[p].x;
-          sks += n2[p].y;
-        }
+      for (int p = 0; p < a.split; ++p) {
+        const float2 n2 = recv_n[p * rmax + threadIdx.x];
+        sxs += n2.x;
+        sks += n2.y;
+      }
       const float sv = sks > 0.f ? sqrtf(sxs / sks) : 1.f;
       s_sh[rr] = sv;
       if (grow < a.M) a.s[grow] = sv;
@@ -302,21 +316,15 @@ __global__ void __launch_bounds__(P_THREADS, 1) prologue_kernel(const __grid_con
       __syncthreads();  // s of the CTA's rows in s_sh
       // T' in items of 4 ranks: 16 per row
       for (int i = threadIdx.x; i < rows * 16; i += P_THREADS) {
-        const int rr = row_lo + i / 16, g = i % 16, grow = r0 + rr;
-        float4 t4[kMaxPrologueSplit];
-        const uint32_t t = smem_u32(tpart + rr * P_TSTRIDE + 4 * g);
-#pragma unroll
-        for (int p = 0; p < kMaxPrologueSplit; ++p)
-          if (p < a.split) t4[p] = ld_cluster_f32x4(mapa_shared_u32(t, p));
+        const int rl = i / 16, g = i % 16, rr = row_lo + rl, grow = r0 + rr;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int p = 0; p < kMaxPrologueSplit; ++p)
-          if (p < a.split) {
-            acc.x += t4[p].x;
-            acc.y += t4[p].y;
-            acc.z += t4[p].z;
-            acc.w += t4[p].w;
-          }
+        for (int p = 0; p < a.split; ++p) {
+          const float4 t4 = *reinterpret_cast<const float4*>(recv_t + (p * rmax + rl) * P_TSTRIDE + 4 * g);
+          acc.x += t4.x;
+          acc.y += t4.y;
+          acc.z += t4.z;
+          acc.w += t4.w;
+        }
         if (grow < a.M) {
           const float inv = 1.f / s_sh[rr];  // T' = T * (1 / s): one division per row
           __nv_bfloat162 b0 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
@@ -326,7 +334,6 @@ __global__ void __launch_bounds__(P_THREADS, 1) prologue_kernel(const __grid_con
         }
       }
     }
-    cluster_sync();  // no CTA leaves while a peer may still read its shared memory
   }
   if (LORA && warp == 1) {
     tc_fence_after();

@@ -425,6 +425,29 @@ def main() -> int:
     assert st == 0, asl.lynx_status_string(st)
     del wpruned, ws_w
 
+    # The in-GEMM selection variant (lynx_linear_fused) at the same shape: the LoRA down-projection, then one GEMM
+    # whose epilogue warps select the 2:4 pattern of every dense X tile themselves (no sparsify pass).
+    ws_f = torch.empty(asl.lynx_dense_workspace_bytes(M, R), dtype=torch.uint8, device=dev)
+
+    def fused(i):
+        s = sets[i % ROTATE]
+        return L.lynx_linear_fused(s["X"].data_ptr(), s["W"].data_ptr(), s["LA"].data_ptr(), s["LB"].data_ptr(),
+                                   s["Y"].data_ptr(), M, N, K, R, ws_f.data_ptr(), ws_f.numel(), sp)
+    for i in range(args.warmup):
+        fused(i)
+    torch.cuda.synchronize()
+    nf = max(4, nd // 4)
+    l0.record(stream)
+    for i in range(nf):
+        if fused(i) != 0:
+            raise RuntimeError("lynx_linear_fused failed")
+    l1.record(stream)
+    torch.cuda.synchronize()
+    fused_ms = l0.elapsed_time(l1) / nf
+    st = asl.lynx_sync_status()
+    assert st == 0, asl.lynx_status_string(st)
+    del ws_f
+
     # The other layer shapes of the DiT workloads (MLP up/down, the CFG batch, the largest stack M): step time
     # of lynx_linear and of the dense cuBLAS GEMM at the same shape, two rotating device copies each.  Inputs
     # are seeded normal draws generated on the device (timing only; the parity tests cover these shapes).
@@ -710,6 +733,11 @@ def main() -> int:
             "weight_2to4_comparator": {"ms": wsparse_ms, "tflops": flops / (wsparse_ms * 1e-3) / 1e12,
                                        "x_vs_dense_cublas": dense_ms / wsparse_ms,
                                        "note": "Y = X W~^T + X (LA LB)^T, W~ = 2:4-pruned W as the sparse operand"},
+            "in_gemm_selection": {"ms": fused_ms, "tflops": flops / (fused_ms * 1e-3) / 1e12,
+                                  "x_vs_two_pass": ms_per_step / fused_ms,
+                                  "note": "lynx_linear_fused: LoRA down-projection + one GEMM that selects the 2:4 "
+                                          "pattern of each dense X tile in its epilogue warps (256 x 256 tiles); "
+                                          "every column tile repeats its rows' selection"},
             "other_shapes": shapes,
             "sparsify_alone": sparsify_alone,
             "block_stack_32_linears": stack,
