@@ -268,6 +268,9 @@ def main() -> int:
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="lynx", choices=["lynx", "reference"])
+    ap.add_argument("--profile-case", default=None, choices=["linear", "fused", "dense"],
+                    help="run only W + K calls of lynx_linear / lynx_linear_fused / lynx_linear_dense (no LoRA) on "
+                         "the workload and print their mean time: a short command for profilers")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -308,6 +311,34 @@ def main() -> int:
     def call(s):
         return L.lynx_linear(s["X"].data_ptr(), s["W"].data_ptr(), s["LA"].data_ptr(), s["LB"].data_ptr(),
                              s["Y"].data_ptr(), M, N, K, R, s["ws"].data_ptr(), s["ws"].numel(), sp)
+
+    if args.profile_case:
+        ws_d = torch.empty(asl.lynx_dense_workspace_bytes(M, R), dtype=torch.uint8, device=dev)
+
+        def case(s):
+            if args.profile_case == "linear":
+                return call(s)
+            if args.profile_case == "fused":
+                return L.lynx_linear_fused(s["X"].data_ptr(), s["W"].data_ptr(), s["LA"].data_ptr(),
+                                           s["LB"].data_ptr(), s["Y"].data_ptr(), M, N, K, R, ws_d.data_ptr(),
+                                           ws_d.numel(), sp)
+            return L.lynx_linear_dense(s["X"].data_ptr(), s["W"].data_ptr(), None, None, s["Y"].data_ptr(), M, N,
+                                       K, R, None, 0, sp)
+        for i in range(args.warmup):
+            assert case(sets[i % ROTATE]) == 0
+        torch.cuda.synchronize()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for i in range(args.steps):
+            assert case(sets[i % ROTATE]) == 0
+        c1.record(stream)
+        torch.cuda.synchronize()
+        st = asl.lynx_sync_status()
+        assert st == 0, asl.lynx_status_string(st)
+        if rank == 0:
+            print(json.dumps({"profile_case": args.profile_case, "calls": args.steps,
+                              "ms_per_call": c0.elapsed_time(c1) / args.steps}), flush=True)
+        return 0
 
     # warm-up
     for i in range(args.warmup):
