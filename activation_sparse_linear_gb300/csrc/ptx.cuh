@@ -57,32 +57,6 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint64_t* bar, uint32_t parity
       : "memory");
   return ok;
 }
-// Non-blocking probe of the phase with the given parity (never suspends the thread).
-__device__ __forceinline__ uint32_t mbar_test_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.b32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok;
-}
-// Bounded spin on mbar_test_wait: for barriers completed by arrivals from the peer CTA, where a suspended
-// try_wait was seen to resume up to about a microsecond after the phase completed.
-__device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity, const DevCtl& c, int site) {
-  const uint64_t t0 = globaltimer_ns();
-  while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 64; ++i)
-      if (mbar_test_wait(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > c.wait_ns) {
-      record_error(c, site);
-      return false;
-    }
-  }
-}
 // Bounded wait for the phase with the given parity.  Returns false (and records
 // `site` in the error word) once c.wait_ns has passed.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const DevCtl& c, int site) {
