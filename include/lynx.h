@@ -147,7 +147,7 @@ LYNX_API int lynx_linear_fused(const void* X, const void* W, const void* LA, con
 #define LYNX_NOALLOC_SCRATCH_BYTES (64u << 20)
 
 /* lynx_linear for callers that must not allocate device memory.  (No
- * counterpart in the RT-Lynx paper: this is a deployment convenience.)
+ * counterpart on the RT-Lynx page: this is a deployment convenience.)
  *
  * Some callers cannot call cudaMalloc or any allocator on the path that runs
  * the layer: a request loop in a serving process that must never stall on
@@ -192,7 +192,7 @@ LYNX_API int lynx_linear_dense(const void* X, const void* W, const void* LA, con
  * Selective Layer Skipping) is a fixed sequence of sparse and dense linears.
  * These calls run such a sequence in order on one stream, or capture it once
  * into a CUDA graph that replays every kernel of it with one host call.
- * (The graph is a deployment convenience, not part of the paper.) */
+ * (The graph is a deployment convenience, not part of the page's method.) */
 
 /* One layer.  flags & LYNX_LAYER_SPARSE: Y = lynx_linear(X, W, LA, LB) (LA
  * and LB required, R = 64); otherwise Y = lynx_linear_dense(X, W, LA, LB) (LA
