@@ -86,18 +86,27 @@ enum Site : int { SITE_PRODUCER = 11, SITE_MMA = 12, SITE_EPILOGUE = 13, SITE_DR
 // F1 (sparse, one row block): the stage carries the dense X tile (two 64-channel boxes per row block) instead of
 // compressed values; the epilogue warps select in registers and write the compressed values over box 0 and the
 // metadata chunk into the stage before the MMAs read them.
+// WIDE (dense, one row block, TN = 448): a tile is two 224-column halves, one MMA each per K = 16 step, and the
+// two MMAs share one shared-memory read of the X tile through the tensor core's A collector (fill, then last
+// use): per 64 channels an SM moves 88 KB through shared memory for 3.7 M MACs (24 bytes per thousand MACs)
+// instead of 64 KB for 2.1 M (31); a LoRA stage per half.
 template <bool SPARSE, int MB, int TN, bool F1 = false>
 struct PairCfg {
   static constexpr int ROWS = MB * BLOCK;    // rows per CTA
   static constexpr int HALF_N = TN / 2;      // W rows staged per CTA
+  static constexpr bool WIDE = TN > 256;
+  static constexpr int NH = WIDE ? 2 : 1;    // MMA column halves per tile
+  static constexpr int MN = TN / NH;         // MMA N
+  static constexpr int QN = MN / 2;          // W rows per CTA and MMA half
   static constexpr int BK = SPARSE ? 128 : kDenseBK;
   static constexpr int BOXES = SPARSE ? (F1 ? 2 : 1) : kDenseBK / 64;  // 64-channel (128-byte) A boxes per row block and stage
   static constexpr int A_BOX = BLOCK * 128;
   static constexpr int A_BLOCK = BOXES * A_BOX;
   static constexpr int A_SLOT = MB * A_BLOCK;
-  static constexpr int SUB = HALF_N * 128;   // one 64-channel W sub-tile of this CTA
+  static constexpr int SUB = HALF_N * 128;   // one 64-channel W sub-tile of this CTA (WIDE: both halves' rows)
   static constexpr int B_SLOT = SPARSE ? 2 * SUB : BOXES * SUB;
   static constexpr int M_SLOT = SPARSE ? MB * kMetaChunkBytes : 0;
+  static constexpr int LORA_LOAD = MB * A_BOX + (WIDE ? QN * 128 : SUB);  // T' and this CTA's LA rows (WIDE: one half's)
   static constexpr int STAGE = A_SLOT + B_SLOT + M_SLOT;
   static constexpr int LOAD_BYTES = F1 ? A_SLOT + B_SLOT : STAGE;  // TMA bytes of a k-step per CTA
   // Output staging boxes per epilogue warp: two, so that a box is refilled while the other is stored; one
@@ -116,7 +125,8 @@ struct PairCfg {
   static constexpr int META_COL = ACC_BUFS * ACC_STRIDE;  // first metadata column (after the accumulators)
   static_assert(STAGE % 1024 == 0, "stage slots keep 1 KiB alignment");
   static_assert(NST >= 2 && SMEM <= SMEM_LIMIT, "shared memory budget");
-  static_assert(TN % 32 == 0 && TN <= 256 && HALF_N % 8 == 0, "MMA N");
+  static_assert(TN % 32 == 0 && MN <= 256 && QN % 8 == 0 && (!WIDE || (!SPARSE && MB == 1 && BOXES == 1)), "MMA N");
+  static_assert(LORA_LOAD <= STAGE, "a LoRA stage fits a stage slot");
   static_assert(META_COL + META_COLS <= TMEM_COLS, "TMEM budget");
   static_assert(ACC_BUFS * ACC_STRIDE <= TMEM_COLS, "TMEM budget of the accumulator buffers");
   static_assert(8 * (2 * NST + 2 * ACC_BUFS + 3 + (F1 ? 2 * NST + 1 : 0)) + 32 <= 256, "barrier area");
@@ -171,6 +181,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ PairArgs a) {
   using C = PairCfg<SPARSE, MB, TN, F1>;
   static_assert(!F1 || (LORA && !TRANS && !SPLIT && !GELU), "in-GEMM selection variant");
+  static_assert(!C::WIDE || (!TRANS && !SPLIT), "the 448-column tile: whole tiles, not transposed");
   // With two row blocks, two threads issue the MMAs (one row block each): while one waits on a barrier or
   // does its per-stage bookkeeping, the other's queued MMAs keep the tensor pipe busy.
   constexpr int NISS = MB >= 2 ? 2 : 1;
@@ -275,7 +286,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       for (int unit = cluster; unit < nunits && !stop; unit += nclusters) {
         const int tile = unit % ntiles, ks = unit / ntiles;
         const int kbeg = ks * nk / S, kend = (ks + 1) * nk / S;
-        const int nst_u = kend - kbeg + ((LORA && ks == S - 1) ? 1 : 0);
+        const int nst_u = kend - kbeg + ((LORA && ks == S - 1) ? C::NH : 0);
         const int mp = tile % num_mp, nb = tile / num_mp;
         const int m0 = mp * 2 * C::ROWS + static_cast<int>(rank) * C::ROWS;
         const int n0 = nb * TN + static_cast<int>(rank) * C::HALF_N;
@@ -297,7 +308,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           uint8_t* sB = sA + C::A_SLOT;
           const uint32_t fb = full_leader0 + 8 * st;
           if (!(a.ctl.inject == 1 && g == 0)) {  // test hook: the first stage never arrives
-            if (kk < kend) {
+            if constexpr (C::WIDE) {
+              // the CTA's X rows and its rows of both column halves of W; a LoRA stage per half: T' and the
+              // CTA's rows of that half of LA
+              const int nw0 = nb * TN + static_cast<int>(rank) * C::QN;
+              if (kk < kend) {
+                if (leader) mbar_arrive_expect_tx(&full[st], 2 * (C::A_SLOT + C::B_SLOT));
+                tma_load_2d_pair(sA, &a.tmA, fb, kk * C::BK, m0);
+                tma_load_2d_pair(sB, &a.tmB, fb, kk * C::BK, nw0);
+                tma_load_2d_pair(sB + C::QN * 128, &a.tmB, fb, kk * C::BK, nw0 + C::MN);
+              } else {
+                if (leader) mbar_arrive_expect_tx(&full[st], 2 * C::LORA_LOAD);
+                tma_load_2d_pair(sA, &a.tmT, fb, 0, m0);
+                tma_load_2d_pair(sA + C::A_BOX, &a.tmLA, fb, 0, nw0 + (kk - kend) * C::MN);
+              }
+            } else if (kk < kend) {
               if constexpr (F1) {  // X (dense, two boxes per row block) lands on this CTA's own barrier
                 if (leader) mbar_arrive_expect_tx(&full[st], 2 * C::B_SLOT);
                 mbar_arrive_expect_tx(&xfull[st], C::A_SLOT);
@@ -371,7 +396,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       for (int unit = cluster; unit < nunits && !stop; unit += nclusters, ++tcount) {
         const int ks = unit / ntiles;
         const int kbeg = ks * nk / S, kend = (ks + 1) * nk / S;
-        const int nst_u = kend - kbeg + ((LORA && ks == S - 1) ? 1 : 0);
+        const int nst_u = kend - kbeg + ((LORA && ks == S - 1) ? C::NH : 0);
         const int ab = tcount % C::ACC_BUFS;  // accumulator buffer of this unit
         const uint32_t acc_base = tmem + ab * C::ACC_STRIDE;
         if (!mbar_wait(&acc_empty[ab], ((tcount / C::ACC_BUFS) & 1) ^ 1, a.ctl, SITE_MMA)) {
@@ -388,7 +413,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           tc_fence_after();
           const uint64_t ad = a0 + st * STEP, bd = b0 + st * STEP;
           const uint32_t acc0 = it != 0;
-          if (kbeg + it < kend) {
+          if constexpr (C::WIDE) {
+            constexpr uint32_t IDESC_W = idesc_bf16(2 * BLOCK, C::MN, false);
+            if (kbeg + it < kend) {
+              // four K = 16 steps, each one MMA per column half: the first fills the A collector, the second
+              // uses it last
+              constexpr uint64_t BH = (C::QN * 128) >> 4;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const uint32_t accj = (it | j) != 0;
+                tc_mma_pair_fill(acc_base, ad + 2 * j, bd + 2 * j, IDESC_W, accj);
+                tc_mma_pair_lastuse(acc_base + C::MN, ad + 2 * j, bd + BH + 2 * j, IDESC_W, accj);
+              }
+            } else {  // LoRA stage of column half L: T' against that half's LA rows (after T' in the slot)
+              const uint32_t d = acc_base + (it - (kend - kbeg)) * C::MN;
+              const uint64_t lh = a0 + st * STEP + (C::A_BOX >> 4);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) tc_mma_pair(d, ad + 2 * j, lh + 2 * j, IDESC_W, 1);
+            }
+          } else if (kbeg + it < kend) {
             if constexpr (SPARSE) {
               // metadata group of this stage: the ring rotates with every k-step this issuer runs
               const uint32_t grp0 = meta0 + (mring++ & (META_RING - 1)) * (MB * META_GROUP_COLS);
@@ -844,14 +887,18 @@ cudaError_t launch(const PairArgs& a, cudaStream_t st) {
 // for the large DiT QKV and MLP-up shapes, 512 x 192 where 224-wide column tiles would add a wave (N = 3072),
 // 256 x 256 when few row tiles would leave pairs idle (e.g. M = 1024, N = 9216), 256 x 192 when narrower tiles
 // keep a short problem inside one wave (e.g. M = 1024, N = 3072: 64 tiles for 76 CTA pairs).
+// Dense shapes: the 256 x 448 tile does a tile's work in 0.965 of the time of 1.75 256 x 256 tiles (measured at
+// M = 4608-16384, K = 3072), so it wins where its waves are about as full as the 256-column tiles' (QKV N = 9216:
+// 5 waves instead of 9, 0.95x the time; N = 3072 at M = 16384: 0.87x) and loses where a wave stays partly idle
+// (N = 3072 at M = 4608: 2 waves of 126 tiles instead of 3 of 216, 1.07x; M = 1024).
 PairShape pair_shape(bool sparse, int M, int N) {
-  if (!sparse) return {1, 256};
   const int64_t clusters = sm_count() / 2 > 0 ? sm_count() / 2 : 1;
   auto cost = [&](int rb, int tn, double bytes_per_kmac) {
     const int64_t tiles = ((M + 256 * rb - 1) / (256 * rb)) * static_cast<int64_t>((N + tn - 1) / tn);
     const int64_t waves = (tiles + clusters - 1) / clusters;
     return static_cast<double>(waves) * 256.0 * rb * tn * bytes_per_kmac;
   };
+  if (!sparse) return cost(1, 448, 0.965) < cost(1, 256, 1.0) ? PairShape{1, 448} : PairShape{1, 256};
   const PairShape cand[4] = {{2, 224}, {2, 192}, {1, 256}, {1, 192}};
   const double bytes[4] = {21.3, 22.9, 23.8, 26.7};
   int best = 0;
@@ -867,7 +914,7 @@ PairShape pair_shape(bool sparse, int M, int N) {
 }
 
 bool pair_shape_valid(bool sparse, PairShape shape) {
-  if (!sparse) return shape.rb == 1 && shape.tn == 256;
+  if (!sparse) return shape.rb == 1 && (shape.tn == 256 || shape.tn == 448);
   return (shape.rb == 2 && (shape.tn == 224 || shape.tn == 192)) || (shape.rb == 1 && (shape.tn == 256 || shape.tn == 192));
 }
 
@@ -881,6 +928,9 @@ cudaError_t launch_gemm_pair(bool sparse, bool lora, PairShape shape, const Pair
                              bool gelu) {
   if (!pair_shape_valid(sparse, shape)) return cudaErrorInvalidValue;
   if (gelu) {  // the MLP up layer: sparse with LoRA, or dense
+    if (!sparse && shape.tn == 448)
+      return lora ? launch<false, true, 1, 448, false, false, true>(a, st)
+                  : launch<false, false, 1, 448, false, false, true>(a, st);
     if (!sparse)
       return lora ? launch<false, true, 1, 256, false, false, true>(a, st)
                   : launch<false, false, 1, 256, false, false, true>(a, st);
@@ -890,6 +940,7 @@ cudaError_t launch_gemm_pair(bool sparse, bool lora, PairShape shape, const Pair
     if (shape.tn == 192) return launch<true, true, 1, 192, false, false, true>(a, st);
     return launch<true, true, 1, 256, false, false, true>(a, st);
   }
+  if (!sparse && shape.tn == 448) return lora ? launch<false, true, 1, 448>(a, st) : launch<false, false, 1, 448>(a, st);
   if (!sparse) return lora ? launch<false, true, 1, 256>(a, st) : launch<false, false, 1, 256>(a, st);
   if (shape.rb == 2 && shape.tn == 224)
     return lora ? launch<true, true, 2, 224>(a, st) : launch<true, false, 2, 224>(a, st);

@@ -28,6 +28,7 @@ std::atomic<int> g_inject{0};
 std::atomic<int> g_force_tile{0};  // 0: tile shape by problem shape; else a forced shape, rb << 16 | tn
 std::atomic<int> g_force_split{0};  // 0: pre-pass cluster size by occupancy; else a forced size
 std::atomic<int> g_force_ksplit{0};  // 0: GEMM k-splits by tile count; else a forced count (one-row-block tiles)
+std::atomic<int> g_force_dense_tile{0};  // 0: dense tile columns by problem shape; else 256 or 448
 constexpr int kMaxKSplit = 4;
 thread_local void* const* t_prof_events = nullptr;
 thread_local int t_prof_count = 0;
@@ -194,6 +195,11 @@ PairShape sparse_shape(int64_t M, int64_t N) {
   return forced ? PairShape{forced >> 16, forced & 0xFFFF} : pair_shape(true, static_cast<int>(M), static_cast<int>(N));
 }
 
+PairShape dense_shape(int64_t M, int64_t N) {
+  const int forced = g_force_dense_tile.load();
+  return forced ? PairShape{1, forced} : pair_shape(false, static_cast<int>(M), static_cast<int>(N));
+}
+
 // T = X LB^T [/ s] on the 64-wide tcgen05 tile (standalone down-projection and the dense path).
 int run_lora_down(const void* X, const void* LB, const float* s, void* T, int64_t M, int64_t K, cudaStream_t st) {
   GemmArgs g;
@@ -354,12 +360,15 @@ int dense_impl(const void* X, const void* W, const void* LA, const void* LB, voi
   const bool lora = LA || LB;
   PairArgs g;
   std::memset(&g, 0, sizeof(g));
+  // W and LA rows per load: this CTA's half of a 256-column tile, or of one 224-column half of a 448-column tile
+  const PairShape shape = dense_shape(M, N);
+  const uint32_t w_rows = shape.tn > 256 ? shape.tn / 4 : shape.tn / 2;
   if (!make_map(&g.tmA, X, K, M, K, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&g.tmB, W, K, N, K, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+      !make_map(&g.tmB, W, K, N, K, 64, w_rows, CU_TENSOR_MAP_SWIZZLE_128B))
     return LYNX_ERR_CUDA;
   if (lora) {
     if (!make_map(&g.tmT, workspace, R, M, R, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&g.tmLA, LA, R, N, R, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+        !make_map(&g.tmLA, LA, R, N, R, 64, w_rows, CU_TENSOR_MAP_SWIZZLE_128B))
       return LYNX_ERR_CUDA;
   }
   if (!set_y_map(&g, Y, M, N)) return LYNX_ERR_CUDA;
@@ -377,10 +386,10 @@ int dense_impl(const void* X, const void* W, const void* LA, const void* LB, voi
   if (lora) {
     if (int e = run_lora_down(X, LB, nullptr, workspace, M, K, st)) return e;
     if (cudaError_t e = prof.mark(1, st)) return cuda_status(e);
-    if (cudaError_t e = launch_gemm_pair(false, true, PairShape{1, 256}, g, st, gelu)) return cuda_status(e);
+    if (cudaError_t e = launch_gemm_pair(false, true, shape, g, st, gelu)) return cuda_status(e);
     return cuda_status(prof.mark(2, st));
   }
-  if (cudaError_t e = launch_gemm_pair(false, false, PairShape{1, 256}, g, st, gelu)) return cuda_status(e);
+  if (cudaError_t e = launch_gemm_pair(false, false, shape, g, st, gelu)) return cuda_status(e);
   return cuda_status(prof.mark(1, st));
 }
 
@@ -420,7 +429,7 @@ bool fusable(const lynx_layer& up, const lynx_layer& dn) {
 PairPlan plan_pair(const lynx_layer& up, const lynx_layer& dn) {
   PairPlan p;
   const int64_t M = up.M;
-  p.up_shape = is_sparse(up) ? sparse_shape(M, up.N) : PairShape{1, 256};
+  p.up_shape = is_sparse(up) ? sparse_shape(M, up.N) : dense_shape(M, up.N);
   p.up_bytes = is_sparse(up) ? carve(nullptr, M, up.K, up.R).bytes
                              : ((up.LA || up.LB) ? lynx_dense_workspace_bytes(M, up.R) : 0);
   p.slots = gelu_norm_slots(is_sparse(up), p.up_shape, static_cast<int>(up.N));
@@ -797,6 +806,12 @@ int lynx_debug_force_ksplit(int splits) {
 int lynx_debug_linear_ksplit(int64_t M, int64_t N, int64_t K) {
   if (check_mk(M, K) != LYNX_OK || check_n(M, N) != LYNX_OK) return 0;
   return ksplit_for(sparse_shape(M, N), M, N, K);
+}
+
+int lynx_debug_force_dense_tile(int tile_cols) {
+  if (tile_cols != 0 && !pair_shape_valid(false, PairShape{1, tile_cols})) return LYNX_ERR_UNSUPPORTED;
+  g_force_dense_tile.store(tile_cols);
+  return LYNX_OK;
 }
 
 int lynx_debug_force_tile(int tile_rows, int tile_cols) {

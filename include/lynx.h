@@ -358,6 +358,12 @@ LYNX_API int lynx_debug_linear_ksplit(int64_t M, int64_t N, int64_t K);
  * Returns LYNX_OK, or LYNX_ERR_UNSUPPORTED (setting unchanged) for any other shape. */
 LYNX_API int lynx_debug_force_tile(int tile_rows, int tile_cols);
 
+/* Test hook.  Makes the dense GEMM (lynx_linear_dense and the dense layers of lynx_run_layers and the graphs
+ * built after the call) use 256 x tile_cols pair tiles for every shape: 256 (one 256-column MMA per K step) or 448
+ * (two 224-column MMAs sharing one read of X); both give the same result.  0 restores the automatic choice by
+ * shape.  Returns LYNX_OK, or LYNX_ERR_UNSUPPORTED (setting unchanged) for any other value. */
+LYNX_API int lynx_debug_force_dense_tile(int tile_cols);
+
 #ifdef __cplusplus
 }
 #endif

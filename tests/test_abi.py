@@ -153,6 +153,17 @@ def test_force_tile_accepts_only_built_shapes(asl):
         assert L.lynx_debug_force_tile(0, 0) == 0
 
 
+def test_force_dense_tile_accepts_only_built_shapes(asl):
+    L = asl.lib
+    try:
+        for cols in [224, 192, 512, -1, 1]:
+            assert L.lynx_debug_force_dense_tile(cols) == -7
+        for cols in [256, 448]:
+            assert L.lynx_debug_force_dense_tile(cols) == 0
+    finally:
+        assert L.lynx_debug_force_dense_tile(0) == 0
+
+
 @pytest.mark.parametrize("M,K", [(1, 16), (5, 136), (130, 256), (17, 96), (300, 512)])
 def test_meta_to_canonical_matches_documented_layout(asl, M, K):
     from helpers import pack_meta_reference

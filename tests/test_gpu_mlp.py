@@ -113,10 +113,15 @@ def test_fused_pair_sparse_up(lynx, M, K, Nup, Nd, tile):
         lynx.lynx_debug_force_tile(0, 0)
 
 
+@pytest.mark.parametrize("tile", [256, 448])
 @pytest.mark.parametrize("M,K,Nup,Nd", [(300, 256, 512, 200), (1, 128, 256, 64), (640, 512, 1024, 3072)])
-def test_fused_pair_dense_up(lynx, M, K, Nup, Nd):
+def test_fused_pair_dense_up(lynx, M, K, Nup, Nd, tile):
     t = _mlp_tensors(M, K, Nup, Nd, seed=7 * M + Nup, up_sparse=False)
-    layers, ws = _run_pair(lynx, *t, up_sparse=False)
+    lynx.lynx_debug_force_dense_tile(tile)
+    try:
+        layers, ws = _run_pair(lynx, *t, up_sparse=False)
+    finally:
+        lynx.lynx_debug_force_dense_tile(0)
     # the down layer run on its own (its own sparsify pass) on the same H: the same selection; only the fp32
     # order of the row-norm sums and of the LoRA down-projection differs
     up, dn = layers

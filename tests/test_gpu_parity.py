@@ -196,18 +196,42 @@ def test_linear_zero_lora_and_24_input_is_cublas_gemm(lynx):
     assert np.mean(to_bits(Y) == cub) > 0.9
 
 
+@pytest.mark.parametrize("tile", [256, 448])
 @pytest.mark.parametrize("M,N,K,lora", [(256, 512, 512, False), (300, 520, 528, True), (129, 136, 144, False),
-                                        (384, 768, 3072, True), (129, 130, 144, True)])
-def test_linear_dense(lynx, M, N, K, lora):
+                                        (384, 768, 3072, True), (129, 130, 144, True), (520, 1000, 1040, True)])
+def test_linear_dense(lynx, M, N, K, lora, tile):
     X, W, LA, LB = _layer(M, N, K, 17)
-    if lora:
-        Y = lynx.lynx_linear_dense(to_dev(X), to_dev(W), to_dev(LA), to_dev(LB))
-        ref = O.linear_dense(X, W, LA, LB)
-    else:
-        Y = lynx.lynx_linear_dense(to_dev(X), to_dev(W))
-        ref = O.linear_dense(X, W)
-    assert lynx.lynx_sync_status() == 0
+    lynx.lynx_debug_force_dense_tile(tile)
+    try:
+        if lora:
+            Y = lynx.lynx_linear_dense(to_dev(X), to_dev(W), to_dev(LA), to_dev(LB))
+            ref = O.linear_dense(X, W, LA, LB)
+        else:
+            Y = lynx.lynx_linear_dense(to_dev(X), to_dev(W))
+            ref = O.linear_dense(X, W)
+        assert lynx.lynx_sync_status() == 0
+    finally:
+        lynx.lynx_debug_force_dense_tile(0)
     assert_y_close(to_bits(Y), ref)
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 896, 512), (300, 1000, 1040), (777, 448, 3072), (1, 8, 16)])
+@pytest.mark.parametrize("lora", [False, True])
+def test_dense_wide_tile_equals_narrow_tile(lynx, M, N, K, lora):
+    """The dense 256 x 448 tile (two 224-column MMAs sharing one read of X) adds every output's products in the
+    same k order as the 256 x 256 tile, LoRA stage last: the results agree bit for bit."""
+    X, W, LA, LB = _layer(M, N, K, seed=23)
+    args = [to_dev(a) for a in ((X, W, LA, LB) if lora else (X, W))]
+    out = {}
+    for tile in (448, 256):
+        lynx.lynx_debug_force_dense_tile(tile)
+        try:
+            out[tile] = to_bits(lynx.lynx_linear_dense(*args))
+            assert lynx.lynx_sync_status() == 0
+        finally:
+            lynx.lynx_debug_force_dense_tile(0)
+    assert np.array_equal(out[448], out[256])
+    assert_y_close(out[448], O.linear_dense(X, W, LA, LB) if lora else O.linear_dense(X, W))
 
 
 def test_linear_is_deterministic(lynx):
