@@ -727,10 +727,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
       } else {
         // Split K: this unit's fp32 partial (this CTA's rows of the tile) goes to global memory, laid out as
-        // [tile][split][CTA of the pair][ROWS][TN].  Each lane writes its row's 32-column chunks (128 bytes).
+        // [tile][split][CTA of the pair][TN][ROWS]: column-major, so that one store of the 32 lanes (32 rows of a
+        // column) fills 128 contiguous bytes.
         const int64_t tile_elems = static_cast<int64_t>(C::ROWS) * TN;
-        const int64_t prow = static_cast<int64_t>(h * BLOCK + q * 32 + lane) * TN + col_off;
-        float* mine = a.partials + ((static_cast<int64_t>(tile) * S + ks) * 2 + rank) * tile_elems + prow;
+        const int64_t pcol = static_cast<int64_t>(col_off) * C::ROWS + h * BLOCK + q * 32 + lane;
+        float* mine = a.partials + ((static_cast<int64_t>(tile) * S + ks) * 2 + rank) * tile_elems + pcol;
 #pragma unroll
         for (int c2 = 0; c2 < NC; c2 += 2) {
           const bool two = c2 + 1 < NC;
@@ -743,17 +744,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster_relaxed(acc_empty_leader0 + 8 * ab);
           }
-          float4* d0 = reinterpret_cast<float4*>(mine + c2 * 32);
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            d0[v] = make_float4(__uint_as_float(r0[4 * v]), __uint_as_float(r0[4 * v + 1]),
-                                __uint_as_float(r0[4 * v + 2]), __uint_as_float(r0[4 * v + 3]));
+          for (int j = 0; j < 32; ++j) __stcg(mine + (c2 * 32 + j) * C::ROWS, __uint_as_float(r0[j]));
           if (two) {
-            float4* d1 = reinterpret_cast<float4*>(mine + (c2 + 1) * 32);
 #pragma unroll
-            for (int v = 0; v < 8; ++v)
-              d1[v] = make_float4(__uint_as_float(r1[4 * v]), __uint_as_float(r1[4 * v + 1]),
-                                  __uint_as_float(r1[4 * v + 2]), __uint_as_float(r1[4 * v + 3]));
+            for (int j = 0; j < 32; ++j) __stcg(mine + ((c2 + 1) * 32 + j) * C::ROWS, __uint_as_float(r1[j]));
           }
         }
         // Publish: every epilogue warp's partial is written (fence, then one arrival per warp); one thread
@@ -779,30 +774,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         if (!ok) break;
         if (*last_flag) {
           __threadfence();
-          const float* base = a.partials + (static_cast<int64_t>(tile) * S * 2 + rank) * tile_elems + prow;
+          const float* base = a.partials + (static_cast<int64_t>(tile) * S * 2 + rank) * tile_elems + pcol;
 #pragma unroll
           for (int c = 0; c < NC; ++c) {
             float acc[32];
-            // four columns at a time: every split's load is issued before the group is added in split order
+            // eight columns at a time: every split's loads are issued before the columns are added in split order
 #pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              float4 t[kPairMaxSplit];
-#pragma unroll
-              for (int s2 = 0; s2 < kPairMaxSplit; ++s2)
-                if (s2 < S) t[s2] = __ldcg(reinterpret_cast<const float4*>(base + s2 * 2 * tile_elems + c * 32) + v);
-              float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int j0 = 0; j0 < 32; j0 += 8) {
+              float t[kPairMaxSplit][8];
 #pragma unroll
               for (int s2 = 0; s2 < kPairMaxSplit; ++s2)
-                if (s2 < S) {
-                  sum.x += t[s2].x;
-                  sum.y += t[s2].y;
-                  sum.z += t[s2].z;
-                  sum.w += t[s2].w;
-                }
-              acc[4 * v] = sum.x;
-              acc[4 * v + 1] = sum.y;
-              acc[4 * v + 2] = sum.z;
-              acc[4 * v + 3] = sum.w;
+                if (s2 < S)
+#pragma unroll
+                  for (int jj = 0; jj < 8; ++jj)
+                    t[s2][jj] = __ldcg(base + s2 * 2 * tile_elems + (c * 32 + j0 + jj) * C::ROWS);
+#pragma unroll
+              for (int jj = 0; jj < 8; ++jj) {
+                float sum = 0.f;
+#pragma unroll
+                for (int s2 = 0; s2 < kPairMaxSplit; ++s2)
+                  if (s2 < S) sum += t[s2][jj];
+                acc[j0 + jj] = sum;
+              }
             }
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
