@@ -268,9 +268,10 @@ def main() -> int:
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="lynx", choices=["lynx", "reference"])
-    ap.add_argument("--profile-case", default=None, choices=["linear", "fused", "dense"],
-                    help="run only W + K calls of lynx_linear / lynx_linear_fused / lynx_linear_dense (no LoRA) on "
-                         "the workload and print their mean time: a short command for profilers")
+    ap.add_argument("--profile-case", default=None, choices=["linear", "fused", "dense", "wsparse"],
+                    help="run only W + K calls of lynx_linear / lynx_linear_fused / lynx_linear_dense (no LoRA) / "
+                         "lynx_linear_wsparse (W pruned and compressed once, before the calls) on the workload and "
+                         "print their mean time: a short command for profilers")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -314,10 +315,19 @@ def main() -> int:
 
     if args.profile_case:
         ws_d = torch.empty(asl.lynx_dense_workspace_bytes(M, R), dtype=torch.uint8, device=dev)
+        pruned = {}
+        if args.profile_case == "wsparse":
+            pruned = {id(s): asl.lynx_prune_weight(s["W"]) for s in sets}
+            torch.cuda.synchronize()
 
         def case(s):
             if args.profile_case == "linear":
                 return call(s)
+            if args.profile_case == "wsparse":
+                wv, wm = pruned[id(s)]
+                return L.lynx_linear_wsparse(s["X"].data_ptr(), wv.data_ptr(), wm.data_ptr(), s["LA"].data_ptr(),
+                                             s["LB"].data_ptr(), s["Y"].data_ptr(), M, N, K, R, ws_d.data_ptr(),
+                                             ws_d.numel(), sp)
             if args.profile_case == "fused":
                 return L.lynx_linear_fused(s["X"].data_ptr(), s["W"].data_ptr(), s["LA"].data_ptr(),
                                            s["LB"].data_ptr(), s["Y"].data_ptr(), M, N, K, R, ws_d.data_ptr(),
