@@ -808,6 +808,11 @@ int lynx_debug_linear_ksplit(int64_t M, int64_t N, int64_t K) {
   return ksplit_for(sparse_shape(M, N), M, N, K);
 }
 
+int lynx_debug_dense_tile(int64_t M, int64_t N) {
+  if (M < 1 || M > kMaxM || check_n(M, N) != LYNX_OK) return 0;
+  return dense_shape(M, N).tn;
+}
+
 int lynx_debug_force_dense_tile(int tile_cols) {
   if (tile_cols != 0 && !pair_shape_valid(false, PairShape{1, tile_cols})) return LYNX_ERR_UNSUPPORTED;
   g_force_dense_tile.store(tile_cols);

@@ -364,6 +364,10 @@ LYNX_API int lynx_debug_force_tile(int tile_rows, int tile_cols);
  * shape.  Returns LYNX_OK, or LYNX_ERR_UNSUPPORTED (setting unchanged) for any other value. */
 LYNX_API int lynx_debug_force_dense_tile(int tile_cols);
 
+/* The columns of the dense GEMM's pair tile (256 or 448) lynx_linear_dense picks on the current device for
+ * these sizes (the forced value while lynx_debug_force_dense_tile holds one); 0 for sizes out of range. */
+LYNX_API int lynx_debug_dense_tile(int64_t M, int64_t N);
+
 #ifdef __cplusplus
 }
 #endif

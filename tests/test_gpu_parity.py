@@ -215,6 +215,22 @@ def test_linear_dense(lynx, M, N, K, lora, tile):
     assert_y_close(to_bits(Y), ref)
 
 
+def test_dense_tile_choice(lynx):
+    """On this GPU the dense layer takes 448-column tiles where their waves are about as full as the 256-column
+    tiles' (the QKV shapes, N = 3072 at 16384 tokens) and 256-column tiles where a 448-column wave would stay
+    partly idle (N = 3072 at 4608 tokens, 1024 tokens)."""
+    for M, N in [(4608, 9216), (9216, 9216), (16384, 3072)]:
+        assert lynx.lynx_debug_dense_tile(M, N) == 448, (M, N)
+    for M, N in [(4608, 3072), (1024, 9216), (1024, 3072), (1024, 12288)]:
+        assert lynx.lynx_debug_dense_tile(M, N) == 256, (M, N)
+    lynx.lynx_debug_force_dense_tile(448)
+    try:
+        assert lynx.lynx_debug_dense_tile(1024, 3072) == 448
+    finally:
+        lynx.lynx_debug_force_dense_tile(0)
+    assert lynx.lynx_debug_dense_tile(0, 8) == 0
+
+
 @pytest.mark.parametrize("M,N,K", [(256, 896, 512), (300, 1000, 1040), (777, 448, 3072), (1, 8, 16)])
 @pytest.mark.parametrize("lora", [False, True])
 def test_dense_wide_tile_equals_narrow_tile(lynx, M, N, K, lora):
