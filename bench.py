@@ -464,6 +464,34 @@ def main() -> int:
     wsparse_ms = l0.elapsed_time(l1) / nd
     st = asl.lynx_sync_status()
     assert st == 0, asl.lynx_status_string(st)
+
+    # The library 2:4 path as shipped: torch's semi-structured sparse GEMM (cuSPARSELt) on the same pruned W, with
+    # the algorithm cuSPARSELt's own search picks (context for the weight-2:4 comparator; no LoRA branch).
+    cslt = {"unavailable": "not measured"}
+    try:
+        s0 = sets[0]
+        dense_w = torch.empty_like(s0["W"])
+        wp = s0["W"].view(N, K // 4, 4)
+        keep = wp.abs().float().topk(2, dim=-1).indices
+        dense_w.copy_((wp * torch.zeros_like(wp, dtype=torch.bool).scatter_(-1, keep, True)).view(N, K))
+        comp = torch._cslt_compress(dense_w)
+        alg = int(torch._cslt_sparse_mm_search(comp, s0["X"].t()))
+        for i in range(2):
+            torch._cslt_sparse_mm(comp, sets[i % ROTATE]["X"].t(), alg_id=alg)
+        torch.cuda.synchronize()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for i in range(10):
+            torch._cslt_sparse_mm(comp, sets[i % ROTATE]["X"].t(), alg_id=alg)
+        c1.record(stream)
+        torch.cuda.synchronize()
+        cms = c0.elapsed_time(c1) / 10
+        cslt = {"ms": cms, "tflops": flops / (cms * 1e-3) / 1e12, "x_vs_dense_cublas": dense_ms / cms,
+                "algorithm": alg, "note": "torch._cslt_sparse_mm (cuSPARSELt) with W 2:4-pruned (the two largest |w| "
+                                          "of every 4), the algorithm from cuSPARSELt's own search; no LoRA"}
+        del comp, dense_w
+    except Exception as ex:  # a torch build without cuSPARSELt for this GPU
+        cslt = {"unavailable": f"{type(ex).__name__}: {str(ex)[:160]}"}
     del wpruned, ws_w
 
     # The in-GEMM selection variant (lynx_linear_fused) at the same shape: the LoRA down-projection, then one GEMM
@@ -777,7 +805,8 @@ def main() -> int:
             "hbm_peak_GBs": hbm, "dense_bf16_peak_tflops": dense_tf,
             "weight_2to4_comparator": {"ms": wsparse_ms, "tflops": flops / (wsparse_ms * 1e-3) / 1e12,
                                        "x_vs_dense_cublas": dense_ms / wsparse_ms,
-                                       "note": "Y = X W~^T + X (LA LB)^T, W~ = 2:4-pruned W as the sparse operand"},
+                                       "note": "Y = X W~^T + X (LA LB)^T, W~ = 2:4-pruned W as the sparse operand",
+                                       "library_2to4_cusparselt": cslt},
             "in_gemm_selection": {"ms": fused_ms, "tflops": flops / (fused_ms * 1e-3) / 1e12,
                                   "x_vs_two_pass": ms_per_step / fused_ms,
                                   "note": "lynx_linear_fused: LoRA down-projection + one GEMM that selects the 2:4 "
