@@ -475,7 +475,8 @@ def main() -> int:
         keep = wp.abs().float().topk(2, dim=-1).indices
         dense_w.copy_((wp * torch.zeros_like(wp, dtype=torch.bool).scatter_(-1, keep, True)).view(N, K))
         comp = torch._cslt_compress(dense_w)
-        alg = int(torch._cslt_sparse_mm_search(comp, s0["X"].t()))
+        cs = getattr(getattr(torch._C, "_cusparselt", None), "mm_search", None)
+        alg = int(cs(comp, s0["X"].t()) if cs is not None else torch._cslt_sparse_mm_search(comp, s0["X"].t()))
         for i in range(2):
             torch._cslt_sparse_mm(comp, sets[i % ROTATE]["X"].t(), alg_id=alg)
         torch.cuda.synchronize()
@@ -795,6 +796,9 @@ def main() -> int:
         "clocks": clocks,
         "detail": {
             "stage_ms": {"sparsify_lora_down": stage_avg[0], "sparse_gemm": stage_avg[1]},
+            "stage_ms_p10_p50_p90": {
+                "sparsify_lora_down": [float(np.percentile(stage_ms[:, 0], q)) for q in (10, 50, 90)],
+                "sparse_gemm": [float(np.percentile(stage_ms[:, 1], q)) for q in (10, 50, 90)]},
             "stage_events": f"on every {PROFILE_EVERY}th timed step ({len(prof_steps)} of {args.steps})",
             "sparse_gemm_pct_of_sparse_peak": 100.0 * gemm_tf / sparse_peak,
             "step_pct_of_sparse_peak": 100.0 * (value / world) / sparse_peak,
