@@ -475,8 +475,15 @@ def main() -> int:
         keep = wp.abs().float().topk(2, dim=-1).indices
         dense_w.copy_((wp * torch.zeros_like(wp, dtype=torch.bool).scatter_(-1, keep, True)).view(N, K))
         comp = torch._cslt_compress(dense_w)
+        alg = None
         cs = getattr(getattr(torch._C, "_cusparselt", None), "mm_search", None)
-        alg = int(cs(comp, s0["X"].t()) if cs is not None else torch._cslt_sparse_mm_search(comp, s0["X"].t()))
+        if cs is not None:
+            try:
+                alg = int(cs(comp, s0["X"].t()))
+            except Exception:
+                alg = None
+        if alg is None:
+            alg = int(torch._cslt_sparse_mm_search(comp, s0["X"].t()))
         for i in range(2):
             torch._cslt_sparse_mm(comp, sets[i % ROTATE]["X"].t(), alg_id=alg)
         torch.cuda.synchronize()
