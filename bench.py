@@ -413,33 +413,36 @@ def main() -> int:
     mma_sparse_c4_tf, _ = asl.lynx_mma_rate(4, 20000)
     mma_more = {f"mode{m}": asl.lynx_mma_rate(m, 20000)[0] for m in (5, 6, 7, 8)}
 
-    # dense cuBLAS at the same shape, same rotation, same stream
-    for i in range(args.warmup):
-        torch.matmul(sets[i % ROTATE]["X"], sets[i % ROTATE]["W"].t(), out=sets[i % ROTATE]["Y"])
-    nd = min(args.steps, 500)
-    torch.cuda.synchronize()
-    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    d0.record(stream)
-    for i in range(nd):
+    # dense cuBLAS and this library's dense tcgen05 GEMM (a selectively skipped layer, no LoRA) at the same shape,
+    # same rotation, same stream, timed in alternating blocks so that both see the same clocks under the power cap
+    def cublas_dense(i):
         s = sets[i % ROTATE]
         torch.matmul(s["X"], s["W"].t(), out=s["Y"])
-    d1.record(stream)
-    torch.cuda.synchronize()
-    dense_ms = d0.elapsed_time(d1) / nd
 
-    # this library's dense tcgen05 GEMM (selectively skipped layer, no LoRA) at the same shape
+    def lynx_dense(i):
+        s = sets[i % ROTATE]
+        if L.lynx_linear_dense(s["X"].data_ptr(), s["W"].data_ptr(), None, None, s["Y"].data_ptr(), M, N, K, R, None,
+                               0, sp) != 0:
+            raise RuntimeError("lynx_linear_dense failed")
+
     for i in range(args.warmup):
-        s = sets[i % ROTATE]
-        L.lynx_linear_dense(s["X"].data_ptr(), s["W"].data_ptr(), None, None, s["Y"].data_ptr(), M, N, K, R, None, 0, sp)
+        cublas_dense(i)
+        lynx_dense(i)
+    nd_block = max(1, min(args.steps, 500) // 5)
+    nd = 5 * nd_block
+    t_arm = {"cublas": 0.0, "lynx": 0.0}
     torch.cuda.synchronize()
-    l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    l0.record(stream)
-    for i in range(nd):
-        s = sets[i % ROTATE]
-        L.lynx_linear_dense(s["X"].data_ptr(), s["W"].data_ptr(), None, None, s["Y"].data_ptr(), M, N, K, R, None, 0, sp)
-    l1.record(stream)
-    torch.cuda.synchronize()
-    lynx_dense_ms = l0.elapsed_time(l1) / nd
+    for blk in range(5):
+        for arm, fn in (("cublas", cublas_dense), ("lynx", lynx_dense)):
+            b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            b0.record(stream)
+            for i in range(nd_block):
+                fn(blk * nd_block + i)
+            b1.record(stream)
+            torch.cuda.synchronize()
+            t_arm[arm] += b0.elapsed_time(b1)
+    dense_ms = t_arm["cublas"] / nd
+    lynx_dense_ms = t_arm["lynx"] / nd
 
     # The weight-2:4 comparator at the same shape (W pruned and compressed once, outside the timed region):
     # the same sparse tensor-core path with W~ as the sparse operand, with the same rank-64 LoRA branch.
@@ -455,6 +458,7 @@ def main() -> int:
     for i in range(args.warmup):
         wsparse(i)
     torch.cuda.synchronize()
+    l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     l0.record(stream)
     for i in range(nd):
         if wsparse(i) != 0:
