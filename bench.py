@@ -220,6 +220,45 @@ def cpu_baseline_leg(t: dict) -> dict:
                    "sample": f"{rows1} rows in {secs1:.1f} s on one thread"}}
 
 
+def oracle_config_timings() -> dict:
+    """The plain C++ oracle on the host cores over the five workloads (the SURVEY's oracle-timing protocol):
+    tiny, QKV, MLP (up + down) and the CFG batch (four layers) in full on every core; the block stack at
+    M = 1024 in full (32 linears) and extrapolated linearly in M to the larger M; one thread on a row sample of
+    each layer, extrapolated to all rows (rows are independent)."""
+    import synth
+    from oracle import cpp
+    O = cpp.CppOracle(cpp.build())
+    cores = host_cores()
+
+    def run_layer(t, rows=None, threads=cores):
+        O.threads = threads
+        t0 = time.perf_counter()
+        if t["sparse"]:
+            O.linear(t["X"], t["W"], t["LA"], t["LB"], rows=rows)
+        else:
+            O.linear_dense(t["X"], t["W"], rows=rows)
+        return time.perf_counter() - t0
+
+    out = {"cores": cores, "cpu_model": cpu_model(), "configs": {}}
+    plans = [("tiny", [("tiny", "linear", None, 0)]), ("qkv", [("qkv", "qkv", None, 0)]),
+             ("mlp", [("mlp", "up", None, 0), ("mlp", "down", None, 0)]),
+             ("cfg2", [("cfg2", ly, None, 0) for ly in ("qkv", "out", "up", "down")]),
+             ("stack M=1024", [("stack", ly, 1024, b) for b in range(8) for ly in ("qkv", "out", "up", "down")])]
+    for name, layers in plans:
+        secs, secs1, flops = 0.0, 0.0, 0.0
+        for wl, ly, M, blk in layers:
+            t = synth.layer_tensors(wl, ly, M=M, block=blk)
+            secs += run_layer(t)
+            sample = np.arange(0, t["M"], max(1, t["M"] // 16))  # 16 rows on one thread
+            secs1 += run_layer(t, rows=sample, threads=1) * t["M"] / len(sample)
+            flops += 2.0 * t["M"] * t["N"] * t["K"]
+        out["configs"][name] = {"seconds": secs, "tflops": flops / secs / 1e12, "seconds_t1_extrapolated": secs1,
+                                "tflops_t1": flops / secs1 / 1e12}
+    st = out["configs"]["stack M=1024"]
+    out["configs"]["stack (extrapolated in M)"] = {f"M={m}": st["seconds"] * m / 1024 for m in (4608, 9216, 16384)}
+    return out
+
+
 def run_reference(args) -> int:
     """The oracle as it stands, on the host cores: each step is one C++ oracle call on a bounded row sample."""
     world, rank, _ = dist_env()
@@ -272,11 +311,16 @@ def main() -> int:
                     help="run only W + K calls of lynx_linear / lynx_linear_fused / lynx_linear_dense (no LoRA) / "
                          "lynx_linear_wsparse (W pruned and compressed once, before the calls) on the workload and "
                          "print their mean time: a short command for profilers")
+    ap.add_argument("--oracle-configs", action="store_true",
+                    help="time the C++ oracle on the host cores over all five workloads and exit (no GPU work)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.oracle_configs:
+        print(json.dumps({"oracle_config_timings": oracle_config_timings()}), flush=True)
+        return 0
 
     import torch
 
