@@ -221,7 +221,7 @@ def cpu_baseline_leg(t: dict) -> dict:
 
 
 def oracle_config_timings() -> dict:
-    """The plain C++ oracle on the host cores over the five workloads (the SURVEY's oracle-timing protocol):
+    """The plain C++ oracle on the host cores over the five workloads:
     tiny, QKV, MLP (up + down) and the CFG batch (four layers) in full on every core; the block stack at
     M = 1024 in full (32 linears) and extrapolated linearly in M to the larger M; one thread on a row sample of
     each layer, extrapolated to all rows (rows are independent)."""
