@@ -48,7 +48,15 @@ def _eager(lynx, layers):
     return outs
 
 
-def test_run_layers_and_graph_match_per_call_results(lynx):
+@pytest.fixture(params=[0, 448], ids=["dense_tile_auto", "dense_tile_448"])
+def dense_tile(request, lynx):
+    """The dense layers' tile: chosen by shape, or the 448-column collector tile forced on every dense layer."""
+    lynx.lynx_debug_force_dense_tile(request.param)
+    yield request.param
+    lynx.lynx_debug_force_dense_tile(0)
+
+
+def test_run_layers_and_graph_match_per_call_results(lynx, dense_tile):
     import torch
     wts = _weights(11)
     X = to_dev(synth.act_bf16((M, 512, 11), M, 512, 0.05, 8.0))
