@@ -23,7 +23,7 @@ __all__ = [
     "lynx_sync_status", "lynx_status_string", "lynx_meta_to_canonical", "lynx_debug_set_fault",
     "lynx_debug_force_tile", "lynx_debug_force_split", "lynx_debug_prologue_split",
     "lynx_debug_force_ksplit", "lynx_debug_linear_ksplit", "lynx_debug_force_dense_tile",
-    "lynx_debug_dense_tile",
+    "lynx_debug_dense_tile", "lynx_debug_auto_plan",
     "lynx_profile_next", "lynx_linear_kernel_count", "lynx_mma_rate",
     "LynxLayer", "lynx_layer", "lynx_layers_workspace_bytes", "lynx_run_layers", "LynxGraph",
     "LYNX_LAYER_SPARSE", "LYNX_LAYER_GELU", "LYNX_LAYER_FUSE_SPARSIFY", "lynx_debug_pair_offsets",
@@ -77,6 +77,8 @@ def _load() -> ctypes.CDLL:
         "lynx_debug_force_ksplit": (ctypes.c_int, [ctypes.c_int]),
         "lynx_debug_force_dense_tile": (ctypes.c_int, [ctypes.c_int]),
         "lynx_debug_dense_tile": (ctypes.c_int, [_c_i64, _c_i64]),
+        "lynx_debug_auto_plan": (ctypes.c_int, [ctypes.c_int, _c_i64, _c_i64, _c_i64, ctypes.c_int,
+                                                ctypes.POINTER(ctypes.c_int32)]),
         "lynx_debug_linear_ksplit": (ctypes.c_int, [_c_i64, _c_i64, _c_i64]),
         "lynx_profile_next": (None, [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]),
         "lynx_linear_kernel_count": (ctypes.c_int, [_c_i64, _c_i64, _c_i64, _c_i64]),
@@ -329,6 +331,14 @@ def lynx_debug_force_split(split: int) -> None:
 def lynx_debug_force_dense_tile(tile_cols: int) -> None:
     """Test hook: the dense GEMM uses 256 x ``tile_cols`` pair tiles (256 or 448) for every shape; 0 = automatic."""
     _check(lib.lynx_debug_force_dense_tile(tile_cols), "lynx_debug_force_dense_tile")
+
+
+def lynx_debug_auto_plan(sparse: bool, M: int, N: int, K: int, sms: int) -> tuple:
+    """Host logic only: (tile rows, tile columns, k-splits) the sparse (or dense) layer would choose on a GPU
+    with ``sms`` SMs."""
+    plan = (ctypes.c_int32 * 3)()
+    _check(lib.lynx_debug_auto_plan(1 if sparse else 0, M, N, K, sms, plan), "lynx_debug_auto_plan")
+    return tuple(plan)
 
 
 def lynx_debug_dense_tile(M: int, N: int) -> int:

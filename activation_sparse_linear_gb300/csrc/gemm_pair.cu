@@ -888,7 +888,11 @@ cudaError_t launch(const PairArgs& a, cudaStream_t st) {
 // 5 waves instead of 9, 0.95x the time; N = 3072 at M = 16384: 0.87x) and loses where a wave stays partly idle
 // (N = 3072 at M = 4608: 2 waves of 126 tiles instead of 3 of 216, 1.07x; M = 1024).
 PairShape pair_shape(bool sparse, int M, int N) {
-  const int64_t clusters = sm_count() / 2 > 0 ? sm_count() / 2 : 1;
+  return pair_shape_for(sparse, M, N, sm_count() / 2 > 0 ? sm_count() / 2 : 1);
+}
+
+PairShape pair_shape_for(bool sparse, int M, int N, int64_t clusters) {
+  if (clusters < 1) clusters = 1;
   auto cost = [&](int rb, int tn, double bytes_per_kmac) {
     const int64_t tiles = ((M + 256 * rb - 1) / (256 * rb)) * static_cast<int64_t>((N + tn - 1) / tn);
     const int64_t waves = (tiles + clusters - 1) / clusters;

@@ -87,6 +87,8 @@ struct PairShape {
   int rb, tn;
 };
 PairShape pair_shape(bool sparse, int M, int N);
+// The same choice for a GPU with `clusters` CTA pairs (host logic only; no device call).
+PairShape pair_shape_for(bool sparse, int M, int N, int64_t clusters);
 bool pair_shape_valid(bool sparse, PairShape shape);
 
 struct PairArgs {

@@ -158,12 +158,9 @@ Workspace carve(void* base, int64_t M, int64_t K, int64_t R) {
 // k-splits of the sparse GEMM: only the one-row-block tiles (the ones few-tile problems take) split, and only
 // when their tiles leave more than half of the CTA pairs idle; the split count (2-4, at least 8 k-steps per
 // unit) that fills the waves best wins.  A forced count (test hook) is clamped to the k-steps.
-int ksplit_for(PairShape shape, int64_t M, int64_t N, int64_t K) {
+int ksplit_auto(PairShape shape, int64_t M, int64_t N, int64_t K, int64_t clusters) {
   if (shape.rb != 1) return 1;
   const int64_t nk = (K + 127) / 128;
-  const int forced = g_force_ksplit.load();
-  if (forced) return static_cast<int>(forced < nk ? forced : nk);
-  const int64_t clusters = sm_count() / 2;
   if (clusters < 4) return 1;
   const int64_t tiles = ((M + 255) / 256) * ((N + shape.tn - 1) / shape.tn);
   if (2 * tiles > clusters) return 1;
@@ -178,6 +175,14 @@ int ksplit_for(PairShape shape, int64_t M, int64_t N, int64_t K) {
     }
   }
   return best;
+}
+
+int ksplit_for(PairShape shape, int64_t M, int64_t N, int64_t K) {
+  if (shape.rb != 1) return 1;
+  const int64_t nk = (K + 127) / 128;
+  const int forced = g_force_ksplit.load();
+  if (forced) return static_cast<int>(forced < nk ? forced : nk);
+  return ksplit_auto(shape, M, N, K, sm_count() / 2);
 }
 
 // Bytes of the split-K region for `splits` (0 for 1): fp32 partial tiles [tile][split][CTA][128 rb][tn], then one
@@ -806,6 +811,17 @@ int lynx_debug_force_ksplit(int splits) {
 int lynx_debug_linear_ksplit(int64_t M, int64_t N, int64_t K) {
   if (check_mk(M, K) != LYNX_OK || check_n(M, N) != LYNX_OK) return 0;
   return ksplit_for(sparse_shape(M, N), M, N, K);
+}
+
+int lynx_debug_auto_plan(int sparse, int64_t M, int64_t N, int64_t K, int sms, int32_t* plan) {
+  if (!plan) return LYNX_ERR_NULL;
+  if (check_mk(M, K) != LYNX_OK || check_n(M, N) != LYNX_OK || sms < 2) return LYNX_ERR_SHAPE;
+  const int64_t clusters = sms / 2;
+  const PairShape shape = pair_shape_for(sparse != 0, static_cast<int>(M), static_cast<int>(N), clusters);
+  plan[0] = 256 * shape.rb;
+  plan[1] = shape.tn;
+  plan[2] = sparse ? ksplit_auto(shape, M, N, K, clusters) : 1;
+  return LYNX_OK;
 }
 
 int lynx_debug_dense_tile(int64_t M, int64_t N) {

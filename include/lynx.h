@@ -368,6 +368,12 @@ LYNX_API int lynx_debug_force_dense_tile(int tile_cols);
  * these sizes (the forced value while lynx_debug_force_dense_tile holds one); 0 for sizes out of range. */
 LYNX_API int lynx_debug_dense_tile(int64_t M, int64_t N);
 
+/* Host logic only (no device call, no test hook applies): the pair tile and k-split count that lynx_linear
+ * (sparse != 0) or lynx_linear_dense (sparse == 0) would choose for these sizes on a GPU with `sms` SMs.
+ * plan[0] = tile rows, plan[1] = tile columns, plan[2] = k-splits (1 for the dense layer).  Returns LYNX_OK,
+ * LYNX_ERR_NULL for a NULL plan, LYNX_ERR_SHAPE for sizes out of range or sms < 2. */
+LYNX_API int lynx_debug_auto_plan(int sparse, int64_t M, int64_t N, int64_t K, int sms, int32_t* plan);
+
 #ifdef __cplusplus
 }
 #endif

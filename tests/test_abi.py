@@ -164,6 +164,36 @@ def test_force_dense_tile_accepts_only_built_shapes(asl):
         assert L.lynx_debug_force_dense_tile(0) == 0
 
 
+def test_auto_plan_on_152_sms(asl):
+    """The tile and split choice for the DiT shapes on a 152-SM GPU (76 CTA pairs), host logic only.  Waves =
+    ceil(tiles / 76); the cost compares waves x tile work x shared-memory bytes per MAC."""
+    plan = asl.lynx_debug_auto_plan
+    # sparse: QKV 9 x 42 = 378 tiles of 512 x 224 = 4.97 waves (432 tiles of 512 x 192 would take 6)
+    assert plan(True, 4608, 9216, 3072, 152) == (512, 224, 1)
+    assert plan(True, 4608, 12288, 3072, 152) == (512, 224, 1)
+    assert plan(True, 16384, 9216, 3072, 152) == (512, 224, 1)
+    # N = 3072: 224-wide columns (14 x 9 = 126 tiles) and 192-wide (16 x 9 = 144) both take 2 waves; 192 is cheaper
+    assert plan(True, 4608, 3072, 12288, 152) == (512, 192, 1)
+    # few row tiles: 4 x 36 = 144 tiles of 256 x 256 fill 2 waves; 4 x 16 = 64 of 256 x 192 fit in one
+    assert plan(True, 1024, 9216, 3072, 152) == (256, 256, 1)
+    assert plan(True, 1024, 3072, 12288, 152) == (256, 192, 1)
+    # 16 tiles leave 60 pairs idle: split K four ways (64 units, one wave)
+    assert plan(True, 256, 3072, 12288, 152) == (256, 192, 4)
+    # dense: 378 tiles of 256 x 448 (4.97 waves) beat 648 of 256 x 256 (8.53); N = 3072 at 4608 keeps 256
+    assert plan(False, 4608, 9216, 3072, 152) == (256, 448, 1)
+    assert plan(False, 4608, 12288, 3072, 152) == (256, 448, 1)
+    assert plan(False, 16384, 3072, 3072, 152) == (256, 448, 1)
+    assert plan(False, 4608, 3072, 3072, 152) == (256, 256, 1)
+    assert plan(False, 1024, 3072, 3072, 152) == (256, 256, 1)
+    # a GPU with 8 SMs (4 pairs) never splits (too few pairs to gain) and keeps the big sparse tile
+    assert plan(True, 256, 3072, 12288, 8)[2] == 1
+    import ctypes
+    p = (ctypes.c_int32 * 3)()
+    assert asl.lib.lynx_debug_auto_plan(1, 0, 8, 16, 152, p) == -2
+    assert asl.lib.lynx_debug_auto_plan(1, 8, 8, 16, 1, p) == -2
+    assert asl.lib.lynx_debug_auto_plan(1, 8, 8, 16, 152, None) == -1
+
+
 @pytest.mark.parametrize("M,K", [(1, 16), (5, 136), (130, 256), (17, 96), (300, 512)])
 def test_meta_to_canonical_matches_documented_layout(asl, M, K):
     from helpers import pack_meta_reference
