@@ -17,7 +17,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "liblynx.so")
-SOURCES = ["lynx_api.cu", "layers.cu", "prologue.cu", "gemm.cu", "gemm_pair.cu", "lora_fin.cu", "mma_rate.cu"]
+SOURCES = ["lynx_api.cu", "layers.cu", "prologue.cu", "gemm.cu", "gemm_pair.cu", "pair_plan.cu", "lora_fin.cu",
+           "mma_rate.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden"]
 
