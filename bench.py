@@ -825,8 +825,8 @@ def main() -> int:
             dist.destroy_process_group()
         return 0
 
-    # CPU baseline: the C++ oracle on bounded row samples, every host core and one thread
-    cpu_base = cpu_baseline_leg(t)
+    # CPU baseline: the C++ oracle on bounded row samples, every host core and one thread (single-GPU runs only)
+    cpu_base = cpu_baseline_leg(t) if world == 1 else None
     clocks = clk.summary()
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
