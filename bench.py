@@ -531,7 +531,10 @@ def main() -> int:
             except Exception:
                 alg = None
         if alg is None:
-            alg = int(torch._cslt_sparse_mm_search(comp, s0["X"].t()))
+            import warnings
+            with warnings.catch_warnings():
+                warnings.simplefilter("ignore")  # the older entry point warns that it is deprecated
+                alg = int(torch._cslt_sparse_mm_search(comp, s0["X"].t()))
         for i in range(2):
             torch._cslt_sparse_mm(comp, sets[i % ROTATE]["X"].t(), alg_id=alg)
         torch.cuda.synchronize()
