@@ -31,9 +31,10 @@
 // same accumulators.  Because the epilogue multiplies the tile by s, T' holds
 // (X LB^T)/s.
 //
-// Roles per CTA: warp 0 lane 0 TMA producer (both CTAs), warp 1 lane 0 MMA
-// issuer (leader only; with two row blocks warp 10 lane 0 issues the second
-// block's MMAs), warps 2-9 epilogue (two warps per TMEM lane quarter:
+// Roles per CTA: warp 0 TMA producer (both CTAs), warp 1 MMA issuer (leader
+// only; with two row blocks warp 10 issues the second block's MMAs); the whole
+// warp runs each of these loops and one lane, picked by elect.sync, issues each
+// instruction.  Warps 2-9 epilogue (two warps per TMEM lane quarter:
 // TMEM -> registers -> scale -> bf16 -> shared staging -> TMA store).  The
 // operand ring is as deep as shared memory allows: three stages for the
 // 512-row tiles, six for the dense 256 x 256 tile, four for the sparse
@@ -85,7 +86,7 @@ enum Site : int { SITE_PRODUCER = 11, SITE_MMA = 12, SITE_EPILOGUE = 13, SITE_DR
 // Per stage and CTA: sparse = 128 channels (A: 64 kept values per row, 128-byte rows, per row block; W: two
 // 64-channel sub-tiles; one metadata chunk per row block) feeding four tcgen05.mma.sp per row block;
 // dense = 64 channels feeding four tcgen05.mma per row block.  Several MMAs per barrier round keep the
-// single issuing thread ahead of the tensor pipe.
+// issuing warp ahead of the tensor pipe.
 // F1 (sparse, one row block): the stage carries the dense X tile (two 64-channel boxes per row block) instead of
 // compressed values; the epilogue warps select in registers and write the compressed values over box 0 and the
 // metadata chunk into the stage before the MMAs read them.
@@ -278,8 +279,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     for (int i = threadIdx.x; i < a.nzero; i += THREADS) a.zero[i] = 0u;
 
   if (warp == 0) {
-    if (lane == 0) {
+    {
       // ------------------------------------------------------------ TMA producer (both CTAs)
+      // The whole warp runs the loop and one elected lane issues each copy (see the warp-wide helpers).
       constexpr uint32_t STAGE_BYTES = C::LOAD_BYTES;
       constexpr uint32_t LORA_BYTES = MB * C::A_BOX + C::SUB;  // T' (one box per row block) and this CTA's LA half
       const uint32_t full_leader0 = mapa_shared(&full[0], 0);  // the leader's full barriers, 8 B apart
@@ -302,7 +304,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
         for (int it = 0; it < nst_u; ++it) {
           const int kk = kbeg + it;
-          if (!mbar_wait(&empty[st], ph ^ 1, a.ctl, SITE_PRODUCER) || *abort_flag) {
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait(&empty[st], ph ^ 1, a.ctl, SITE_PRODUCER)) || *abort_flag) {
             *abort_flag = 1;
             stop = true;
             break;
@@ -316,54 +318,54 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
               // CTA's rows of that half of LA
               const int nw0 = nb * TN + static_cast<int>(rank) * C::QN;
               if (kk < kend) {
-                if (leader) mbar_arrive_expect_tx(&full[st], 2 * (C::A_SLOT + C::B_SLOT));
-                tma_load_2d_pair(sA, &a.tmA, fb, kk * C::BK, m0);
-                tma_load_2d_pair(sB, &a.tmB, fb, kk * C::BK, nw0);
-                tma_load_2d_pair(sB + C::QN * 128, &a.tmB, fb, kk * C::BK, nw0 + C::MN);
+                if (leader) mbar_arrive_expect_tx_w(&full[st], 2 * (C::A_SLOT + C::B_SLOT));
+                tma_load_2d_pair_w(sA, &a.tmA, fb, kk * C::BK, m0);
+                tma_load_2d_pair_w(sB, &a.tmB, fb, kk * C::BK, nw0);
+                tma_load_2d_pair_w(sB + C::QN * 128, &a.tmB, fb, kk * C::BK, nw0 + C::MN);
               } else {
-                if (leader) mbar_arrive_expect_tx(&full[st], 2 * C::LORA_LOAD);
-                tma_load_2d_pair(sA, &a.tmT, fb, 0, m0);
-                tma_load_2d_pair(sA + C::A_BOX, &a.tmLA, fb, 0, nw0 + (kk - kend) * C::MN);
+                if (leader) mbar_arrive_expect_tx_w(&full[st], 2 * C::LORA_LOAD);
+                tma_load_2d_pair_w(sA, &a.tmT, fb, 0, m0);
+                tma_load_2d_pair_w(sA + C::A_BOX, &a.tmLA, fb, 0, nw0 + (kk - kend) * C::MN);
               }
             } else if (kk < kend) {
               if constexpr (F1) {  // X (dense, two boxes per row block) lands on this CTA's own barrier
-                if (leader) mbar_arrive_expect_tx(&full[st], 2 * C::B_SLOT);
-                mbar_arrive_expect_tx(&xfull[st], C::A_SLOT);
+                if (leader) mbar_arrive_expect_tx_w(&full[st], 2 * C::B_SLOT);
+                mbar_arrive_expect_tx_w(&xfull[st], C::A_SLOT);
 #pragma unroll
                 for (int h = 0; h < MB; ++h)
 #pragma unroll
                   for (int j = 0; j < C::BOXES; ++j)
-                    tma_load_2d(sA + h * C::A_BLOCK + j * C::A_BOX, &a.tmA, &xfull[st], kk * 128 + 64 * j, m0 + h * BLOCK);
+                    tma_load_2d_w(sA + h * C::A_BLOCK + j * C::A_BOX, &a.tmA, &xfull[st], kk * 128 + 64 * j, m0 + h * BLOCK);
               } else {
-                if (leader) mbar_arrive_expect_tx(&full[st], 2 * STAGE_BYTES);
+                if (leader) mbar_arrive_expect_tx_w(&full[st], 2 * STAGE_BYTES);
 #pragma unroll
                 for (int h = 0; h < MB; ++h)
 #pragma unroll
                   for (int j = 0; j < C::BOXES; ++j)  // sparse: 64 kept values per row = 128 channels
-                    tma_load_2d_pair(sA + h * C::A_BLOCK + j * C::A_BOX, &a.tmA, fb,
+                    tma_load_2d_pair_w(sA + h * C::A_BLOCK + j * C::A_BOX, &a.tmA, fb,
                                      kk * (SPARSE ? 64 : C::BK) + 64 * j, m0 + h * BLOCK);
               }
               if constexpr (SPARSE) {
-                tma_load_2d_pair(sB, &a.tmB, fb, kk * 128, n0);
-                tma_load_2d_pair(sB + C::SUB, &a.tmB, fb, kk * 128 + 64, n0);
+                tma_load_2d_pair_w(sB, &a.tmB, fb, kk * 128, n0);
+                tma_load_2d_pair_w(sB + C::SUB, &a.tmB, fb, kk * 128 + 64, n0);
                 if constexpr (!F1)
 #pragma unroll
                   for (int h = 0; h < MB; ++h)
-                    tma_load_2d_pair(sB + C::B_SLOT + h * kMetaChunkBytes, &a.tmMeta, fb, 0, meta_row[h] + 2 * kk);
+                    tma_load_2d_pair_w(sB + C::B_SLOT + h * kMetaChunkBytes, &a.tmMeta, fb, 0, meta_row[h] + 2 * kk);
               } else {
 #pragma unroll
-                for (int j = 0; j < C::BOXES; ++j) tma_load_2d_pair(sB + j * C::SUB, &a.tmB, fb, kk * C::BK + 64 * j, n0);
+                for (int j = 0; j < C::BOXES; ++j) tma_load_2d_pair_w(sB + j * C::SUB, &a.tmB, fb, kk * C::BK + 64 * j, n0);
               }
             } else {
               if constexpr (F1) {  // T' comes from the epilogue warps; the stage is free for them to write
-                if (leader) mbar_arrive_expect_tx(&full[st], 2 * C::SUB);
-                mbar_arrive(&xfull[st]);
+                if (leader) mbar_arrive_expect_tx_w(&full[st], 2 * C::SUB);
+                mbar_arrive_w(&xfull[st]);
               } else {
-                if (leader) mbar_arrive_expect_tx(&full[st], 2 * LORA_BYTES);
+                if (leader) mbar_arrive_expect_tx_w(&full[st], 2 * LORA_BYTES);
 #pragma unroll
-                for (int h = 0; h < MB; ++h) tma_load_2d_pair(sA + h * C::A_BLOCK, &a.tmT, fb, 0, m0 + h * BLOCK);
+                for (int h = 0; h < MB; ++h) tma_load_2d_pair_w(sA + h * C::A_BLOCK, &a.tmT, fb, 0, m0 + h * BLOCK);
               }
-              tma_load_2d_pair(sB, &a.tmLA, fb, 0, n0);
+              tma_load_2d_pair_w(sB, &a.tmLA, fb, 0, n0);
             }
           }
           ++g;
@@ -373,12 +375,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           }
         }
       }
-      *issued_sh = g;
+      if (lane == 0) *issued_sh = g;
     }
   } else if (warp == 1 || warp == MMA_WARP2) {
     const int k = warp == 1 ? 0 : 1;  // issuer index: row blocks h = k, k + NISS, ...
-    if (lane == 0 && leader && k < NISS) {
+    if (leader && k < NISS) {
       // ------------------------------------------------------------ MMA issuers (leader)
+      // The whole warp runs the loop and one elected lane issues each tcgen05 instruction.
       // Descriptors and TMEM addresses are built once; each stage only adds offsets, so the issuing
       // thread's work per MMA stays well under the MMA's own duration.
       constexpr uint32_t IDESC = idesc_bf16(2 * BLOCK, TN, false);
@@ -402,13 +405,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         const int nst_u = kend - kbeg + ((LORA && ks == S - 1) ? C::NH : 0);
         const int ab = tcount % C::ACC_BUFS;  // accumulator buffer of this unit
         const uint32_t acc_base = tmem + ab * C::ACC_STRIDE;
-        if (!mbar_wait(&acc_empty[ab], ((tcount / C::ACC_BUFS) & 1) ^ 1, a.ctl, SITE_MMA)) {
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&acc_empty[ab], ((tcount / C::ACC_BUFS) & 1) ^ 1, a.ctl, SITE_MMA))) {
           *abort_flag = 1;
           break;
         }
         tc_fence_after();
         for (int it = 0; it < nst_u; ++it) {
-          if (!mbar_wait(&full[st], ph, a.ctl, SITE_MMA) || (F1 && !mbar_wait(&conv_full[st], ph, a.ctl, SITE_MMA))) {
+          const bool ok = mbar_wait(&full[st], ph, a.ctl, SITE_MMA) &&
+                          (!F1 || mbar_wait(&conv_full[st], ph, a.ctl, SITE_MMA));
+          if (!__all_sync(0xFFFFFFFFu, ok)) {
             *abort_flag = 1;
             stop = true;
             break;
@@ -425,14 +430,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 #pragma unroll
               for (int j = 0; j < 4; ++j) {
                 const uint32_t accj = (it | j) != 0;
-                tc_mma_pair_fill(acc_base, ad + 2 * j, bd + 2 * j, IDESC_W, accj);
-                tc_mma_pair_lastuse(acc_base + C::MN, ad + 2 * j, bd + BH + 2 * j, IDESC_W, accj);
+                tc_mma_pair_fill_w(acc_base, ad + 2 * j, bd + 2 * j, IDESC_W, accj);
+                tc_mma_pair_lastuse_w(acc_base + C::MN, ad + 2 * j, bd + BH + 2 * j, IDESC_W, accj);
               }
             } else {  // LoRA stage of column half L: T' against that half's LA rows (after T' in the slot)
               const uint32_t d = acc_base + (it - (kend - kbeg)) * C::MN;
               const uint64_t lh = a0 + st * STEP + (C::A_BOX >> 4);
 #pragma unroll
-              for (int j = 0; j < 4; ++j) tc_mma_pair(d, ad + 2 * j, lh + 2 * j, IDESC_W, 1);
+              for (int j = 0; j < 4; ++j) tc_mma_pair_w(d, ad + 2 * j, lh + 2 * j, IDESC_W, 1);
             }
           } else if (kbeg + it < kend) {
             if constexpr (SPARSE) {
@@ -441,7 +446,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 #pragma unroll
               for (int hh = 0; hh < MB / NISS; ++hh) {
                 const int h = k + hh * NISS;
-                tc_cp_pair_128x128b(grp0 + h * META_GROUP_COLS, e0 + st * STEP + h * MCHUNK);
+                tc_cp_pair_128x128b_w(grp0 + h * META_GROUP_COLS, e0 + st * STEP + h * MCHUNK);
               }
 #pragma unroll
               for (int hh = 0; hh < MB / NISS; ++hh) {
@@ -450,10 +455,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 // metadata column pair j/2 of row block h's group with selector j%2
                 const uint32_t d = acc_base + h * TN, grp = grp0 + h * META_GROUP_COLS;
                 const uint64_t ah = ad + h * ABLK;
-                tc_mma_sp_pair(d, ah, bd, grp, IDESC_SP, acc0);
-                tc_mma_sp_pair(d, ah + 2, bd + 4, grp, IDESC_SP | 1u, 1);
-                tc_mma_sp_pair(d, ah + 4, bd + WSUB, grp + 2, IDESC_SP, 1);
-                tc_mma_sp_pair(d, ah + 6, bd + WSUB + 4, grp + 2, IDESC_SP | 1u, 1);
+                tc_mma_sp_pair_w(d, ah, bd, grp, IDESC_SP, acc0);
+                tc_mma_sp_pair_w(d, ah + 2, bd + 4, grp, IDESC_SP | 1u, 1);
+                tc_mma_sp_pair_w(d, ah + 4, bd + WSUB, grp + 2, IDESC_SP, 1);
+                tc_mma_sp_pair_w(d, ah + 6, bd + WSUB + 4, grp + 2, IDESC_SP | 1u, 1);
               }
             } else {
 #pragma unroll
@@ -463,10 +468,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 const uint64_t ah = ad + h * ABLK;
 #pragma unroll
                 for (int j = 0; j < C::BOXES; ++j) {  // box j: A box j and W sub-tile j, four K = 16 steps
-                  tc_mma_pair(d, ah + j * ABOX, bd + j * WSUB, IDESC, acc0 | j);
-                  tc_mma_pair(d, ah + j * ABOX + 2, bd + j * WSUB + 2, IDESC, 1);
-                  tc_mma_pair(d, ah + j * ABOX + 4, bd + j * WSUB + 4, IDESC, 1);
-                  tc_mma_pair(d, ah + j * ABOX + 6, bd + j * WSUB + 6, IDESC, 1);
+                  tc_mma_pair_w(d, ah + j * ABOX, bd + j * WSUB, IDESC, acc0 | j);
+                  tc_mma_pair_w(d, ah + j * ABOX + 2, bd + j * WSUB + 2, IDESC, 1);
+                  tc_mma_pair_w(d, ah + j * ABOX + 4, bd + j * WSUB + 4, IDESC, 1);
+                  tc_mma_pair_w(d, ah + j * ABOX + 6, bd + j * WSUB + 6, IDESC, 1);
                 }
               }
             }
@@ -476,23 +481,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
               const int h = k + hh * NISS;
               const uint32_t d = acc_base + h * TN;
               const uint64_t ah = ad + h * ABLK;
-              tc_mma_pair(d, ah, bd, IDESC, 1);
-              tc_mma_pair(d, ah + 2, bd + 2, IDESC, 1);
-              tc_mma_pair(d, ah + 4, bd + 4, IDESC, 1);
-              tc_mma_pair(d, ah + 6, bd + 6, IDESC, 1);
+              tc_mma_pair_w(d, ah, bd, IDESC, 1);
+              tc_mma_pair_w(d, ah + 2, bd + 2, IDESC, 1);
+              tc_mma_pair_w(d, ah + 4, bd + 4, IDESC, 1);
+              tc_mma_pair_w(d, ah + 6, bd + 6, IDESC, 1);
             }
           }
-          tc_commit_pair(&empty[st], 0x3);
+          tc_commit_pair_w(&empty[st], 0x3);
           ++g;
           if (++st == C::NST) {
             st = 0;
             ph ^= 1;
           }
         }
-        if (!stop) tc_commit_pair(&acc_full[ab], 0x3);
+        if (!stop) tc_commit_pair_w(&acc_full[ab], 0x3);
       }
-      consumed_sh[k] = g;
-      tc_commit_pair(drain, 0x1);  // every MMA of both issuers has completed once this phase completes
+      if (lane == 0) consumed_sh[k] = g;
+      tc_commit_pair_w(drain, 0x1);  // every MMA of both issuers has completed once this phase completes
       mbar_wait(drain, 0, a.ctl, SITE_DRAIN);
     }
   } else {
