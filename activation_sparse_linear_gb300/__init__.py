@@ -34,6 +34,7 @@ LYNX_ERR_TIMEOUT = -6
 LYNX_LAYER_SPARSE = 1
 LYNX_LAYER_GELU = 2
 LYNX_LAYER_FUSE_SPARSIFY = 4
+LYNX_KSPLIT_STREAM = 8  # lynx_debug_force_ksplit / lynx_debug_linear_ksplit: the stream-K schedule
 
 _c_i64, _c_sz, _c_p = ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p
 
@@ -348,12 +349,13 @@ def lynx_debug_dense_tile(M: int, N: int) -> int:
 
 def lynx_debug_force_ksplit(splits: int) -> None:
     """Test hook: the sparse GEMM splits the k-steps of each one-row-block tile (256 x 256, 256 x 192) over
-    ``splits`` units; 0 = automatic."""
+    ``splits`` units, or runs the stream-K schedule (``LYNX_KSPLIT_STREAM``) where it applies; 0 = automatic."""
     _check(lib.lynx_debug_force_ksplit(splits), "lynx_debug_force_ksplit")
 
 
 def lynx_debug_linear_ksplit(M: int, N: int, K: int) -> int:
-    """The k-split count lynx_linear picks on this device for M x K -> N (1 = none)."""
+    """The k-split schedule lynx_linear picks on this device for M x K -> N (1 = none, 2-4 = equal splits,
+    ``LYNX_KSPLIT_STREAM`` = stream-K)."""
     return lib.lynx_debug_linear_ksplit(M, N, K)
 
 

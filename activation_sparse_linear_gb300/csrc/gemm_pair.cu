@@ -180,6 +180,43 @@ __device__ __forceinline__ void store_chunk_t(void* Y, int64_t ldy, int zrow, in
 // stage's X rows (two threads per row, 64 channels each), keep the top two of every four in registers, write the
 // compressed values and the metadata into the stage, add x^2 and kept x^2 over the tile's whole K, and at the
 // LoRA stage write T' = bf16(T / s) of their rows (T = X LB^T, unscaled, from a.lora_t) in place of a loaded T'.
+// One work unit: k-steps [kbeg, kend) of a tile, part `seg` of the tile's `nseg` parts (in k order).
+struct Unit {
+  int tile, kbeg, kend, seg, nseg;
+};
+// The u-th unit of CTA pair `cluster` of `nclusters`; false past the last.  The tile and split schedules deal
+// (tile, split) units out round-robin, tile fastest, each tile cut into S equal k-ranges.  Stream-K gives pair c
+// the contiguous range [c T / P, (c + 1) T / P) of all T = ntiles nk k-steps (tile-major order, P pairs): a tile
+// is cut wherever a pair's range ends, and the pairs that share it leave partials as split units do (at most
+// kPairMaxSplit parts; the host enables it only where ntiles >= P / 2 and nk >= 8, which guarantees that).
+__device__ __forceinline__ bool unit_at(int u, int cluster, int nclusters, int ntiles, int nk, int S, bool streamk,
+                                        Unit& o) {
+  if (!streamk) {
+    const int unit = cluster + u * nclusters;
+    if (unit >= ntiles * S) return false;
+    const int ks = unit / ntiles;
+    o.tile = unit % ntiles;
+    o.kbeg = ks * nk / S;
+    o.kend = (ks + 1) * nk / S;
+    o.seg = ks;
+    o.nseg = S;
+    return true;
+  }
+  const int64_t T = static_cast<int64_t>(ntiles) * nk;
+  const int64_t b0 = cluster * T / nclusters, b1 = (cluster + 1) * T / nclusters;
+  const int64_t t = b0 / nk + u;
+  if (b0 >= b1 || t * nk >= b1) return false;
+  // the pair whose range holds k-step s: the last c with c T / P <= s
+  auto owner = [&](int64_t st) { return static_cast<int>(((st + 1) * nclusters - 1) / T); };
+  o.tile = static_cast<int>(t);
+  o.kbeg = static_cast<int>(b0 > t * nk ? b0 - t * nk : 0);
+  o.kend = static_cast<int>(b1 < (t + 1) * nk ? b1 - t * nk : nk);
+  const int first = owner(t * nk);
+  o.seg = cluster - first;
+  o.nseg = owner(t * nk + nk - 1) - first + 1;
+  return true;
+}
+
 template <bool SPARSE, bool LORA, int MB, int TN, bool TRANS, bool SPLIT, bool GELU, bool F1 = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ PairArgs a) {
@@ -224,7 +261,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   // the last split also the LoRA stage.  With S > 1 each unit leaves an fp32 partial in global memory and the
   // last unit of a tile to finish adds the S partials in split order (see the epilogue).
   const int S = SPLIT ? a.splits : 1;
-  const int nunits = ntiles * S;
+  const bool streamk = SPLIT && a.stream_k != 0;  // stream-K: S is the partials' stride, kPairMaxSplit
   const int64_t blocks_k = meta_blocks_k(a.K);
   const int meta_rowblocks = static_cast<int>(round_up(a.M, kMetaRowPad) / kMetaRows);
 
@@ -288,10 +325,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       int g = 0, st = 0;
       uint32_t ph = 0;
       bool stop = false;
-      for (int unit = cluster; unit < nunits && !stop; unit += nclusters) {
-        const int tile = unit % ntiles, ks = unit / ntiles;
-        const int kbeg = ks * nk / S, kend = (ks + 1) * nk / S;
-        const int nst_u = kend - kbeg + ((LORA && ks == S - 1) ? C::NH : 0);
+      Unit un;
+      for (int u = 0; !stop && unit_at(u, cluster, nclusters, ntiles, nk, S, streamk, un); ++u) {
+        const int tile = un.tile, kbeg = un.kbeg, kend = un.kend;
+        const int nst_u = kend - kbeg + ((LORA && kend == nk) ? C::NH : 0);
         const int mp = tile % num_mp, nb = tile / num_mp;
         const int m0 = mp * 2 * C::ROWS + static_cast<int>(rank) * C::ROWS;
         const int n0 = nb * TN + static_cast<int>(rank) * C::HALF_N;
@@ -399,10 +436,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       int g = 0, st = 0, tcount = 0, mring = 0;
       uint32_t ph = 0;
       bool stop = false;
-      for (int unit = cluster; unit < nunits && !stop; unit += nclusters, ++tcount) {
-        const int ks = unit / ntiles;
-        const int kbeg = ks * nk / S, kend = (ks + 1) * nk / S;
-        const int nst_u = kend - kbeg + ((LORA && ks == S - 1) ? C::NH : 0);
+      Unit un;
+      for (int u = 0; !stop && unit_at(u, cluster, nclusters, ntiles, nk, S, streamk, un); ++u, ++tcount) {
+        const int kbeg = un.kbeg, kend = un.kend;
+        const int nst_u = kend - kbeg + ((LORA && kend == nk) ? C::NH : 0);
         const int ab = tcount % C::ACC_BUFS;  // accumulator buffer of this unit
         const uint32_t acc_base = tmem + ab * C::ACC_STRIDE;
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(&acc_empty[ab], ((tcount / C::ACC_BUFS) & 1) ^ 1, a.ctl, SITE_MMA))) {
@@ -594,8 +631,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       bool oks = mbar_wait(s_bar, tcount & 1, a.ctl, SITE_EPILOGUE);
       return __all_sync(0xFFFFFFFFu, oks) && !*abort_flag;
     };
-    for (int unit = cluster; unit < nunits; unit += nclusters, ++tcount) {
-      const int tile = unit % ntiles, ks = unit / ntiles;
+    Unit un;
+    for (int u = 0; unit_at(u, cluster, nclusters, ntiles, nk, S, streamk, un); ++u, ++tcount) {
+      const int tile = un.tile, ks = un.seg;
       const int mp = tile % num_mp, nb = tile / num_mp;
       const int row0 = mp * 2 * C::ROWS + static_cast<int>(rank) * C::ROWS + h * BLOCK + q * 32;
       const int row = row0 + lane;
@@ -699,7 +737,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
         write_chunk(c);
       };
-      if constexpr (!SPLIT) {
+      if (!SPLIT || un.nseg == 1) {  // a whole tile (stream-K leaves some tiles whole)
 #pragma unroll
         for (int c2 = 0; c2 < NC; c2 += 2) {
           const bool two = c2 + 1 < NC;
@@ -734,6 +772,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           if (a.hvals && live) a.hnorm[static_cast<int64_t>(row) * a.hnorm_slots + n0 / COLS] = make_float2(hn_all, hn_kept);
         }
       } else {
+        if (un.nseg > S) {  // never: the host enables stream-K only where a tile has at most S parts
+          if (lane == 0) {
+            *abort_flag = 1;
+            record_error(a.ctl, SITE_EPILOGUE);
+          }
+          break;
+        }
         // Split K: this unit's fp32 partial (this CTA's rows of the tile) goes to global memory, laid out as
         // [tile][split][CTA of the pair][TN][ROWS]: column-major, so that one store of the 32 lanes (32 rows of a
         // column) fills 128 contiguous bytes.
@@ -760,8 +805,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           }
         }
         // Publish: every epilogue warp's partial is written (fence, then one arrival per warp); one thread
-        // takes the tile's arrival ticket.  The unit that draws the last ticket adds the S partials in split
-        // order -- the same order whichever unit finishes last, so the result does not depend on timing --
+        // takes the tile's arrival ticket.  The unit that draws the last ticket adds the tile's nseg partials in
+        // k order -- the same order whichever unit finishes last, so the result does not depend on timing --
         // and writes Y.  No unit waits for another: the others go on to their next unit.
         __threadfence();
         __syncwarp();
@@ -773,7 +818,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                        : "=r"(ticket)
                        : "l"(a.counters + 2 * tile + static_cast<int>(rank))
                        : "memory");
-          *last_flag = ticket == static_cast<unsigned int>(S - 1);
+          *last_flag = ticket == static_cast<unsigned int>(un.nseg - 1);
           mbar_arrive(epi_bar2);
         }
         ok = ok && mbar_wait(epi_bar2, nsplit & 1, a.ctl, SITE_EPILOGUE);
@@ -792,7 +837,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
               float t[kPairMaxSplit][8];
 #pragma unroll
               for (int s2 = 0; s2 < kPairMaxSplit; ++s2)
-                if (s2 < S)
+                if (s2 < un.nseg)
 #pragma unroll
                   for (int jj = 0; jj < 8; ++jj)
                     t[s2][jj] = __ldcg(base + s2 * 2 * tile_elems + (c * 32 + j0 + jj) * C::ROWS);
@@ -801,7 +846,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 float sum = 0.f;
 #pragma unroll
                 for (int s2 = 0; s2 < kPairMaxSplit; ++s2)
-                  if (s2 < S) sum += t[s2][jj];
+                  if (s2 < un.nseg) sum += t[s2][jj];
                 acc[j0 + jj] = sum;
               }
             }
@@ -863,9 +908,12 @@ cudaError_t launch(const PairArgs& a, cudaStream_t st) {
     attr_set[dev] = true;
   }
   const int ntiles = ((a.M + 2 * C::ROWS - 1) / (2 * C::ROWS)) * ((a.N + TN - 1) / TN);
-  const int nunits = ntiles * (SPLIT ? a.splits : 1);
+  const int nk = (a.K + C::BK - 1) / C::BK;
+  // stream-K: every pair takes a share of the k-steps (at least one each); otherwise one pair per unit at most
+  const int64_t nunits = (SPLIT && a.stream_k) ? static_cast<int64_t>(ntiles) * nk
+                                               : static_cast<int64_t>(ntiles) * (SPLIT ? a.splits : 1);
   int clusters = sm_count() / 2;
-  if (clusters > nunits) clusters = nunits;
+  if (clusters > nunits) clusters = static_cast<int>(nunits);
   if (clusters < 1) clusters = 1;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];

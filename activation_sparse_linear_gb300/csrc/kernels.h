@@ -105,6 +105,7 @@ struct PairArgs {
   int64_t ldy;
   int M, N, K;
   int splits;              // k-splits per tile (1: none); > 1 needs partials and counters
+  int stream_k;            // with splits = kPairMaxSplit: stream-K (contiguous k-step ranges per CTA pair)
   float* partials;         // fp32 partial tiles, [tile][split][CTA][rows][TN] (splits > 1)
   unsigned int* counters;  // one arrival counter per (tile, CTA), zero on entry (splits > 1)
   // GELU epilogue (the MLP up layer): Y = bf16(GELU(bf16(y))); with hvals non-NULL the epilogue also writes the

@@ -155,9 +155,24 @@ Workspace carve(void* base, int64_t M, int64_t K, int64_t R) {
   return w;
 }
 
-// k-splits of the sparse GEMM: only the one-row-block tiles (the ones few-tile problems take) split, and only
-// when their tiles leave more than half of the CTA pairs idle; the split count (2-4, at least 8 k-steps per
-// unit) that fills the waves best wins.  A forced count (test hook) is clamped to the k-steps.
+constexpr int kStreamK = LYNX_KSPLIT_STREAM;  // schedule code of stream-K; its partials use kMaxKSplit slots
+
+// Partial slots per tile of a k-split schedule (1: none).
+int split_stride(int sched) { return sched == kStreamK ? kMaxKSplit : sched; }
+
+// Stream-K cuts a tile into at most kMaxKSplit parts where there are at least half as many tiles as CTA pairs and
+// each tile has at least 8 k-steps: every pair's range then spans at least half a tile.
+bool stream_k_fits(PairShape shape, int64_t M, int64_t N, int64_t K, int64_t clusters) {
+  const int64_t nk = (K + 127) / 128;
+  const int64_t tiles = ((M + 255) / 256) * ((N + shape.tn - 1) / shape.tn);
+  return shape.rb == 1 && clusters >= 1 && 2 * tiles >= clusters && nk >= 8;
+}
+
+// k-split schedule of the sparse GEMM: only the one-row-block tiles (the ones few-tile problems take) split, and
+// only when their tiles leave more than half of the CTA pairs idle; the split count (2-4, at least 8 k-steps per
+// unit) that fills the waves best wins.  Stream-K is never chosen here: it was slower than the unsplit schedule at
+// every few-tile shape measured (a tile's last part ends with its pair's range, so every pair finishes with a
+// partial sum); the test hook selects it.  A forced count (test hook) is clamped to the k-steps.
 int ksplit_auto(PairShape shape, int64_t M, int64_t N, int64_t K, int64_t clusters) {
   if (shape.rb != 1) return 1;
   const int64_t nk = (K + 127) / 128;
@@ -181,6 +196,7 @@ int ksplit_for(PairShape shape, int64_t M, int64_t N, int64_t K) {
   if (shape.rb != 1) return 1;
   const int64_t nk = (K + 127) / 128;
   const int forced = g_force_ksplit.load();
+  if (forced == kStreamK) return stream_k_fits(shape, M, N, K, sm_count() / 2) ? kStreamK : 1;
   if (forced) return static_cast<int>(forced < nk ? forced : nk);
   return ksplit_auto(shape, M, N, K, sm_count() / 2);
 }
@@ -336,10 +352,12 @@ int linear_impl(const void* X, const void* W, const void* LA, const void* LB, vo
   PairArgs g;
   if (int e = sparse_gemm_args(&g, ws.vals, ws.meta, ws.s, ws.T, W, LA, Y, M, N, K, R, shape)) return e;
   // split K when the workspace holds the partials (else the unsplit schedule, which needs only the base part)
-  int splits = gelu ? 1 : ksplit_for(shape, M, N, K);
+  const int sched = gelu ? 1 : ksplit_for(shape, M, N, K);
+  int splits = split_stride(sched);
   size_t counters_off = 0;
   if (splits > 1 && workspace_bytes < ws.bytes + split_bytes(shape, M, N, splits, &counters_off)) splits = 1;
   g.splits = splits;
+  g.stream_k = splits > 1 && sched == kStreamK;
   if (splits > 1) {
     g.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + ws.bytes);
     g.counters = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(workspace) + ws.bytes + counters_off);
@@ -422,6 +440,7 @@ int single_status(const lynx_layer& l, const void* ws, size_t ws_bytes) {
 struct PairPlan {
   PairShape up_shape{1, 256}, dn_shape{1, 256};
   int slots = 0, fin_splits = 1, dn_splits = 1, fin_counters = 0, dn_counters = 0;
+  bool dn_stream = false;  // the down GEMM runs the stream-K schedule (dn_splits = its partial slots)
   size_t up_bytes = 0, dn_off = 0, hnorm_off = 0, fin_off = 0, cnt_off = 0, dsplit_off = 0, total = 0;
 };
 
@@ -440,7 +459,9 @@ PairPlan plan_pair(const lynx_layer& up, const lynx_layer& dn) {
   p.slots = gelu_norm_slots(is_sparse(up), p.up_shape, static_cast<int>(up.N));
   p.fin_splits = lora_fin_splits(static_cast<int>(M), static_cast<int>(dn.K));
   p.dn_shape = sparse_shape(M, dn.N);
-  p.dn_splits = ksplit_for(p.dn_shape, M, dn.N, dn.K);
+  const int dn_sched = ksplit_for(p.dn_shape, M, dn.N, dn.K);
+  p.dn_splits = split_stride(dn_sched);
+  p.dn_stream = dn_sched == kStreamK;
   p.fin_counters = p.fin_splits > 1 ? lora_fin_counters(static_cast<int>(M)) : 0;
   size_t dn_cnt_off = 0;
   const size_t dsplit = split_bytes(p.dn_shape, M, dn.N, p.dn_splits, &dn_cnt_off);
@@ -503,6 +524,7 @@ int run_pair(const lynx_layer& up, const lynx_layer& dn, const PairPlan& p, void
                                 p.dn_shape))
     return ge;
   g.splits = p.dn_splits;
+  g.stream_k = p.dn_splits > 1 && p.dn_stream;
   if (p.dn_splits > 1) {
     g.partials = reinterpret_cast<float*>(base + p.dsplit_off);
     g.counters = counters + p.fin_counters;
@@ -590,7 +612,7 @@ size_t lynx_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t R) {
   size_t b = carve(nullptr, M, K, R).bytes;
   if (N >= 1 && N <= (int64_t(1) << 24) && M <= 65535LL * 128) {
     const PairShape shape = sparse_shape(M, N);
-    b += split_bytes(shape, M, N, ksplit_for(shape, M, N, K));
+    b += split_bytes(shape, M, N, split_stride(ksplit_for(shape, M, N, K)));
   }
   return b;
 }
@@ -803,7 +825,7 @@ int lynx_debug_prologue_split(int64_t M, int64_t K) {
 }
 
 int lynx_debug_force_ksplit(int splits) {
-  if (splits < 0 || splits > kMaxKSplit) return LYNX_ERR_UNSUPPORTED;
+  if ((splits < 0 || splits > kMaxKSplit) && splits != kStreamK) return LYNX_ERR_UNSUPPORTED;
   g_force_ksplit.store(splits);
   return LYNX_OK;
 }

@@ -341,14 +341,23 @@ LYNX_API int lynx_debug_force_split(int split);
  * each CTA owns whole rows); 0 for sizes out of range. */
 LYNX_API int lynx_debug_prologue_split(int64_t M, int64_t K);
 
+/* Schedule code of the sparse GEMM's stream-K schedule ("RT-Lynx" page, Method, CUDA kernel optimisation: the
+ * page splits its sparse GEMM's work stream-K fashion): CTA pair c of P takes the contiguous range
+ * [c T / P, (c + 1) T / P) of all T = tiles x k-steps, so a tile is cut wherever a range ends; the pairs that
+ * share a tile leave fp32 partials and the last to finish adds them in k order.  Only the test hook selects it:
+ * it was slower than the unsplit schedule at every few-tile shape measured. */
+#define LYNX_KSPLIT_STREAM 8
+
 /* Test hook.  splits = 1 .. 4 makes the sparse GEMM of every later lynx_linear call whose tile shape has one row
- * block per CTA (256 x 256 or 256 x 192) split each tile's k-steps over that many work units (clamped to the tile's 128-channel steps; 1 =
- * never split); 0 restores the automatic choice.  lynx_workspace_bytes follows the setting.  Returns LYNX_OK, or
- * LYNX_ERR_UNSUPPORTED (setting unchanged) for other values. */
+ * block per CTA (256 x 256 or 256 x 192) split each tile's k-steps over that many work units (clamped to the tile's
+ * 128-channel steps; 1 = never split); LYNX_KSPLIT_STREAM selects the stream-K schedule for those tiles wherever
+ * it applies (at least half as many tiles as CTA pairs and 8 k-steps per tile; elsewhere no split); 0 restores
+ * the automatic choice.  lynx_workspace_bytes follows the setting.  Returns LYNX_OK, or LYNX_ERR_UNSUPPORTED
+ * (setting unchanged) for other values. */
 LYNX_API int lynx_debug_force_ksplit(int splits);
 
-/* The k-split count lynx_linear picks on the current device for these sizes (1 = no split); 0 for sizes out of
- * range. */
+/* The k-split schedule lynx_linear picks on the current device for these sizes (1 = no split, 2 .. 4 = that many
+ * equal k-ranges per tile, LYNX_KSPLIT_STREAM = stream-K); 0 for sizes out of range. */
 LYNX_API int lynx_debug_linear_ksplit(int64_t M, int64_t N, int64_t K);
 
 /* Test hook.  Makes lynx_linear (and lynx_linear_wsparse, whose tile rows are output columns) use sparse
@@ -370,7 +379,8 @@ LYNX_API int lynx_debug_dense_tile(int64_t M, int64_t N);
 
 /* Host logic only (no device call, no test hook applies): the pair tile and k-split count that lynx_linear
  * (sparse != 0) or lynx_linear_dense (sparse == 0) would choose for these sizes on a GPU with `sms` SMs.
- * plan[0] = tile rows, plan[1] = tile columns, plan[2] = k-splits (1 for the dense layer).  Returns LYNX_OK,
+ * plan[0] = tile rows, plan[1] = tile columns, plan[2] = the k-split schedule as lynx_debug_linear_ksplit reports it
+ * (1 for the dense layer).  Returns LYNX_OK,
  * LYNX_ERR_NULL for a NULL plan, LYNX_ERR_SHAPE for sizes out of range or sms < 2. */
 LYNX_API int lynx_debug_auto_plan(int sparse, int64_t M, int64_t N, int64_t K, int sms, int32_t* plan);
 

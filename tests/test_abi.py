@@ -133,13 +133,15 @@ def test_force_split_range(asl):
 def test_force_ksplit_range(asl):
     L = asl.lib
     try:
-        for bad in (-1, 5, 64):
+        for bad in (-1, 5, 7, 9, 64):
             assert L.lynx_debug_force_ksplit(bad) == -7
-        for ok in (1, 2, 3, 4):
+        for ok in (1, 2, 3, 4, asl.LYNX_KSPLIT_STREAM):
             assert L.lynx_debug_force_ksplit(ok) == 0
     finally:
         assert L.lynx_debug_force_ksplit(0) == 0
     assert L.lynx_debug_linear_ksplit(0, 16, 16) == 0 and L.lynx_debug_linear_ksplit(16, 16, 24) == 0
+    # the binding's schedule code is the header's
+    assert re.search(r"#define LYNX_KSPLIT_STREAM (\d+)", open(HEADER).read()).group(1) == str(asl.LYNX_KSPLIT_STREAM)
 
 
 def test_force_tile_accepts_only_built_shapes(asl):
@@ -174,9 +176,11 @@ def test_auto_plan_on_152_sms(asl):
     assert plan(True, 16384, 9216, 3072, 152) == (512, 224, 1)
     # N = 3072: 224-wide columns (14 x 9 = 126 tiles) and 192-wide (16 x 9 = 144) both take 2 waves; 192 is cheaper
     assert plan(True, 4608, 3072, 12288, 152) == (512, 192, 1)
-    # few row tiles: 4 x 36 = 144 tiles of 256 x 256 fill 2 waves; 4 x 16 = 64 of 256 x 192 fit in one
+    # few row tiles: 4 x 36 = 144 tiles of 256 x 256 fill 2 waves; 4 x 16 = 64 of 256 x 192 fit in one (stream-K,
+    # measured slower there, is never chosen)
     assert plan(True, 1024, 9216, 3072, 152) == (256, 256, 1)
     assert plan(True, 1024, 3072, 12288, 152) == (256, 192, 1)
+    assert plan(True, 1024, 3072, 3072, 152) == (256, 192, 1)
     # 16 tiles leave 60 pairs idle: split K four ways (64 units, one wave)
     assert plan(True, 256, 3072, 12288, 152) == (256, 192, 4)
     # dense: 378 tiles of 256 x 448 (4.97 waves) beat 648 of 256 x 256 (8.53); N = 3072 at 4608 keeps 256

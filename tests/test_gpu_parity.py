@@ -354,6 +354,51 @@ def test_split_k_is_deterministic_and_reuses_its_workspace(lynx):
     assert_y_close(outs[0], O.linear(to_bits(X), to_bits(W), to_bits(LA), to_bits(LB)))
 
 
+# ------------------------------------------------------------------ stream-K
+@pytest.mark.parametrize("tile", [(256, 256), (256, 192)])
+@pytest.mark.parametrize("M,N,K", [(1100, 2000, 1104), (520, 4000, 2048)])
+def test_linear_stream_k(lynx, M, N, K, tile):
+    """Stream-K: each CTA pair takes a contiguous share of all tiles' k-steps, so tiles are cut at arbitrary steps
+    (ragged M, N and K included); the pairs that share a tile leave fp32 partials, the last to finish adds them in
+    k order and the LoRA stage runs in the part holding the tile's last k-step; a tile one pair covers whole is
+    written directly."""
+    X, W, LA, LB = _layer(M, N, K, seed=33)
+    lynx.lynx_debug_force_tile(*tile)
+    lynx.lynx_debug_force_ksplit(lynx.LYNX_KSPLIT_STREAM)
+    try:
+        assert lynx.lynx_debug_linear_ksplit(M, N, K) == lynx.LYNX_KSPLIT_STREAM
+        Y = lynx.lynx_linear(to_dev(X), to_dev(W), to_dev(LA), to_dev(LB))
+        assert lynx.lynx_sync_status() == 0
+    finally:
+        lynx.lynx_debug_force_ksplit(0)
+        lynx.lynx_debug_force_tile(0, 0)
+    assert_y_close(to_bits(Y), O.linear(X, W, LA, LB))
+
+
+def test_stream_k_is_deterministic_and_falls_back(lynx):
+    """Repeated stream-K calls on one workspace give the same bits (the parts of a tile are added in k order
+    whichever pair finishes last); where stream-K cannot cut the tiles into at most four parts (fewer tiles than
+    half the CTA pairs) the forced setting runs the unsplit schedule."""
+    import torch
+    M, N, K = 1024, 3072, 2048
+    X, W, LA, LB = (to_dev(a) for a in _layer(M, N, K, seed=35))
+    lynx.lynx_debug_force_tile(256, 192)
+    lynx.lynx_debug_force_ksplit(lynx.LYNX_KSPLIT_STREAM)
+    try:
+        assert lynx.lynx_debug_linear_ksplit(M, N, K) == lynx.LYNX_KSPLIT_STREAM
+        assert lynx.lynx_debug_linear_ksplit(256, 1536, 2048) == 1  # 8 tiles
+        ws = torch.empty(lynx.lynx_workspace_bytes(M, N, K), dtype=torch.uint8, device="cuda")
+        outs = [to_bits(lynx.lynx_linear(X, W, LA, LB, workspace=ws)) for _ in range(3)]
+        assert lynx.lynx_sync_status() == 0
+    finally:
+        lynx.lynx_debug_force_ksplit(0)
+        lynx.lynx_debug_force_tile(0, 0)
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+    rows = np.arange(0, M, 37)
+    Xh, Wh, LAh, LBh = (to_bits(a) for a in (X, W, LA, LB))
+    assert_y_close(outs[0][rows], O.linear(Xh[rows], Wh, LAh, LBh))
+
+
 def test_split_k_choice_and_workspace_fallback(lynx):
     """On this GPU a short, wide-K problem (256 tokens through the MLP down shape: 16 tiles of 256 x 192) splits;
     the DiT shapes do not (the MLP down shape at 1024 tokens fills one wave with 64 tiles of 256 x 192).  A
