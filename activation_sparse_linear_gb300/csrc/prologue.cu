@@ -39,7 +39,9 @@ constexpr int P_ROWS = 128;                       // rows per CTA = TMEM lanes
 constexpr int P_NST = 7;                          // pipeline stages
 constexpr int P_WORKERS = 16;                     // selection warps: four threads per row
 constexpr int P_TPR = 32 * P_WORKERS / 128;       // threads per row (16 of each stage's 64 channels each)
-constexpr int P_THREADS = 64 + 32 * P_WORKERS;    // warp 0 TMA, warp 1 MMA, warps 2..17 selection
+constexpr int P_DRAIN0 = 2 + P_WORKERS;           // warps 18, 19: with warps 0 and 1, the T drain in cluster mode
+constexpr int P_THREADS = 64 + 32 * P_WORKERS + 64;  // warp 0 TMA, warp 1 MMA, warps 2..17 selection, 18..19 drain
+static_assert(P_DRAIN0 % 4 == 2, "warps 0, 1, 18, 19 cover the four TMEM lane quarters");
 static_assert(P_TPR == 4, "the selection code below assumes four threads per row");
 constexpr int P_XT = P_ROWS * 128;                // X tile: 128 rows x 64 channels (16 KiB)
 constexpr int P_LBT = kRankLB * 128;              // LB tile: 64 ranks x 64 channels (8 KiB)
@@ -112,6 +114,31 @@ __global__ void __launch_bounds__(P_THREADS, 1) prologue_kernel(const __grid_con
     o = r * a.split / P_ROWS;
     return sp * rmax + r - (P_ROWS * o + a.split - 1) / a.split;
   };
+  // Cluster mode: warp w of {0, 1, 18, 19} reads TMEM lane quarter w % 4 of X LB^T as soon as the last MMA has
+  // completed and stores its rows' shares into the owners' slots, while the selection warps still work on the
+  // last channel block; the CTA's start-up barrier phase is waited for first (every CTA of the cluster started).
+  auto push_t_shares = [&](bool ok) {
+    const int q = warp & 3;
+    bool got = ok && mbar_wait(acc_full, 0, a.ctl, SITE_P_ACC);
+    got = __all_sync(0xFFFFFFFFu, got);
+    cluster_wait();
+    if (!got) return;
+    tc_fence_after();
+    uint32_t t0[32], t1[32];
+    tc_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16), t0);
+    tc_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + 32, t1);
+    tc_wait_ld();
+    int o;
+    const int slot = owner_slot(q * 32 + lane, o);  // 272-byte rows
+    const uint32_t dst = mapa_shared(recv_t + slot * P_TSTRIDE, o);
+#pragma unroll
+    for (int v4 = 0; v4 < 16; ++v4) {
+      const uint32_t* src = v4 < 8 ? t0 + 4 * v4 : t1 + 4 * (v4 - 8);
+      st_cluster_f32x4(dst + 16 * v4, make_float4(__uint_as_float(src[0]), __uint_as_float(src[1]),
+                                                  __uint_as_float(src[2]), __uint_as_float(src[3])));
+    }
+  };
+  const bool drain_warp = LORA && a.split > 1 && (warp < 2 || warp >= P_DRAIN0);
   if (a.split > 1) cluster_arrive_relaxed();
   // The set-up above may overlap the previous kernel; nothing below touches global memory before it is done.
   pdl_launch_dependents();
@@ -145,6 +172,8 @@ __global__ void __launch_bounds__(P_THREADS, 1) prologue_kernel(const __grid_con
         if (n > 0) mbar_wait(&full[st], (n - 1) & 1, a.ctl, SITE_P_PRODUCER);
       }
     }
+    __syncwarp();
+    if (drain_warp) push_t_shares(true);
   } else if (warp == 1) {
     if (LORA && lane == 0) {
       // -------------------------------------------------------------- MMA issuer: T += X_tile LB_tile^T
@@ -168,6 +197,10 @@ __global__ void __launch_bounds__(P_THREADS, 1) prologue_kernel(const __grid_con
       tc_commit(acc_full);  // fires once every MMA issued above has completed
       mbar_wait(acc_full, 0, a.ctl, SITE_P_ACC);  // no MMA may still run when TMEM is released
     }
+    __syncwarp();
+    if (drain_warp) push_t_shares(true);
+  } else if (warp >= P_DRAIN0) {
+    if (drain_warp) push_t_shares(true);
   } else {
     // ---------------------------------------------------------------- selection warps
     // Warp sw (0..15) takes rows base + i and base + 8 + i (i = 0..3, base = 16 (sw / 2) + 4 (sw % 2)), four
@@ -245,9 +278,8 @@ __global__ void __launch_bounds__(P_THREADS, 1) prologue_kernel(const __grid_con
         st_cluster_f32x2(mapa_shared(&recv_n[slot], o), make_float2(sx, skept));
       }
     }
-    if (LORA) {
-      // s_sh complete (direct mode)
-      named_sync_workers();
+    if (LORA && a.split == 1) {
+      named_sync_workers();  // s_sh complete
       if (warp < 6) {
         // TMEM lane quarter q = warp % 4 holds rows 32 q .. 32 q + 31
         const int q = warp & 3;
@@ -260,39 +292,28 @@ __global__ void __launch_bounds__(P_THREADS, 1) prologue_kernel(const __grid_con
           tc_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + 32, t1);
           tc_wait_ld();
           const int trow = q * 32 + lane, grow = r0 + trow;
-          if (a.split == 1) {
-            if (grow < a.M) {
-              const float inv = 1.f / s_sh[trow];  // T' = T * (1 / s): one division per row
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.T) + static_cast<int64_t>(grow) * kRankLB);
+          if (grow < a.M) {
+            const float inv = 1.f / s_sh[trow];  // T' = T * (1 / s): one division per row
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.T) + static_cast<int64_t>(grow) * kRankLB);
 #pragma unroll
-              for (int v8 = 0; v8 < 8; ++v8) {
-                const uint32_t* src = v8 < 4 ? t0 + 8 * v8 : t1 + 8 * (v8 - 4);
-                uint32_t pk[4];
+            for (int v8 = 0; v8 < 8; ++v8) {
+              const uint32_t* src = v8 < 4 ? t0 + 8 * v8 : t1 + 8 * (v8 - 4);
+              uint32_t pk[4];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(src[2 * j]) * inv,
-                                                            __uint_as_float(src[2 * j + 1]) * inv);
-                  pk[j] = *reinterpret_cast<uint32_t*>(&b2);
-                }
-                dst[v8] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              for (int j = 0; j < 4; ++j) {
+                __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(src[2 * j]) * inv,
+                                                          __uint_as_float(src[2 * j + 1]) * inv);
+                pk[j] = *reinterpret_cast<uint32_t*>(&b2);
               }
-            }
-          } else {  // this CTA's share of row trow of X LB^T, into the owner's slot (272-byte rows)
-            int o;
-            const int slot = owner_slot(trow, o);
-            const uint32_t dst = mapa_shared(recv_t + slot * P_TSTRIDE, o);
-#pragma unroll
-            for (int v4 = 0; v4 < 16; ++v4) {
-              const uint32_t* src = v4 < 8 ? t0 + 4 * v4 : t1 + 4 * (v4 - 8);
-              st_cluster_f32x4(dst + 16 * v4, make_float4(__uint_as_float(src[0]), __uint_as_float(src[1]),
-                                                          __uint_as_float(src[2]), __uint_as_float(src[3])));
+              dst[v8] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
           }
         }
       }
     }
   }
-  if (a.split > 1 && warp < 2) cluster_wait();  // the producer and MMA warps' half of the start-up phase
+  // the start-up phase for the warps that have not waited for it above
+  if (a.split > 1 && (warp < 2 || warp >= P_DRAIN0) && !drain_warp) cluster_wait();
   tc_fence_before();
   __syncthreads();
   if (a.split > 1) {
