@@ -621,6 +621,52 @@ def main() -> int:
         del cs
     torch.cuda.empty_cache()
 
+    # The stream-K schedule (opt-in: lynx_debug_force_ksplit(LYNX_KSPLIT_STREAM)) against the automatic one at
+    # the stack's few-tile MLP-down shape (64 tiles of 256 x 192 for the CTA pairs), in alternating blocks of calls.
+    Ms, Ns, Ks = 1024, 3072, 12288
+    cs = [{"X": torch.randn((Ms, Ks), generator=gen, device=dev).to(torch.bfloat16),
+           "W": (torch.randn((Ns, Ks), generator=gen, device=dev) / Ks ** 0.5).to(torch.bfloat16),
+           "LA": (0.02 * torch.randn((Ns, R), generator=gen, device=dev)).to(torch.bfloat16),
+           "LB": (0.02 * torch.randn((R, Ks), generator=gen, device=dev)).to(torch.bfloat16),
+           "Y": torch.empty((Ms, Ns), dtype=torch.bfloat16, device=dev)} for _ in range(2)]
+    sched = {}
+    for mode in (0, asl.LYNX_KSPLIT_STREAM):
+        asl.lynx_debug_force_ksplit(mode)
+        sched[mode] = (asl.lynx_debug_linear_ksplit(Ms, Ns, Ks),
+                       torch.empty(asl.lynx_workspace_bytes(Ms, Ns, Ks, R), dtype=torch.uint8, device=dev))
+    sk_ms = {0: [], asl.LYNX_KSPLIT_STREAM: []}
+    try:
+        for blk in range(5):
+            for mode in (0, asl.LYNX_KSPLIT_STREAM):
+                asl.lynx_debug_force_ksplit(mode)
+                ws_m = sched[mode][1]
+
+                def one_sk(c):
+                    return L.lynx_linear(c["X"].data_ptr(), c["W"].data_ptr(), c["LA"].data_ptr(),
+                                         c["LB"].data_ptr(), c["Y"].data_ptr(), Ms, Ns, Ks, R, ws_m.data_ptr(),
+                                         ws_m.numel(), sp)
+                for i in range(3):
+                    one_sk(cs[i % 2])
+                a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a0.record(stream)
+                for i in range(20):
+                    one_sk(cs[i % 2])
+                a1.record(stream)
+                torch.cuda.synchronize()
+                sk_ms[mode].append(a0.elapsed_time(a1) / 20)
+    finally:
+        asl.lynx_debug_force_ksplit(0)
+    st = asl.lynx_sync_status()
+    assert st == 0, asl.lynx_status_string(st)
+    stream_k = {"shape": "1024x12288->3072 (256 x 192 tiles)",
+                "auto_schedule": sched[0][0], "auto_ms": statistics.median(sk_ms[0]),
+                "stream_k_schedule": sched[asl.LYNX_KSPLIT_STREAM][0],
+                "stream_k_ms": statistics.median(sk_ms[asl.LYNX_KSPLIT_STREAM]),
+                "note": "whole lynx_linear calls, median of 5 alternating blocks of 20; stream-K is opt-in because "
+                        "it measured slower"}
+    del cs, sched
+    torch.cuda.empty_cache()
+
     # The sparsify pass alone (lynx_sparsify, and lynx_sparsify_lora with the LoRA down-projection), back to back
     # on inputs rotated over copies larger than L2: algorithmic bytes per call / time against the HBM peak, at
     # the QKV input and at the largest activations of the workloads (the CFG batch's MLP-down input and the
@@ -875,6 +921,7 @@ def main() -> int:
                                           "pattern of each dense X tile in its epilogue warps (256 x 256 tiles); "
                                           "every column tile repeats its rows' selection"},
             "other_shapes": shapes,
+            "stream_k": stream_k,
             "sparsify_alone": sparsify_alone,
             "block_stack_32_linears": stack,
             "mlp_pair": mlp_pair,

@@ -1,12 +1,15 @@
 """Shared test helpers: moving bf16 bit arrays between numpy and torch, and the
 floating-point acceptance check for Y.
 
-Tolerances for Y: relative Frobenius error <= 5e-3 and max |error| <=
-2e-2 * rms(Y_ref).  Rounding of the bf16 output alone costs up to 2^-9 |y|,
-i.e. about 0.012 rms at the largest |y| (~6 rms) of a multi-million-entry
-Gaussian-like output, which fits inside the max-abs bound; fp32 accumulation
-over K <= 12288 and the bf16 rounding of the M x 64 LoRA intermediate add
-far less than 5e-3 to the Frobenius error.
+Tolerances for Y: relative Frobenius error <= 5e-3 and, per element,
+|error| <= 2e-2 * rms(Y_ref) + half a bf16 unit in the last place of y_ref.
+The max-abs bound is the arithmetic's; the second term is the rounding of the
+bf16 output itself.  bf16 keeps 8 significant bits, so storing y moves it by
+up to 2^-8 |y| (an element just above a power of two); at the largest |y| of
+a multi-million-entry Gaussian-like output (~6 rms) that is up to 0.023 rms,
+more than 2e-2 rms: the exact result rounded to bf16 could fail the bound
+alone.  fp32 accumulation over K <= 12288 and the bf16 rounding of the M x 64
+LoRA intermediate add far less than 5e-3 to the Frobenius error.
 """
 from __future__ import annotations
 
@@ -32,23 +35,32 @@ def widen(bits: np.ndarray) -> np.ndarray:
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
+def half_ulp_bf16(v: np.ndarray) -> np.ndarray:
+    """Half a bf16 unit in the last place at |v|: the largest change storing v in bf16 makes (8 significant
+    bits: 2^(floor(log2 |v|) - 8)); normal range."""
+    a = np.maximum(np.abs(v), 2.0 ** -126)
+    return np.exp2(np.floor(np.log2(a)) - 8)
+
+
 def y_stats(y: np.ndarray, ref: np.ndarray) -> dict:
     err = y - ref
     rms = float(np.sqrt(np.mean(ref * ref)))
     fro = float(np.linalg.norm(err) / max(np.linalg.norm(ref), 1e-300))
     mx = float(np.max(np.abs(err))) if err.size else 0.0
+    bound = MAX_ABS_RMS * rms + half_ulp_bf16(ref)
+    worst = float(np.max(np.abs(err) / bound)) if err.size else 0.0
     cos = float(np.sum(y * ref) / max(np.linalg.norm(y) * np.linalg.norm(ref), 1e-300))
-    return {"rel_fro": fro, "max_abs_over_rms": mx / max(rms, 1e-300), "cosine": cos,
+    return {"rel_fro": fro, "max_abs_over_rms": mx / max(rms, 1e-300), "max_abs_over_bound": worst, "cosine": cos,
             "nonfinite": int(np.count_nonzero(~np.isfinite(y)))}
 
 
 def assert_y_close(y_bits: np.ndarray, ref: np.ndarray, what: str = "Y") -> dict:
-    """Relative Frobenius error <= 5e-3 and max |err| <= 2e-2 rms(Y_ref)."""
+    """Relative Frobenius error <= 5e-3 and, per element, |err| <= 2e-2 rms(Y_ref) + half a bf16 ulp of y_ref."""
     y = widen(y_bits)
     st = y_stats(y, ref)
     assert st["nonfinite"] == 0, (what, st)
     assert st["rel_fro"] <= REL_FRO, (what, st)
-    assert st["max_abs_over_rms"] <= MAX_ABS_RMS, (what, st)
+    assert st["max_abs_over_bound"] <= 1.0, (what, st)
     return st
 
 

@@ -113,6 +113,22 @@ def test_fused_pair_sparse_up(lynx, M, K, Nup, Nd, tile):
         lynx.lynx_debug_force_tile(0, 0)
 
 
+def test_fused_pair_down_stream_k(lynx):
+    """The fused pair with the down layer's GEMM on the stream-K schedule (forced; 256 x 192 tiles: 3 x 16 = 48
+    tiles of 8 k-steps on the CTA pairs): its partials and arrival counters in the pair's workspace plan."""
+    M, K, Nup, Nd = 600, 384, 1024, 3072
+    t = _mlp_tensors(M, K, Nup, Nd, seed=43)
+    lynx.lynx_debug_force_tile(256, 192)
+    lynx.lynx_debug_force_ksplit(lynx.LYNX_KSPLIT_STREAM)
+    try:
+        assert lynx.lynx_debug_linear_ksplit(M, Nd, Nup) == lynx.LYNX_KSPLIT_STREAM
+        layers, ws = _run_pair(lynx, *t, up_sparse=True)
+        _check_pair(lynx, layers, ws, *t, up_sparse=True)
+    finally:
+        lynx.lynx_debug_force_ksplit(0)
+        lynx.lynx_debug_force_tile(0, 0)
+
+
 @pytest.mark.parametrize("tile", [256, 448])
 @pytest.mark.parametrize("M,K,Nup,Nd", [(300, 256, 512, 200), (1, 128, 256, 64), (640, 512, 1024, 3072)])
 def test_fused_pair_dense_up(lynx, M, K, Nup, Nd, tile):
