@@ -262,7 +262,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   // last unit of a tile to finish adds the S partials in split order (see the epilogue).
   const int S = SPLIT ? a.splits : 1;
   const bool streamk = SPLIT && a.stream_k != 0;  // stream-K: S is the partials' stride, kPairMaxSplit
-  const bool krot = SPARSE && MB == 2 && !TRANS && !SPLIT && !F1 && nk <= 32;  // staggered k order (producer)
+  const bool krot = SPARSE && MB == 2 && !TRANS && !SPLIT && !F1;  // staggered k order (producer)
   const int64_t blocks_k = meta_blocks_k(a.K);
   const int meta_rowblocks = static_cast<int>(round_up(a.M, kMetaRowPad) / kMetaRows);
 
@@ -340,12 +340,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           if (rb >= meta_rowblocks) rb = meta_rowblocks - 1;  // rows past the padded M: never stored
           meta_row[h] = static_cast<int>(2 * (rb * blocks_k));
         }
-        // Staggered k order: the pairs of one W column tile would otherwise load each W slice at the same moment
-        // and all wait for the same DRAM fetch; starting pair mp at k-step mp nk_u / num_mp lets one pair's load
-        // bring each slice into L2 for the others.  Only where that measured faster: sparse two-row-block tiles
-        // of at most 32 k-steps (QKV and MLP up -4 to -6%); with long K (MLP down) the whole W tile would have
-        // to stay in L2 beside the values, and the one-row-block tiles measured slower.
-        const int nk_u = kend - kbeg, rot = krot ? (mp * nk_u) / num_mp : 0;
+        // Staggered k order: the pairs that share a W column tile (same nb) or a row tile (same mp) would
+        // otherwise load the same slice at the same moment and all wait for one DRAM fetch.  Pair (mp, nb) starts
+        // at offset (mp + nb) mod G of G = min(8, row tiles) steps spread over at most 24 k-steps, so one pair's
+        // load brings each slice into L2 for the others; the window bounds how long a slice has to stay there.
+        // Measured on the sparse two-row-block tiles (QKV and MLP up -4 to -5%, MLP down -2%, M = 16384 -3%);
+        // the one-row-block tiles measured slower and keep the plain order.
+        const int nk_u = kend - kbeg, G = num_mp < 8 ? num_mp : 8;
+        const int rot = krot ? (((mp + nb) % G) * (nk_u < 24 ? nk_u : 24)) / G : 0;
         for (int it = 0; it < nst_u; ++it) {
           const int kk = it < nk_u ? kbeg + (it + rot) % nk_u : kbeg + it;
           if (!__all_sync(0xFFFFFFFFu, mbar_wait(&empty[st], ph ^ 1, a.ctl, SITE_PRODUCER)) || *abort_flag) {
