@@ -366,9 +366,9 @@ int linear_impl(const void* X, const void* W, const void* LA, const void* LB, vo
 
   ProArgs pa;
   if (int e = make_prologue(&pa, X, LB, M, K, ws.vals, ws.meta, ws.s, ws.T)) return e;
-  if (splits > 1) {  // the pre-pass zeroes the GEMM's arrival counters
+  if (splits > 1) {  // the pre-pass zeroes the GEMM's arrival counters: the whole counter block split_bytes sized
     pa.zero = g.counters;
-    pa.nzero = static_cast<int>(((M + 255) / 256) * ((N + shape.tn - 1) / shape.tn) * 2);
+    pa.nzero = static_cast<int>((split_bytes(shape, M, N, splits) - counters_off) / 4);
   }
   if (cudaError_t e = prof.mark(0, st)) return cuda_status(e);
   if (cudaError_t e = launch_prologue(pa, true, st)) return cuda_status(e);
