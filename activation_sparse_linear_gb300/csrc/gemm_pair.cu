@@ -344,7 +344,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         // otherwise load the same slice at the same moment and all wait for one DRAM fetch.  Pair (mp, nb) starts
         // at offset (mp + nb) mod G of G = min(8, row tiles) steps spread over at most 24 k-steps, so one pair's
         // load brings each slice into L2 for the others; the window bounds how long a slice has to stay there.
-        // Measured on the sparse two-row-block tiles (QKV and MLP up -4 to -5%, MLP down -2%, M = 16384 -3%);
+        // Measured on the sparse two-row-block tiles (QKV and MLP up -3 to -5%, MLP down -2%, M = 16384 -3%);
         // the one-row-block tiles measured slower and keep the plain order.
         const int nk_u = kend - kbeg, G = num_mp < 8 ? num_mp : 8;
         const int rot = krot ? (((mp + nb) % G) * (nk_u < 24 ? nk_u : 24)) / G : 0;
