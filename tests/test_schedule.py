@@ -64,3 +64,31 @@ def test_fewer_tiles_than_half_the_pairs_can_need_more_parts():
     P, tiles, nk = 76, 8, 96
     most = max(nparts for c in range(P) for *_, nparts in units(c, P, tiles, nk))
     assert most > 4
+
+
+def stagger(mp, nb, num_mp, nk_u):
+    """The producer's staggered k order for a two-row-block tile: pair (mp, nb) starts at offset
+    ((mp + nb) mod G) * min(nk_u, 24) / G, G = min(8, num_mp), and wraps around."""
+    G = min(8, num_mp)
+    rot = ((mp + nb) % G) * min(nk_u, 24) // G
+    return [(it + rot) % nk_u for it in range(nk_u)], rot
+
+
+def test_stagger_is_a_permutation_of_the_unit_steps():
+    for num_mp in (1, 2, 3, 8, 9, 32):
+        for nk_u in (1, 2, 7, 24, 25, 96):
+            for mp in range(num_mp):
+                for nb in range(10):
+                    order, rot = stagger(mp, nb, num_mp, nk_u)
+                    assert 0 <= rot < nk_u or nk_u == 1 and rot == 0
+                    assert sorted(order) == list(range(nk_u))
+
+
+def test_stagger_separates_the_pairs_that_share_a_column_tile():
+    """The pairs of one W column tile (same nb, consecutive mp) start on different k-steps when there are up to
+    eight of them and at least eight steps."""
+    for num_mp in (2, 4, 8, 9, 36):
+        for nk_u in (8, 24, 96):
+            for nb in range(5):
+                starts = [stagger(mp, nb, num_mp, nk_u)[1] for mp in range(min(num_mp, 8))]
+                assert len(set(starts)) == len(starts)
